@@ -1,0 +1,276 @@
+"""The canvas sampler step in plain fp64 NumPy -- test infrastructure only.
+
+One step over a batch of canvases (B sequences, L positions, vocabulary V, width d):
+
+1. logits      z_ij = H_i . E_j                   (technical report s.6 "Sampling": the
+                                                    softmax runs over the full vocabulary)
+2. temperature y_ij = z_ij / T_b
+3. softmax     p_ij = exp(y_ij - m_i) / l_i,  m_i = max_j y_ij,  l_i = sum_j exp(y_ij - m_i)
+               entropy_i = -sum_j p_ij ln p_ij (nats); argmax_i = lowest j with y_ij = m_i
+4. self-cond.  s_i = sum_j p_ij E_j               (s.6 "Sampling": "self-conditioning
+                                                    embedding matmul"; s.8: fed back as z_t)
+5. sample      Gumbel-max: x_i = argmax_j (y_ij + g_ij), g_ij = -ln(-ln u_ij), lowest j on
+               ties; with top-k the argmax runs over the k largest y_ij only (s.6
+               "Multi-user throughput": top-k applies to the sampling step). The
+               confidence c_i is the probability of x_i under the distribution sampled from.
+6. lock / re-noise / stop (sokufu.com "A diffusion language model refines 256 tokens in 12
+               steps"; alphasignal "How text diffusion actually works"; see lock_update).
+
+The pages print no sampler listing; the readings taken where they are silent:
+
+* confidence threshold: a position is locked when c_i >= tau_b;
+* at least one lock per step: if no unlocked position passes, the unlocked position with
+  the largest c_i (lowest i on ties) is locked;
+* locks are sticky: a locked position keeps its token for the rest of the canvas;
+* the last allowed step (step + 1 == max_steps) locks every remaining position with x_i;
+* unlocked positions are re-noised with a fresh uniform token;
+* a sequence is done when every position is locked; done sequences are left untouched;
+* temperature divides the logits for the softmax, the entropy, s and the sample alike;
+* top-k keeps s and the entropy on the full softmax;
+* random draws come from Philox4x32-10 keyed by the seed (low, high word), with counters
+    Gumbel  (j >> 2, i, b, 4*step + 0), word j & 3, u = (2*(r >> 9) + 1) / 2**24,
+    re-noise (i >> 2, 0, b, 4*step + 1), word i & 3, token = (r * V) >> 32.
+  u takes 2**23 values, symmetric in (0, 1) and exactly representable in fp32; the token
+  map is exactly uniform when V is a power of two.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .philox import philox4x32_10, seed_key
+
+GUMBEL_STREAM = 0
+RENOISE_STREAM = 1
+
+
+# --------------------------------------------------------------------------------------
+# number formats
+# --------------------------------------------------------------------------------------
+
+def bf16_bits_to_f64(b) -> np.ndarray:
+    """Exact value of bf16 bit patterns (uint16)."""
+    u = np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return u.view(np.float32).astype(np.float64)
+
+
+def f64_to_bf16_bits(x) -> np.ndarray:
+    """Round fp64 values to the nearest bf16, ties to even (one rounding, from fp64).
+
+    The fp32 conversion is exact to within half an fp32 ulp, so it can only mislead the
+    bf16 rounding when it lands exactly on a bf16 midpoint; that case is decided from the
+    fp64 value itself."""
+    x = np.asarray(x, dtype=np.float64)
+    f = x.astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    low = u & np.uint64(0xFFFF)
+    base = u >> np.uint64(16)
+    up = (low > 0x8000) | ((low == 0x8000) & ((base & np.uint64(1)) == 1))
+    f64 = f.astype(np.float64)
+    midpoint_hazard = (low == 0x8000) & (f64 != x)
+    up = np.where(midpoint_hazard, np.abs(x) > np.abs(f64), up)
+    return (base + up.astype(np.uint64)).astype(np.uint16)
+
+
+# --------------------------------------------------------------------------------------
+# random draws
+# --------------------------------------------------------------------------------------
+
+def gumbel_uniforms(seed: int, b: int, positions, step: int, V: int) -> np.ndarray:
+    """u_ij in (0, 1) for positions i (array) and all tokens j < V, shape [len(i), V]."""
+    positions = np.asarray(positions, dtype=np.int64)
+    nblk = (V + 3) // 4
+    c0 = np.arange(nblk, dtype=np.uint64)[None, :]
+    c1 = positions.astype(np.uint64)[:, None]
+    c3 = np.uint64(4 * int(step) + GUMBEL_STREAM)
+    words = philox4x32_10(c0, c1, np.uint64(b), c3, seed_key(seed))  # [n, nblk, 4]
+    r = words.reshape(len(positions), 4 * nblk)[:, :V].astype(np.float64)
+    return (2.0 * np.floor(r / 512.0) + 1.0) / 16777216.0
+
+
+def renoise_tokens(seed: int, b: int, positions, step: int, V: int) -> np.ndarray:
+    """Uniform replacement tokens for positions i of sequence b at a step."""
+    positions = np.asarray(positions, dtype=np.int64)
+    c0 = (positions >> 2).astype(np.uint64)
+    c3 = np.uint64(4 * int(step) + RENOISE_STREAM)
+    words = philox4x32_10(c0, np.uint64(0), np.uint64(b), c3, seed_key(seed))
+    r = words[np.arange(len(positions)), positions & 3].astype(np.uint64)
+    return ((r * np.uint64(V)) >> np.uint64(32)).astype(np.int32)
+
+
+# --------------------------------------------------------------------------------------
+# the step
+# --------------------------------------------------------------------------------------
+
+def softmax_stats(y: np.ndarray):
+    """Row-wise softmax of y [n, V]: (m, l, p, entropy, argmax)."""
+    m = y.max(axis=1)
+    e = np.exp(y - m[:, None])
+    l = e.sum(axis=1)
+    p = e / l[:, None]
+    plogp = np.where(p > 0.0, p * np.log(np.where(p > 0.0, p, 1.0)), 0.0)
+    entropy = -plogp.sum(axis=1)
+    argmax = y.argmax(axis=1)  # numpy returns the first (lowest j) maximum
+    return m, l, p, entropy, argmax
+
+
+def _top_k_set(y_row: np.ndarray, k: int) -> np.ndarray:
+    """Indices of the k largest values; among equal values the lower index is kept."""
+    order = np.argsort(-y_row, kind="stable")
+    return np.sort(order[:k])
+
+
+def _sample_row(y_row, g_row, p_row, top_k):
+    """Gumbel-max over the row (or its top-k set): (x, c, margin of the top two)."""
+    if top_k and top_k < y_row.shape[0]:
+        cand = _top_k_set(y_row, top_k)
+        v = y_row[cand] + g_row[cand]
+        best = int(np.argmax(v))
+        x = int(cand[best])
+        w = np.exp(y_row[cand] - y_row[cand].max())
+        c = float(w[best] / w.sum())
+        vs = np.sort(v)
+    else:
+        v = y_row + g_row
+        x = int(np.argmax(v))
+        c = float(p_row[x])
+        vs = np.partition(v, -2)[-2:] if v.shape[0] > 1 else np.array([-np.inf, v[0]])
+        vs = np.sort(vs)
+    margin = float(vs[-1] - vs[-2]) if vs.shape[0] > 1 else np.inf
+    return x, c, margin
+
+
+def sampler_step(H, E, T, tau, canvas, lock, step, done, seed, *, top_k=0, max_steps=48,
+                 positions=None, row_chunk=64):
+    """One sampler step over a batch, in fp64.
+
+    H [B, L, d] and E [V, d] are the exact input values as float64 (bf16 or fp32 inputs
+    convert exactly); T, tau [B]; canvas [B, L] int; lock [B, L] 0/1; step [B]; done [B].
+
+    Returns a dict of the outputs for active sequences (done ones keep NaN / -1 outputs and
+    unchanged state): s [B, L, d], sampled, conf, entropy, argmax, pmax (= 1 / l_i), and the
+    updated canvas, lock, step, done, plus diagnostics used to exclude near-ties from exact
+    comparisons: gumbel_margin (top-two perturbed logits) and top-k boundary gaps.
+
+    With ``positions`` set, only those positions are computed and the lock update is
+    skipped (it needs the whole canvas)."""
+    H = np.asarray(H, dtype=np.float64)
+    E = np.asarray(E, dtype=np.float64)
+    B, L, d = H.shape
+    V = E.shape[0]
+    pos = np.arange(L) if positions is None else np.asarray(positions, dtype=np.int64)
+    out = {
+        "s": np.full((B, L, d), np.nan),
+        "sampled": np.full((B, L), -1, np.int64),
+        "conf": np.full((B, L), np.nan),
+        "entropy": np.full((B, L), np.nan),
+        "argmax": np.full((B, L), -1, np.int64),
+        "pmax": np.full((B, L), np.nan),
+        "gumbel_margin": np.full((B, L), np.inf),
+        "topk_gap": np.full((B, L), np.inf),
+    }
+    for b in range(B):
+        if done[b]:
+            continue
+        for c0 in range(0, len(pos), row_chunk):
+            rows = pos[c0:c0 + row_chunk]
+            y = (H[b, rows] @ E.T) / float(T[b])
+            m, l, p, ent, am = softmax_stats(y)
+            out["s"][b, rows] = p @ E
+            out["entropy"][b, rows] = ent
+            out["argmax"][b, rows] = am
+            out["pmax"][b, rows] = 1.0 / l
+            u = gumbel_uniforms(seed, b, rows, int(step[b]), V)
+            g = -np.log(-np.log(u))
+            for r, i in enumerate(rows):
+                x, c, margin = _sample_row(y[r], g[r], p[r], top_k)
+                out["sampled"][b, i] = x
+                out["conf"][b, i] = c
+                out["gumbel_margin"][b, i] = margin
+                if top_k and top_k < V:
+                    ys = np.sort(y[r])
+                    out["topk_gap"][b, i] = ys[-top_k] - ys[-top_k - 1]
+    new = {k: np.array(v, copy=True) for k, v in
+           (("canvas", canvas), ("lock", lock), ("step", step), ("done", done))}
+    if positions is None:
+        for b in range(B):
+            if done[b]:
+                continue
+            cv, lk, st, dn = lock_update(new["canvas"][b], new["lock"][b], out["sampled"][b],
+                                         out["conf"][b], float(tau[b]), int(step[b]), seed, b,
+                                         V, max_steps)
+            new["canvas"][b], new["lock"][b], new["step"][b], new["done"][b] = cv, lk, st, dn
+    out.update(new)
+    return out
+
+
+def lock_update(canvas_b, lock_b, sampled_b, conf_b, tau_b, step_b, seed, b, V, max_steps):
+    """Lock confident positions, re-noise the others, advance the step; one sequence.
+
+    Returns (canvas, lock, step, done) after the step."""
+    canvas_b = np.array(canvas_b, copy=True)
+    lock_b = np.array(lock_b, copy=True).astype(np.uint8)
+    L = lock_b.shape[0]
+    unlocked = lock_b == 0
+    if step_b + 1 >= max_steps:
+        newly = unlocked.copy()
+    else:
+        newly = unlocked & (np.asarray(conf_b) >= tau_b)
+        if not newly.any() and unlocked.any():
+            cand = np.where(unlocked, conf_b, -np.inf)
+            newly[int(np.argmax(cand))] = True  # first maximum: lowest position
+    canvas_b[newly] = np.asarray(sampled_b)[newly]
+    lock_b[newly] = 1
+    still = np.nonzero(lock_b == 0)[0]
+    if still.size:
+        canvas_b[still] = renoise_tokens(seed, b, still, step_b, V)
+    done = 1 if (lock_b == 1).all() else 0
+    return canvas_b, lock_b, step_b + 1, done
+
+
+# --------------------------------------------------------------------------------------
+# the hidden-state stand-in and the loop
+# --------------------------------------------------------------------------------------
+
+def standin_hidden(W_bits, s_prev, E, canvas):
+    """H = bf16(tanh(W . [bf16(s_prev); E[x]])) per position, as bf16 bits [B, L, d].
+
+    A stand-in for the model's decoder, which the pages do not give: it feeds the
+    self-conditioning vector of the previous step (report s.8, z_t) and the current canvas
+    tokens back into the next step's hidden state."""
+    W = bf16_bits_to_f64(W_bits)  # [d, 2d]
+    s_prev = np.asarray(s_prev, dtype=np.float64)
+    E = np.asarray(E, dtype=np.float64)
+    s_b = bf16_bits_to_f64(f64_to_bf16_bits(s_prev))
+    u = np.concatenate([s_b, E[np.asarray(canvas)]], axis=-1)  # [B, L, 2d]
+    return f64_to_bf16_bits(np.tanh(u @ W.T))
+
+
+def denoise_loop(E, T, tau, canvas, lock, step, done, seed, *, H=None, W_bits=None,
+                 s_prev=None, top_k=0, max_steps=48, max_iters=None):
+    """Run steps until every sequence is done (or max_iters); returns the per-step records.
+
+    Fixed-H mode passes H (fp64 [B, L, d]); stand-in mode passes W_bits and recomputes H
+    from the previous s (zero at the start) and the canvas before each step."""
+    E = np.asarray(E, dtype=np.float64)
+    B, L = np.asarray(canvas).shape
+    d = E.shape[1]
+    state = {"canvas": np.array(canvas), "lock": np.array(lock), "step": np.array(step),
+             "done": np.array(done),
+             "s": np.zeros((B, L, d)) if s_prev is None else np.array(s_prev, np.float64)}
+    records = []
+    iters = max_steps if max_iters is None else max_iters
+    for _ in range(iters):
+        if state["done"].all():
+            break
+        Hs = H if W_bits is None else bf16_bits_to_f64(
+            standin_hidden(W_bits, state["s"], E, state["canvas"]))
+        out = sampler_step(Hs, E, T, tau, state["canvas"], state["lock"], state["step"],
+                           state["done"], seed, top_k=top_k, max_steps=max_steps)
+        out["H"] = Hs
+        active = state["done"] == 0
+        s_new = state["s"].copy()
+        s_new[active] = out["s"][active]
+        state = {"canvas": out["canvas"], "lock": out["lock"], "step": out["step"],
+                 "done": out["done"], "s": s_new}
+        records.append(out)
+    return state, records
