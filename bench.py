@@ -1,0 +1,377 @@
+#!/usr/bin/env python
+"""Benchmark of the canvas sampler step on GB300.
+
+One step = one pass of the whole per-step hot path over one batch of synthetic canvases:
+logits GEMM, softmax statistics, exp(y - m) split + Gumbel-max, self-conditioning GEMM, the
+reduction of s, the sampled tokens and confidences, and the lock / re-noise / stop update.
+The default workload is one B=1 canvas of 256 positions over a 262,144-token vocabulary at
+d = 2816 (the shapes of the DiffusionGemma pages; synthetic data).
+
+    python bench.py [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Prints one JSON line. Under torchrun every rank runs its own canvas on its own GPU (weak
+scaling, no data-path collective); the timed region is bracketed by barriers and the slowest
+rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from canvas_sampler_gb300 import workloads as W  # noqa: E402
+
+METRIC = "canvas sampler steps/s & TFLOP/s (B=1, 256×262144 vocab) vs roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_FILE = os.path.join(ROOT, "profiles", "selfcond_tc_step_v262144_d2816.md")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=W.BENCH_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--kernel-impl", default="auto", choices=["auto", "tensor", "simt"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-positions", type=int, default=32,
+                    help="canvas positions in the oracle's timed sample")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------ helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock / throttle reasons during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "-i", str(self.gpu),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_traffic(kernel_src: str):
+    """DRAM bytes per launch of the self-conditioning kernel from the committed ncu summary,
+    if the kernel source has not changed since the capture (else None)."""
+    try:
+        text = open(PROFILE_FILE).read()
+    except OSError:
+        return None
+    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    if not (m_b and m_h):
+        return None
+    h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    return float(m_b.group(1)) if h == m_h.group(1) else None
+
+
+def algorithmic_flops(w: W.Workload) -> float:
+    return 4.0 * w.B * w.L * w.V * w.d
+
+
+# ------------------------------------------------------------------------------ oracle timing
+
+def oracle_sample_seconds(w, inp, E64, positions, reps=1):
+    import oracle
+    H64 = oracle.bf16_bits_to_f64(inp["H"]) if w.dtype == "bf16" else inp["H"].astype(np.float64)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.sampler_step(H64, E64, inp["T"], inp["tau"], inp["canvas"], inp["lock"], inp["step"],
+                            inp["done"], inp["seed"], top_k=w.top_k, max_steps=w.max_steps,
+                            positions=positions)
+    return (time.perf_counter() - t0) / reps
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = W.WORKLOADS[args.workload]
+    inp = W.make_inputs(w)
+    import oracle
+    E64 = oracle.bf16_bits_to_f64(inp["E"]) if w.dtype == "bf16" else inp["E"].astype(np.float64)
+    n = max(1, min(w.L, 4))
+    pos = np.arange(n)
+    for _ in range(args.warmup):
+        oracle_sample_seconds(w, inp, E64, pos)
+    t = [oracle_sample_seconds(w, inp, E64, pos) for _ in range(args.steps)]
+    sec_per_step = float(np.mean(t)) * (w.L / n) * w.B
+    value = 1.0 / sec_per_step
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec_per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "L": w.L, "V": w.V, "d": w.d},
+        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"each step: the fp64 oracle over {n} of {w.L} canvas positions "
+                                   f"(full vocabulary) x {w.B} sequence(s), scaled by "
+                                   f"{w.L // n * w.B}"},
+        "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "tflops": algorithmic_flops(w) / sec_per_step / 1e12,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from canvas_sampler_gb300.sampler import CanvasState, Sampler, StepOutputs
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.WORKLOADS[args.workload]
+    inp = W.make_inputs(w)
+    seed = inp["seed"] + rank  # each rank samples its own canvas
+
+    def upload(a):
+        if w.dtype == "fp32":
+            return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    E = upload(inp["E"])
+    H = upload(inp["H"]) if inp["H"] is not None else None
+    if H is None:  # stand-in workloads: time the step on the first stand-in hidden state
+        raise SystemExit("bench times fixed-H workloads; stand-in loops are covered by the tests")
+    T = torch.from_numpy(inp["T"]).to(dev)
+    tau = torch.from_numpy(inp["tau"]).to(dev)
+    sampler = Sampler(w.V, w.d, canvas_len=w.L, max_batch=w.B, dtype=w.dtype, top_k=w.top_k,
+                      max_steps=w.max_steps, impl=args.kernel_impl)
+    B, L = w.B, w.L
+    # state in one byte buffer so that one copy resets it before every step (every sequence
+    # stays active, so every step does the full work)
+    nb = B * L * 4 + B * 4 + B * L + B
+    pristine = torch.zeros(nb, dtype=torch.uint8, device=dev)
+    buf = torch.zeros(nb, dtype=torch.uint8, device=dev)
+
+    def views(t):
+        o = 0
+        cv = t[o:o + B * L * 4].view(torch.int32).view(B, L); o += B * L * 4
+        st = t[o:o + B * 4].view(torch.int32); o += B * 4
+        lk = t[o:o + B * L].view(B, L); o += B * L
+        dn = t[o:o + B]
+        return CanvasState(cv, lk, st, dn)
+
+    p = views(pristine)
+    p.canvas.copy_(torch.from_numpy(inp["canvas"]))
+    state = views(buf)
+    out = StepOutputs.empty(B, L, w.d, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def one_step():
+        buf.copy_(pristine)
+        sampler.step(H, E, T, tau, state, seed, out=out, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        one_step()
+    torch.cuda.synchronize()
+    assert sampler.device_status() == 0
+    if world > 1:
+        dist.barrier()
+    clocks = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                          int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = sampler.launch_count
+    sampler.set_phase_timing(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        one_step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    phases, nsteps = sampler.phase_times()
+    sampler.set_phase_timing(False)
+    launches = sampler.launch_count - launches0
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    status = sampler.device_status()
+
+    # end to end through the public API: pinned host buffers in, results back, every step
+    hs = CanvasState(torch.from_numpy(inp["canvas"].copy()).pin_memory(),
+                     torch.zeros(B, L, dtype=torch.uint8).pin_memory(),
+                     torch.zeros(B, dtype=torch.int32).pin_memory(),
+                     torch.zeros(B, dtype=torch.uint8).pin_memory())
+    hout = StepOutputs.empty(B, L, w.d, pin=True)
+    Hh = H.cpu().pin_memory()
+    Th, tauh = T.cpu().pin_memory(), tau.cpu().pin_memory()
+    h2d = Hh.numel() * Hh.element_size() + 2 * B * 4 + hs.canvas.numel() * 4 + B * L + B * 4 + B
+    d2h = sum(t.numel() * t.element_size() for t in vars(hout).values()) + B * L * 4 + B * L + B * 4 + B
+    for _ in range(2):
+        sampler.step_host(Hh, E, Th, tauh, hs, seed, hout, stream=stream)
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        hs.lock.zero_(); hs.done.zero_(); hs.step.zero_()
+        sampler.step_host(Hh, E, Th, tauh, hs, seed, hout, stream=stream)
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    step_s = ms / 1e3 / args.steps
+    value = world * args.steps / (ms / 1e3)
+    flops = algorithmic_flops(w)
+    peaks, peak_src = load_peaks()
+    # dominant kernel: the self-conditioning GEMM (tensor cores); algorithmic work per launch is
+    # 2 B L V d (the bf16 hi/lo doubling of the tensor work is not algorithmic)
+    dom = max(phases, key=phases.get) if nsteps else "selfcond"
+    dom_ms = phases.get(dom, 0.0) / max(1, nsteps)
+    dom_flops = {"logits": 2.0 * w.B * w.L * w.V * w.d,
+                 "selfcond": 2.0 * w.B * w.L * w.V * w.d}.get(dom)
+    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    roof = None
+    if dom_flops and dom_ms > 0:
+        ach = dom_flops / (dom_ms / 1e3) / 1e12
+        traffic = measured_traffic(os.path.join(ROOT, "canvas_sampler_gb300", "csrc", "ds_tc.cu"))
+        roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak_tf,
+                "unit": "TFLOP/s", "frac": ach / peak_tf, "traffic": traffic,
+                "peak_source": f"bf16_tflops ({peak_src}, burst)"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "L": w.L, "V": w.V, "d": w.d,
+                   "impl": sampler.impl, "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (E is %.2f GB); no flush" % (w.V * w.d * 2 / 1e9),
+                   "state_reset": "one device copy of the 2 KB canvas state before each step"},
+        "tflops": world * flops / step_s / 1e12,
+        "step_roofline": {"bound": "tensor", "achieved": flops / step_s / 1e12, "peak": peak_tf,
+                          "unit": "TFLOP/s", "frac": flops / step_s / 1e12 / peak_tf,
+                          "note": "4 B L V d algorithmic FLOP per step over the whole step"},
+        "roofline": roof,
+        "phase_ms_per_step": {k: v / max(1, nsteps) for k, v in phases.items()},
+        "gpu_launches": launches,
+        "e2e": {"value": world * args.e2e_steps / e2e_s, "unit": "steps/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "clocks": clk,
+        "device_status": status,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        E64 = oracle.bf16_bits_to_f64(inp["E"]) if w.dtype == "bf16" else inp["E"].astype(np.float64)
+        n = max(1, min(w.L, args.cpu_positions))
+        pos = np.arange(n)
+        sec = oracle_sample_seconds(w, inp, E64, pos)
+        sec_step = sec * (w.L / n) * w.B
+        line["cpu_baseline"] = {
+            "value": 1.0 / sec_step, "unit": "steps/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"fp64 oracle over {n} of {w.L} canvas positions (full vocabulary), "
+                      f"{sec:.1f} s, scaled by {w.L / n * w.B:g} to one step"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

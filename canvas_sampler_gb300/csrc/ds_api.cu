@@ -1,0 +1,567 @@
+// C ABI of the canvas sampler (include/ds_sampler.h): argument validation, the workspace, the
+// order of kernel launches in a step, the host-buffer variant and the CUDA-graph denoising loop.
+//
+// A step enqueues, on the caller's stream:
+//   logits GEMM (tensor cores or CUDA cores)  -> y [B*L, V] fp32
+//   chunk statistics, row merge               -> m, l, entropy, argmax per row
+//   [top-k candidates per chunk]
+//   exp(y - m) as bf16 hi/lo + chunk Gumbel-max
+//   self-conditioning GEMM over vocabulary splits -> O partials
+//   reduction s = sum(O) / l; finalize (sample, confidence)
+//   lock / re-noise / stop
+// The loop (report section 6, "Eliminating CPU-GPU synchronization") is one graph launch: a
+// while node whose condition the last kernel of each iteration sets from the done flags.
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/ds_sampler.h"
+#include "ds_internal.h"
+
+using namespace ds;
+
+namespace {
+
+struct LoopGraph {
+  ds_loop_args key;
+  int batch;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
+}  // namespace
+
+struct ds_sampler {
+  ds_sampler_config cfg{};
+  int device = 0;
+  int impl = DS_IMPL_SIMT;
+  int num_sms = 1;
+  int n_chunks = 1;
+  size_t ws_bytes = 0;
+  float* Y = nullptr;
+  uint16_t* Phi = nullptr;
+  uint16_t* Plo = nullptr;
+  ChunkStat* cs = nullptr;
+  RowStat* rs = nullptr;
+  Best* best = nullptr;
+  Cand* cand = nullptr;
+  float* Opart = nullptr;
+  size_t opart_floats = 0;
+  uint32_t* err = nullptr;
+  int32_t* iter = nullptr;
+  int last_batch = 0;
+  // device staging for ds_sampler_step_host (allocated on first use)
+  void* stage = nullptr;
+  size_t stage_bytes = 0;
+  cudaStream_t capture_stream = nullptr;
+  std::vector<LoopGraph> graphs;
+  std::vector<void*> allocations;
+  // phase timing (ds_sampler_set_phase_timing)
+  bool timing = false;
+  std::vector<cudaEvent_t> events;  // kPhaseEvents per timed step
+  int timed_steps = 0;
+  cudaStream_t timed_stream = nullptr;
+  int64_t launches = 0;
+};
+
+namespace {
+
+constexpr int kPhases = 7;
+constexpr int kPhaseEvents = kPhases + 1;
+
+// Event marking the end of `phase` (or the start of the step for phase -1) in the current
+// timed step; nullptr when timing is off.
+void mark(ds_sampler* s, int phase, cudaStream_t st) {
+  if (!s->timing) return;
+  const size_t need = (size_t)(s->timed_steps + 1) * kPhaseEvents;
+  while (s->events.size() < need) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      s->timing = false;
+      return;
+    }
+    s->events.push_back(e);
+  }
+  cudaEventRecord(s->events[(size_t)s->timed_steps * kPhaseEvents + (phase + 1)], st);
+}
+
+int esize(int dtype) { return dtype == DS_DTYPE_FP32 ? 4 : 2; }
+
+int splits_for(const ds_sampler* s, int batch) {
+  const int R = batch * s->cfg.canvas_len;
+  const int64_t V = s->cfg.vocab;
+  const int d = s->cfg.d_model;
+  if (s->impl == DS_IMPL_TENSOR) return selfcond_tc_splits(R, V, d, s->num_sms);
+  // CUDA-core GEMM: aim at about four waves of 128 x 64 tiles, >= 1024 tokens per split
+  const long tiles = (long)(d / 64) * (R / 128);
+  long S = (4L * s->num_sms + tiles - 1) / tiles;
+  S = std::max(1L, std::min(S, std::min(64L, (long)(V / 1024))));
+  return (int)std::max(1L, S);
+}
+
+ds_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return DS_OK;
+  if (e == cudaErrorMemoryAllocation) return DS_ERR_OOM;
+  return DS_ERR_CUDA;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+ds_status check_step_args(const ds_sampler* s, const ds_step_args* a) {
+  if (!a) return DS_ERR_INVALID_ARG;
+  if (a->batch < 1 || a->batch > s->cfg.max_batch) return DS_ERR_INVALID_ARG;
+  if (!a->H || !a->E || !a->temperature || !a->tau || !a->step || !a->canvas || !a->lock ||
+      !a->done || !a->s || !a->sampled || !a->conf || !a->entropy || !a->argmax)
+    return DS_ERR_INVALID_ARG;
+  if (!aligned(a->H, 16) || !aligned(a->E, 16) || !aligned(a->s, 16)) return DS_ERR_INVALID_ARG;
+  return DS_OK;
+}
+
+ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
+  const int L = s->cfg.canvas_len, d = s->cfg.d_model, B = a->batch;
+  const int64_t V = s->cfg.vocab;
+  const int R = B * L;
+  const bool fp32 = s->cfg.dtype == DS_DTYPE_FP32;
+  const int k = s->cfg.top_k;
+  const int S = splits_for(s, B);
+  s->last_batch = B;
+  mark(s, -1, st);
+  if (s->impl == DS_IMPL_TENSOR) {
+    cudaError_t e = launch_logits_tc(static_cast<const uint16_t*>(a->H),
+                                     static_cast<const uint16_t*>(a->E), R, V, d, L,
+                                     a->temperature, a->done, s->Y, s->err, st);
+    if (e != cudaSuccess) return cuda_status(e);
+  } else {
+    launch_logits_simt(a->H, a->E, fp32, R, V, d, L, a->temperature, a->done, s->Y, st);
+  }
+  mark(s, 0, st);
+  launch_chunk_stats(s->Y, R, V, L, a->done, s->cs, st);
+  launch_row_merge(s->cs, s->n_chunks, R, L, a->done, s->rs, st);
+  mark(s, 1, st);
+  if (k > 0) launch_topk_chunk(s->Y, R, V, L, a->done, k, s->cand, st);
+  mark(s, 2, st);
+  launch_convert(s->Y, s->rs, R, V, L, a->done, a->step, a->seed, k == 0, s->Phi, s->Plo, s->best,
+                 st);
+  mark(s, 3, st);
+  if (s->impl == DS_IMPL_TENSOR) {
+    cudaError_t e = launch_selfcond_tc(s->Phi, s->Plo, static_cast<const uint16_t*>(a->E), R, V, d,
+                                       L, a->done, S, s->Opart, s->err, st);
+    if (e != cudaSuccess) return cuda_status(e);
+  } else {
+    launch_selfcond_simt(s->Phi, s->Plo, a->E, fp32, R, V, d, L, a->done, S, s->Opart, st);
+  }
+  mark(s, 4, st);
+  launch_reduce_s(s->Opart, S, R, d, L, a->done, s->rs, a->s, st);
+  launch_finalize(s->rs, s->best, s->cand, s->n_chunks, k, R, L, a->done, a->step, a->seed,
+                  a->sampled, a->conf, a->entropy, a->argmax, st);
+  mark(s, 5, st);
+  launch_lock(B, L, V, s->cfg.max_steps, a->seed, a->tau, a->sampled, a->conf, a->step, a->canvas,
+              a->lock, a->done, st);
+  mark(s, 6, st);
+  if (s->timing) {
+    ++s->timed_steps;
+    s->timed_stream = st;
+  }
+  s->launches += 8 + (k > 0 ? 1 : 0);
+  return cuda_status(cudaGetLastError());
+}
+
+ds_status enqueue_standin(ds_sampler* s, const void* W, const float* s_prev, const void* E,
+                          const int32_t* canvas, const uint8_t* done, void* H_out, int batch,
+                          cudaStream_t st) {
+  launch_standin_simt(static_cast<const uint16_t*>(W), s_prev, static_cast<const uint16_t*>(E),
+                      canvas, done, batch * s->cfg.canvas_len, s->cfg.d_model, s->cfg.canvas_len,
+                      static_cast<uint16_t*>(H_out), st);
+  s->launches += 1;
+  return cuda_status(cudaGetLastError());
+}
+
+ds_status enqueue_iteration(ds_sampler* s, const ds_loop_args* a, cudaStream_t st) {
+  if (a->h_mode == DS_H_STANDIN) {
+    ds_status r = enqueue_standin(s, a->W, a->step.s, a->step.E, a->step.canvas, a->step.done,
+                                  a->H_buf, a->step.batch, st);
+    if (r != DS_OK) return r;
+    ds_step_args sa = a->step;
+    sa.H = a->H_buf;
+    return enqueue_step(s, &sa, st);
+  }
+  return enqueue_step(s, &a->step, st);
+}
+
+template <class T>
+T* carve(ds_sampler* s, size_t count, cudaError_t* e) {
+  void* p = nullptr;
+  if (*e != cudaSuccess || count == 0) return nullptr;
+  *e = cudaMalloc(&p, count * sizeof(T));
+  if (*e == cudaSuccess) {
+    s->allocations.push_back(p);
+    s->ws_bytes += count * sizeof(T);
+  }
+  return static_cast<T*>(p);
+}
+
+void free_all(ds_sampler* s) {
+  for (auto& g : s->graphs) {
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+    if (g.graph) cudaGraphDestroy(g.graph);
+  }
+  s->graphs.clear();
+  for (cudaEvent_t e : s->events) cudaEventDestroy(e);
+  s->events.clear();
+  for (void* p : s->allocations) cudaFree(p);
+  s->allocations.clear();
+  if (s->stage) cudaFree(s->stage);
+  s->stage = nullptr;
+  if (s->capture_stream) cudaStreamDestroy(s->capture_stream);
+  s->capture_stream = nullptr;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t ds_abi_version(void) { return DS_SAMPLER_ABI_VERSION; }
+
+const char* ds_status_string(ds_status status) {
+  switch (status) {
+    case DS_OK: return "ok";
+    case DS_ERR_INVALID_ARG: return "invalid argument";
+    case DS_ERR_UNSUPPORTED: return "unsupported configuration";
+    case DS_ERR_CUDA: return "CUDA runtime error";
+    case DS_ERR_TIMEOUT: return "a device-side bounded wait ran out";
+    case DS_ERR_OOM: return "out of device memory";
+    case DS_ERR_DEVICE: return "device-side check failed";
+  }
+  return "unknown status";
+}
+
+ds_status ds_sampler_create(const ds_sampler_config* cfg, ds_sampler** out) {
+  if (!cfg || !out) return DS_ERR_INVALID_ARG;
+  *out = nullptr;
+  const ds_sampler_config& c = *cfg;
+  if (c.canvas_len < 128 || c.canvas_len > 1024 || c.canvas_len % 128) return DS_ERR_INVALID_ARG;
+  if (c.vocab < 256 || c.vocab > (1 << 24) || c.vocab % 256) return DS_ERR_INVALID_ARG;
+  if (c.d_model < 64 || c.d_model > 16384 || c.d_model % 64) return DS_ERR_INVALID_ARG;
+  if (c.max_batch < 1 || (int64_t)c.max_batch * c.canvas_len > 65535) return DS_ERR_INVALID_ARG;
+  if (c.dtype != DS_DTYPE_BF16 && c.dtype != DS_DTYPE_FP32) return DS_ERR_INVALID_ARG;
+  if (c.top_k < 0 || c.top_k > kMaxTopK) return DS_ERR_INVALID_ARG;
+  if (c.max_steps < 1 || c.max_steps > (1 << 28)) return DS_ERR_INVALID_ARG;
+  if (c.impl != DS_IMPL_AUTO && c.impl != DS_IMPL_TENSOR && c.impl != DS_IMPL_SIMT)
+    return DS_ERR_INVALID_ARG;
+  const int n_chunks = n_chunks_of(c.vocab);
+  if (c.top_k > 0 && (int64_t)n_chunks * c.top_k > kMaxTopKPool) return DS_ERR_UNSUPPORTED;
+
+  ds_sampler* s = new (std::nothrow) ds_sampler();
+  if (!s) return DS_ERR_OOM;
+  s->cfg = c;
+  s->n_chunks = n_chunks;
+  cudaError_t e = cudaGetDevice(&s->device);
+  if (e != cudaSuccess) {
+    delete s;
+    return DS_ERR_CUDA;
+  }
+  if (c.impl == DS_IMPL_SIMT) {
+    s->impl = DS_IMPL_SIMT;
+  } else {
+    const bool tc_ok = c.dtype == DS_DTYPE_BF16 && tc_available();
+    if (c.impl == DS_IMPL_TENSOR && !tc_ok) {
+      delete s;
+      return DS_ERR_UNSUPPORTED;
+    }
+    s->impl = tc_ok ? DS_IMPL_TENSOR : DS_IMPL_SIMT;
+  }
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, s->device);
+  s->num_sms = sms > 0 ? sms : 1;
+
+  const size_t Rm = (size_t)c.max_batch * c.canvas_len;
+  const size_t V = (size_t)c.vocab, d = (size_t)c.d_model;
+  size_t opart = 0;
+  for (int b = 1; b <= c.max_batch; ++b)
+    opart = std::max(opart, (size_t)splits_for(s, b) * b * c.canvas_len * d);
+  e = cudaSuccess;
+  s->Y = carve<float>(s, Rm * V, &e);
+  s->Phi = carve<uint16_t>(s, Rm * V, &e);
+  s->Plo = carve<uint16_t>(s, Rm * V, &e);
+  s->cs = carve<ChunkStat>(s, Rm * n_chunks, &e);
+  s->rs = carve<RowStat>(s, Rm, &e);
+  s->best = carve<Best>(s, Rm * n_chunks, &e);
+  if (c.top_k > 0) s->cand = carve<Cand>(s, Rm * n_chunks * c.top_k, &e);
+  s->Opart = carve<float>(s, opart, &e);
+  s->opart_floats = opart;
+  s->err = carve<uint32_t>(s, 4, &e);
+  s->iter = carve<int32_t>(s, 4, &e);
+  if (e == cudaSuccess) e = cudaMemset(s->err, 0, 4 * sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s->capture_stream, cudaStreamNonBlocking);
+  if (e != cudaSuccess) {
+    free_all(s);
+    delete s;
+    cudaGetLastError();
+    return cuda_status(e);
+  }
+  *out = s;
+  return DS_OK;
+}
+
+ds_status ds_sampler_destroy(ds_sampler* s) {
+  if (!s) return DS_OK;
+  cudaDeviceSynchronize();
+  free_all(s);
+  delete s;
+  return DS_OK;
+}
+
+ds_status ds_sampler_workspace_bytes(const ds_sampler* s, size_t* bytes) {
+  if (!s || !bytes) return DS_ERR_INVALID_ARG;
+  *bytes = s->ws_bytes;
+  return DS_OK;
+}
+
+ds_status ds_sampler_impl(const ds_sampler* s, int32_t* impl) {
+  if (!s || !impl) return DS_ERR_INVALID_ARG;
+  *impl = s->impl;
+  return DS_OK;
+}
+
+ds_status ds_sampler_step(ds_sampler* s, const ds_step_args* a, void* stream) {
+  if (!s) return DS_ERR_INVALID_ARG;
+  ds_status r = check_step_args(s, a);
+  if (r != DS_OK) return r;
+  return enqueue_step(s, a, static_cast<cudaStream_t>(stream));
+}
+
+ds_status ds_sampler_step_host(ds_sampler* s, const ds_step_args* h, void* stream) {
+  if (!s) return DS_ERR_INVALID_ARG;
+  if (!h || h->batch < 1 || h->batch > s->cfg.max_batch || !h->E) return DS_ERR_INVALID_ARG;
+  if (!h->H || !h->temperature || !h->tau || !h->step || !h->canvas || !h->lock || !h->done ||
+      !h->s || !h->sampled || !h->conf || !h->entropy || !h->argmax)
+    return DS_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t B = (size_t)h->batch, L = (size_t)s->cfg.canvas_len, d = (size_t)s->cfg.d_model;
+  const size_t Bm = (size_t)s->cfg.max_batch;
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  // staging layout for max_batch: H | s | T | tau | step | canvas | lock | done | sampled | conf
+  // | entropy | argmax
+  const size_t nH = up(Bm * L * d * esize(s->cfg.dtype)), nS = up(Bm * L * d * 4);
+  const size_t nB4 = up(Bm * 4), nBL4 = up(Bm * L * 4), nBL1 = up(Bm * L), nB1 = up(Bm);
+  const size_t total = nH + nS + 3 * nB4 + nBL4 + nBL1 + nB1 + 4 * nBL4;
+  if (!s->stage) {
+    cudaError_t e = cudaMalloc(&s->stage, total);
+    if (e != cudaSuccess) {
+      s->stage = nullptr;
+      return cuda_status(e);
+    }
+    s->stage_bytes = total;
+  }
+  uint8_t* p = static_cast<uint8_t*>(s->stage);
+  ds_step_args a{};
+  a.batch = h->batch;
+  a.seed = h->seed;
+  a.E = h->E;
+  a.H = p; p += nH;
+  a.s = reinterpret_cast<float*>(p); p += nS;
+  a.temperature = reinterpret_cast<const float*>(p); p += nB4;
+  a.tau = reinterpret_cast<const float*>(p); p += nB4;
+  a.step = reinterpret_cast<int32_t*>(p); p += nB4;
+  a.canvas = reinterpret_cast<int32_t*>(p); p += nBL4;
+  a.lock = p; p += nBL1;
+  a.done = p; p += nB1;
+  a.sampled = reinterpret_cast<int32_t*>(p); p += nBL4;
+  a.conf = reinterpret_cast<float*>(p); p += nBL4;
+  a.entropy = reinterpret_cast<float*>(p); p += nBL4;
+  a.argmax = reinterpret_cast<int32_t*>(p); p += nBL4;
+  cudaError_t e = cudaSuccess;
+  auto h2d = [&](const void* dst, const void* src, size_t n) {
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(const_cast<void*>(dst), src, n, cudaMemcpyHostToDevice, st);
+  };
+  auto d2h = [&](void* dst, const void* src, size_t n) {
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToHost, st);
+  };
+  h2d(a.H, h->H, B * L * d * esize(s->cfg.dtype));
+  h2d(a.temperature, h->temperature, B * 4);
+  h2d(a.tau, h->tau, B * 4);
+  h2d(a.step, h->step, B * 4);
+  h2d(a.canvas, h->canvas, B * L * 4);
+  h2d(a.lock, h->lock, B * L);
+  h2d(a.done, h->done, B);
+  if (e != cudaSuccess) return cuda_status(e);
+  ds_status r = check_step_args(s, &a);
+  if (r != DS_OK) return r;
+  r = enqueue_step(s, &a, st);
+  if (r != DS_OK) return r;
+  d2h(h->s, a.s, B * L * d * 4);
+  d2h(h->sampled, a.sampled, B * L * 4);
+  d2h(h->conf, a.conf, B * L * 4);
+  d2h(h->entropy, a.entropy, B * L * 4);
+  d2h(h->argmax, a.argmax, B * L * 4);
+  d2h(h->step, a.step, B * 4);
+  d2h(h->canvas, a.canvas, B * L * 4);
+  d2h(h->lock, a.lock, B * L);
+  d2h(h->done, a.done, B);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return cuda_status(e);
+}
+
+ds_status ds_standin_hidden(ds_sampler* s, const void* W, const float* s_prev, const void* E,
+                            const int32_t* canvas, const uint8_t* done, void* H_out, int32_t batch,
+                            void* stream) {
+  if (!s || !W || !s_prev || !E || !canvas || !H_out) return DS_ERR_INVALID_ARG;
+  if (batch < 1 || batch > s->cfg.max_batch || s->cfg.dtype != DS_DTYPE_BF16)
+    return DS_ERR_INVALID_ARG;
+  return enqueue_standin(s, W, s_prev, E, canvas, done, H_out, batch,
+                         static_cast<cudaStream_t>(stream));
+}
+
+ds_status ds_denoise_loop(ds_sampler* s, const ds_loop_args* a, void* stream) {
+  if (!s || !a) return DS_ERR_INVALID_ARG;
+  if (a->max_iters < 1 || a->max_iters > s->cfg.max_steps) return DS_ERR_INVALID_ARG;
+  if (a->h_mode != DS_H_FIXED && a->h_mode != DS_H_STANDIN) return DS_ERR_INVALID_ARG;
+  ds_step_args sa = a->step;
+  if (a->h_mode == DS_H_STANDIN) {
+    if (!a->W || !a->H_buf || s->cfg.dtype != DS_DTYPE_BF16) return DS_ERR_INVALID_ARG;
+    sa.H = a->H_buf;
+  }
+  ds_status r = check_step_args(s, &sa);
+  if (r != DS_OK) return r;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!a->use_graph) {
+    for (int it = 0; it < a->max_iters; ++it) {
+      r = enqueue_iteration(s, a, st);
+      if (r != DS_OK) return r;
+    }
+    return DS_OK;
+  }
+  const bool was_timing = s->timing;
+  s->timing = false;
+  struct Restore {
+    ds_sampler* s;
+    bool v;
+    ~Restore() { s->timing = v; }
+  } restore{s, was_timing};
+  LoopGraph* g = nullptr;
+  for (auto& e : s->graphs)
+    if (std::memcmp(&e.key, a, sizeof(ds_loop_args)) == 0) g = &e;
+  if (!g) {
+    LoopGraph ng;
+    std::memcpy(&ng.key, a, sizeof(ds_loop_args));
+    ng.batch = a->step.batch;
+    cudaError_t e = cudaGraphCreate(&ng.graph, 0);
+    cudaGraphConditionalHandle h = 0;
+    if (e == cudaSuccess) e = cudaGraphConditionalHandleCreate(&h, ng.graph, 0, 0);
+    cudaStream_t cs = s->capture_stream;
+    if (e == cudaSuccess)
+      e = cudaStreamBeginCaptureToGraph(cs, ng.graph, nullptr, nullptr, 0,
+                                        cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) {
+      launch_loop_begin(a->step.done, a->step.batch, s->iter, a->max_iters, h, cs);
+      s->launches += 1;
+      cudaGraph_t outg = nullptr;
+      e = cudaStreamEndCapture(cs, &outg);
+    }
+    cudaGraphNode_t begin_node = nullptr;
+    size_t n_nodes = 1;
+    if (e == cudaSuccess) e = cudaGraphGetNodes(ng.graph, &begin_node, &n_nodes);
+    cudaGraphNodeParams cp{};
+    cudaGraphNode_t cond_node = nullptr;
+    if (e == cudaSuccess) {
+      cp.type = cudaGraphNodeTypeConditional;
+      cp.conditional.handle = h;
+      cp.conditional.type = cudaGraphCondTypeWhile;
+      cp.conditional.size = 1;
+      e = cudaGraphAddNode(&cond_node, ng.graph, &begin_node, nullptr, 1, &cp);
+    }
+    if (e == cudaSuccess) {
+      cudaGraph_t body = cp.conditional.phGraph_out[0];
+      e = cudaStreamBeginCaptureToGraph(cs, body, nullptr, nullptr, 0,
+                                        cudaStreamCaptureModeThreadLocal);
+      if (e == cudaSuccess) {
+        ds_status rr = enqueue_iteration(s, a, cs);
+        launch_loop_end(a->step.done, a->step.batch, s->iter, a->max_iters, h, cs);
+        s->launches += 1;
+        cudaGraph_t outb = nullptr;
+        cudaError_t e2 = cudaStreamEndCapture(cs, &outb);
+        e = (rr != DS_OK) ? cudaErrorUnknown : e2;
+      }
+    }
+    if (e == cudaSuccess) e = cudaGraphInstantiate(&ng.exec, ng.graph, 0);
+    if (e != cudaSuccess) {
+      if (ng.exec) cudaGraphExecDestroy(ng.exec);
+      if (ng.graph) cudaGraphDestroy(ng.graph);
+      cudaGetLastError();
+      return DS_ERR_CUDA;
+    }
+    s->graphs.push_back(ng);
+    g = &s->graphs.back();
+  }
+  return cuda_status(cudaGraphLaunch(g->exec, st));
+}
+
+ds_status ds_sampler_device_status(ds_sampler* s, ds_status* out) {
+  if (!s || !out) return DS_ERR_INVALID_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return DS_ERR_CUDA;
+  uint32_t w = 0;
+  e = cudaMemcpy(&w, s->err, sizeof(w), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return DS_ERR_CUDA;
+  cudaMemset(s->err, 0, sizeof(uint32_t));
+  *out = (w & kErrTimeout) ? DS_ERR_TIMEOUT : (w ? DS_ERR_DEVICE : DS_OK);
+  return DS_OK;
+}
+
+ds_status ds_philox4x32_10(const uint32_t* ctr, uint64_t seed, uint32_t* out, int64_t n,
+                           void* stream) {
+  if (n < 0 || (n > 0 && (!ctr || !out))) return DS_ERR_INVALID_ARG;
+  if (!aligned(ctr, 16) || !aligned(out, 16)) return DS_ERR_INVALID_ARG;
+  launch_philox(ctr, seed, out, n, static_cast<cudaStream_t>(stream));
+  return cuda_status(cudaGetLastError());
+}
+
+ds_status ds_sampler_set_phase_timing(ds_sampler* s, int32_t enable) {
+  if (!s) return DS_ERR_INVALID_ARG;
+  s->timing = enable != 0;
+  s->timed_steps = 0;
+  return DS_OK;
+}
+
+ds_status ds_sampler_phase_times(ds_sampler* s, float* ms, int32_t n, int32_t* steps) {
+  if (!s || (n > 0 && !ms)) return DS_ERR_INVALID_ARG;
+  double acc[kPhases] = {0};
+  if (s->timed_steps > 0) {
+    cudaError_t e = cudaStreamSynchronize(s->timed_stream);
+    if (e != cudaSuccess) return DS_ERR_CUDA;
+    for (int t = 0; t < s->timed_steps; ++t)
+      for (int p = 0; p < kPhases; ++p) {
+        float x = 0.f;
+        const size_t base = (size_t)t * kPhaseEvents;
+        if (cudaEventElapsedTime(&x, s->events[base + p], s->events[base + p + 1]) == cudaSuccess)
+          acc[p] += x;
+      }
+  }
+  for (int p = 0; p < n && p < kPhases; ++p) ms[p] = (float)acc[p];
+  if (steps) *steps = s->timed_steps;
+  s->timed_steps = 0;
+  return DS_OK;
+}
+
+ds_status ds_sampler_launch_count(const ds_sampler* s, int64_t* count) {
+  if (!s || !count) return DS_ERR_INVALID_ARG;
+  *count = s->launches;
+  return DS_OK;
+}
+
+ds_status ds_sampler_debug_buffer(ds_sampler* s, int32_t which, const void** ptr, size_t* bytes) {
+  if (!s || !ptr || !bytes) return DS_ERR_INVALID_ARG;
+  const size_t R = (size_t)std::max(1, s->last_batch) * s->cfg.canvas_len;
+  const size_t V = (size_t)s->cfg.vocab;
+  switch (which) {
+    case 0: *ptr = s->Y; *bytes = R * V * 4; return DS_OK;
+    case 1: *ptr = s->rs; *bytes = R * sizeof(RowStat); return DS_OK;
+    case 2: *ptr = s->Phi; *bytes = R * V * 2; return DS_OK;
+    case 3: *ptr = s->Plo; *bytes = R * V * 2; return DS_OK;
+  }
+  return DS_ERR_INVALID_ARG;
+}
+
+}  // extern "C"

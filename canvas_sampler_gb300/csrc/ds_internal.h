@@ -1,0 +1,69 @@
+// Host-side interface between the C ABI (ds_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ds_common.cuh"
+
+namespace ds {
+
+// Vocabulary chunk handled by one CTA of the row kernels (256 threads x 32 values).
+constexpr int kChunk = 8192;
+// Largest top-k the sampler supports, and the largest candidate pool its merge takes.
+constexpr int kMaxTopK = 256;
+constexpr int kMaxTopKPool = 8192;
+
+inline int n_chunks_of(int64_t V) { return (int)((V + kChunk - 1) / kChunk); }
+
+// ---- row kernels (ds_rows.cu) ----
+void launch_chunk_stats(const float* Y, int R, int64_t V, int L, const uint8_t* done,
+                        ChunkStat* cs, cudaStream_t st);
+void launch_row_merge(const ChunkStat* cs, int n_chunks, int R, int L, const uint8_t* done,
+                      RowStat* rs, cudaStream_t st);
+void launch_convert(const float* Y, const RowStat* rs, int R, int64_t V, int L,
+                    const uint8_t* done, const int32_t* step, uint64_t seed, bool gumbel,
+                    uint16_t* Phi, uint16_t* Plo, Best* best, cudaStream_t st);
+void launch_topk_chunk(const float* Y, int R, int64_t V, int L, const uint8_t* done, int k,
+                       Cand* cand, cudaStream_t st);
+void launch_finalize(const RowStat* rs, const Best* best, const Cand* cand, int n_chunks, int k,
+                     int R, int L, const uint8_t* done, const int32_t* step, uint64_t seed,
+                     int32_t* sampled, float* conf, float* entropy, int32_t* argmax,
+                     cudaStream_t st);
+void launch_reduce_s(const float* Opart, int S, int R, int d, int L, const uint8_t* done,
+                     const RowStat* rs, float* s, cudaStream_t st);
+void launch_lock(int B, int L, int64_t V, int max_steps, uint64_t seed, const float* tau,
+                 const int32_t* sampled, const float* conf, int32_t* step, int32_t* canvas,
+                 uint8_t* lock, uint8_t* done, cudaStream_t st);
+void launch_philox(const uint32_t* ctr, uint64_t seed, uint32_t* out, int64_t n, cudaStream_t st);
+void launch_loop_begin(const uint8_t* done, int B, int32_t* iter, int max_iters,
+                       cudaGraphConditionalHandle h, cudaStream_t st);
+void launch_loop_end(const uint8_t* done, int B, int32_t* iter, int max_iters,
+                     cudaGraphConditionalHandle h, cudaStream_t st);
+
+// ---- CUDA-core GEMMs (ds_simt.cu) ----
+void launch_logits_simt(const void* H, const void* E, bool fp32_inputs, int R, int64_t V, int d,
+                        int L, const float* T, const uint8_t* done, float* Y, cudaStream_t st);
+void launch_selfcond_simt(const uint16_t* Phi, const uint16_t* Plo, const void* E,
+                          bool fp32_inputs, int R, int64_t V, int d, int L, const uint8_t* done,
+                          int S, float* Opart, cudaStream_t st);
+void launch_standin_simt(const uint16_t* W, const float* s_prev, const uint16_t* E,
+                         const int32_t* canvas, const uint8_t* done, int R, int d, int L,
+                         uint16_t* H_out, cudaStream_t st);
+
+// ---- tensor-core GEMMs (ds_tc.cu) ----
+// Resolves the driver's tensor-map encoder; false when unavailable.
+bool tc_available();
+int tc_num_sms();
+cudaError_t launch_logits_tc(const uint16_t* H, const uint16_t* E, int R, int64_t V, int d, int L,
+                             const float* T, const uint8_t* done, float* Y, uint32_t* err,
+                             cudaStream_t st);
+cudaError_t launch_selfcond_tc(const uint16_t* Phi, const uint16_t* Plo, const uint16_t* E, int R,
+                               int64_t V, int d, int L, const uint8_t* done, int S, float* Opart,
+                               uint32_t* err, cudaStream_t st);
+// Split count of the tensor-core self-conditioning GEMM for a shape.
+int selfcond_tc_splits(int R, int64_t V, int d, int num_sms);
+
+}  // namespace ds

@@ -1,0 +1,580 @@
+// Row-level kernels of the sampler step: softmax statistics over the vocabulary, the
+// bf16 hi/lo split of exp(y - m) that feeds the self-conditioning GEMM, Gumbel-max sampling
+// (optionally restricted to the top-k logits), the final reduction of s, and the
+// lock / re-noise / stop kernel.
+//
+// Definitions: DiffusionGemma Technical Report, section 6 "Sampling" (full-precision softmax
+// over the vocabulary, self-conditioning matmul), section 6 "Multi-user throughput" (top-k
+// truncation of the sampling step); "DiffusionGemma: Google's open diffusion LLM", section "A
+// diffusion language model refines 256 tokens in 12 steps" (accept confident tokens,
+// re-noise the rest uniformly, at most 48 steps).
+#include <cfloat>
+#include <climits>
+
+#include "ds_internal.h"
+
+namespace ds {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kPer = kChunk / kThreads;   // 32 values per thread
+constexpr int kGroups = kPer / 4;         // float4 groups per thread
+// An element more than this below the row maximum cannot win the Gumbel-max: the largest
+// Gumbel draw is -ln(-ln(1 - 2^-24)) = 16.64, the smallest -ln(-ln 2^-24) = -2.81, and
+// 19.6 > 16.64 + 2.81 leaves margin for fp32 rounding.
+constexpr float kGumbelReach = 19.6f;
+
+__device__ float block_sum(float v, float* sh) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, ln = threadIdx.x & 31;
+  __syncthreads();
+  if (ln == 0) sh[w] = v;
+  __syncthreads();
+  v = ln < (int)(blockDim.x >> 5) ? sh[ln] : 0.f;
+  return warp_sum(v);
+}
+
+// Best (v, j) over the block, then the y carried by the winner; every thread gets the result.
+__device__ void block_best(float& v, int32_t& j, float& y, float* shv, int32_t* shj, float* shy) {
+  float bv = v;
+  int32_t bj = j;
+  warp_best(bv, bj);
+  const int w = threadIdx.x >> 5, ln = threadIdx.x & 31;
+  __syncthreads();
+  if (ln == 0) {
+    shv[w] = bv;
+    shj[w] = bj;
+  }
+  __syncthreads();
+  bv = ln < (int)(blockDim.x >> 5) ? shv[ln] : -INFINITY;
+  bj = ln < (int)(blockDim.x >> 5) ? shj[ln] : INT_MAX;
+  warp_best(bv, bj);
+  __syncthreads();
+  if (j == bj && v == bv && bj != INT_MAX) *shy = y;
+  __syncthreads();
+  v = bv;
+  j = bj;
+  y = (bj != INT_MAX) ? *shy : 0.f;
+}
+
+// Inclusive/exclusive scan of one int per thread over the block (256 threads).
+__device__ int block_exclusive_scan(int x, int* sh, int* total) {
+  const int w = threadIdx.x >> 5, ln = threadIdx.x & 31;
+  int incl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (ln >= o) incl += t;
+  }
+  __syncthreads();
+  if (ln == 31) sh[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int v = ln < (int)(blockDim.x >> 5) ? sh[ln] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, v, o);
+      if (ln >= o) v += t;
+    }
+    if (ln < (int)(blockDim.x >> 5)) sh[ln] = v;  // inclusive warp totals
+  }
+  __syncthreads();
+  const int warp_off = w > 0 ? sh[w - 1] : 0;
+  *total = sh[(blockDim.x >> 5) - 1];
+  return warp_off + incl - x;
+}
+
+// Select the k largest keys held by the block (NPER per thread, element order (q, thread)),
+// ties at the k-th key broken toward earlier elements. Calls emit(q, slot) for each selected
+// element with slot in [0, k) following element order. Radix select on 8-bit digits.
+template <int NPER, class Emit>
+__device__ void block_select_topk(const uint32_t (&key)[NPER], const bool (&valid)[NPER], int k,
+                                  int* hist, int* scan_sh, Emit emit) {
+  uint32_t prefix = 0, mask = 0;
+  int need = k;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int t = threadIdx.x; t < 256; t += blockDim.x) hist[t] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < NPER; ++q)
+      if (valid[q] && (key[q] & mask) == prefix) atomicAdd(&hist[(key[q] >> shift) & 255u], 1);
+    __syncthreads();
+    __shared__ int sel_bin, sel_need;
+    if (threadIdx.x == 0) {
+      int cum = 0, bin = 0;
+      for (bin = 255; bin >= 0; --bin) {
+        if (cum + hist[bin] >= need) break;
+        cum += hist[bin];
+      }
+      if (bin < 0) bin = 0;  // fewer valid elements than k: take everything
+      sel_bin = bin;
+      sel_need = need - cum;
+    }
+    __syncthreads();
+    prefix |= (uint32_t)sel_bin << shift;
+    mask |= 255u << shift;
+    need = sel_need;
+    __syncthreads();
+  }
+  // `prefix` is the k-th largest key; take all larger ones and the first `need` equal ones.
+  int base = 0;
+#pragma unroll
+  for (int q = 0; q < NPER; ++q) {
+    const bool gt = valid[q] && key[q] > prefix;
+    const bool eq = valid[q] && key[q] == prefix;
+    int total_eq = 0;
+    const int eq_rank = block_exclusive_scan(eq ? 1 : 0, scan_sh, &total_eq);
+    int dummy = 0;
+    const bool take = gt || (eq && eq_rank < need);
+    const int slot = block_exclusive_scan(take ? 1 : 0, scan_sh, &dummy);
+    if (take) emit(q, base + slot);
+    base += dummy;
+    need -= min(need, total_eq);
+  }
+}
+
+// ----------------------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kThreads) k_chunk_stats(const float* __restrict__ Y, int64_t V,
+                                                          int L, const uint8_t* __restrict__ done,
+                                                          ChunkStat* __restrict__ cs,
+                                                          int n_chunks) {
+  __shared__ float shf[32];
+  __shared__ float shv[32], shy;
+  __shared__ int32_t shj[32];
+  const int c = blockIdx.x, r = blockIdx.y;
+  if (done && done[r / L]) return;
+  const float* y = Y + (size_t)r * V;
+  const int64_t j0 = (int64_t)c * kChunk, j1 = min(V, j0 + kChunk);
+  float v[kPer];
+  float m = -INFINITY;
+  int32_t arg = INT_MAX;
+#pragma unroll
+  for (int g = 0; g < kGroups; ++g) {
+    const int64_t j = j0 + 4 * (threadIdx.x + kThreads * g);
+    if (j < j1) {
+      const float4 t = *reinterpret_cast<const float4*>(y + j);
+      v[4 * g] = t.x;
+      v[4 * g + 1] = t.y;
+      v[4 * g + 2] = t.z;
+      v[4 * g + 3] = t.w;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (better(v[4 * g + e], (int32_t)(j + e), m, arg)) {
+          m = v[4 * g + e];
+          arg = (int32_t)(j + e);
+        }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[4 * g + e] = -INFINITY;
+    }
+  }
+  float dummy_y = 0.f;
+  block_best(m, arg, dummy_y, shv, shj, &shy);
+  float l = 0.f, a = 0.f;
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    if (v[q] != -INFINITY) {
+      const float t = v[q] - m;
+      const float e = expf(t);
+      l += e;
+      a = fmaf(e, t, a);
+    }
+  }
+  l = block_sum(l, shf);
+  a = block_sum(a, shf);
+  if (threadIdx.x == 0) cs[(size_t)r * n_chunks + c] = ChunkStat{m, l, a, arg};
+}
+
+// One warp per row; fp64 merge of the chunk statistics.
+__global__ void k_row_merge(const ChunkStat* __restrict__ cs, int n_chunks, int R, int L,
+                            const uint8_t* __restrict__ done, RowStat* __restrict__ rs) {
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int ln = threadIdx.x & 31;
+  if (r >= R) return;
+  if (done && done[r / L]) return;
+  const ChunkStat* c = cs + (size_t)r * n_chunks;
+  float m = -INFINITY;
+  int32_t arg = INT_MAX;
+  for (int q = ln; q < n_chunks; q += 32)
+    if (better(c[q].m, c[q].arg, m, arg)) {
+      m = c[q].m;
+      arg = c[q].arg;
+    }
+  warp_best(m, arg);
+  double l = 0.0, a = 0.0;
+  for (int q = ln; q < n_chunks; q += 32) {
+    const double dm = (double)c[q].m - (double)m;
+    const double sc = exp(dm);
+    l += (double)c[q].l * sc;
+    a += ((double)c[q].a + (double)c[q].l * dm) * sc;
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    l += __shfl_xor_sync(0xffffffffu, l, o);
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+  }
+  if (ln == 0) rs[r] = RowStat{m, (float)l, (float)(log(l) - a / l), arg};
+}
+
+__device__ __forceinline__ void split_bf16(float p, uint16_t& hi, uint16_t& lo) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(p);
+  const __nv_bfloat16 q = __float2bfloat16_rn(p - __bfloat162float(h));
+  hi = __bfloat16_as_ushort(h);
+  lo = __bfloat16_as_ushort(q);
+}
+
+// exp(y - m) as bf16 hi + lo (the A operand of the self-conditioning GEMM) and the chunk's
+// best Gumbel-perturbed logit.
+__global__ void __launch_bounds__(kThreads) k_convert(const float* __restrict__ Y,
+                                                      const RowStat* __restrict__ rs, int64_t V,
+                                                      int L, const uint8_t* __restrict__ done,
+                                                      const int32_t* __restrict__ step,
+                                                      uint64_t seed, int gumbel,
+                                                      uint16_t* __restrict__ Phi,
+                                                      uint16_t* __restrict__ Plo,
+                                                      Best* __restrict__ best, int n_chunks) {
+  __shared__ float shv[32], shy;
+  __shared__ int32_t shj[32];
+  const int c = blockIdx.x, r = blockIdx.y;
+  const int b = r / L, i = r % L;
+  if (done && done[b]) return;
+  const float m = rs[r].m;
+  const uint32_t st = gumbel ? (uint32_t)step[b] : 0u;
+  const float* y = Y + (size_t)r * V;
+  uint16_t* ph = Phi + (size_t)r * V;
+  uint16_t* pl = Plo + (size_t)r * V;
+  const int64_t j0 = (int64_t)c * kChunk, j1 = min(V, j0 + kChunk);
+  float bv = -INFINITY, by = 0.f;
+  int32_t bj = INT_MAX;
+#pragma unroll 2
+  for (int g = 0; g < kGroups; ++g) {
+    const int64_t j = j0 + 4 * (threadIdx.x + kThreads * g);
+    if (j >= j1) continue;
+    const float4 t = *reinterpret_cast<const float4*>(y + j);
+    const float yy[4] = {t.x, t.y, t.z, t.w};
+    uint16_t hi[4], lo[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) split_bf16(expf(yy[e] - m), hi[e], lo[e]);
+    *reinterpret_cast<uint2*>(ph + j) =
+        make_uint2((uint32_t)hi[0] | ((uint32_t)hi[1] << 16), (uint32_t)hi[2] | ((uint32_t)hi[3] << 16));
+    *reinterpret_cast<uint2*>(pl + j) =
+        make_uint2((uint32_t)lo[0] | ((uint32_t)lo[1] << 16), (uint32_t)lo[2] | ((uint32_t)lo[3] << 16));
+    if (gumbel) {
+      const float floor_y = m - kGumbelReach;
+      if (fmaxf(fmaxf(yy[0], yy[1]), fmaxf(yy[2], yy[3])) >= floor_y) {
+        const u32x4 w = gumbel_block((uint32_t)(j >> 2), (uint32_t)i, (uint32_t)b, st, seed);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (yy[e] >= floor_y) {
+            const float v = yy[e] + gumbel_from_word(word_of(w, e));
+            if (better(v, (int32_t)(j + e), bv, bj)) {
+              bv = v;
+              bj = (int32_t)(j + e);
+              by = yy[e];
+            }
+          }
+        }
+      }
+    }
+  }
+  if (gumbel) {
+    block_best(bv, bj, by, shv, shj, &shy);
+    if (threadIdx.x == 0) best[(size_t)r * n_chunks + c] = Best{bv, bj, by, 0};
+  }
+}
+
+// The k largest logits of a chunk (ties toward lower tokens), written in token order.
+// Element q of thread t is token j0 + t + 256 q, so the selection's (q, thread) order is
+// token order.
+__global__ void __launch_bounds__(kThreads) k_topk_chunk(const float* __restrict__ Y, int64_t V,
+                                                         int L, const uint8_t* __restrict__ done,
+                                                         int k, Cand* __restrict__ cand,
+                                                         int n_chunks) {
+  __shared__ int hist[256];
+  __shared__ int scan_sh[32];
+  const int c = blockIdx.x, r = blockIdx.y;
+  if (done && done[r / L]) return;
+  const float* y = Y + (size_t)r * V;
+  const int64_t j0 = (int64_t)c * kChunk, j1 = min(V, j0 + kChunk);
+  uint32_t key[kPer];
+  bool valid[kPer];
+  float val[kPer];
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int64_t j = j0 + threadIdx.x + (int64_t)kThreads * q;
+    valid[q] = j < j1;
+    val[q] = valid[q] ? y[j] : -INFINITY;
+    key[q] = float_key(val[q]);
+  }
+  Cand* out = cand + ((size_t)r * n_chunks + c) * k;
+  for (int t = threadIdx.x; t < k; t += kThreads) out[t] = Cand{-INFINITY, INT_MAX};
+  __syncthreads();
+  block_select_topk<kPer>(key, valid, k, hist, scan_sh, [&](int q, int slot) {
+    out[slot] = Cand{val[q], (int32_t)(j0 + threadIdx.x + (int64_t)kThreads * q)};
+  });
+}
+
+// Per row: the sampled token, its confidence, the entropy and the argmax.
+__global__ void __launch_bounds__(kThreads) k_finalize(
+    const RowStat* __restrict__ rs, const Best* __restrict__ best, const Cand* __restrict__ cand,
+    int n_chunks, int k, int L, const uint8_t* __restrict__ done, const int32_t* __restrict__ step,
+    uint64_t seed, int32_t* __restrict__ sampled, float* __restrict__ conf,
+    float* __restrict__ entropy, int32_t* __restrict__ argmax) {
+  __shared__ float shv[32], shy, shf[32];
+  __shared__ int32_t shj[32];
+  __shared__ int hist[256];
+  __shared__ int scan_sh[32];
+  __shared__ float sel_y[kMaxTopK];
+  __shared__ int32_t sel_j[kMaxTopK];
+  const int r = blockIdx.x;
+  const int b = r / L, i = r % L;
+  if (done && done[b]) return;
+  const RowStat st = rs[r];
+  float bv = -INFINITY, by = 0.f;
+  int32_t bj = INT_MAX;
+  float cval;
+  if (k == 0) {
+    for (int q = threadIdx.x; q < n_chunks; q += kThreads) {
+      const Best t = best[(size_t)r * n_chunks + q];
+      if (better(t.v, t.j, bv, bj)) {
+        bv = t.v;
+        bj = t.j;
+        by = t.y;
+      }
+    }
+    block_best(bv, bj, by, shv, shj, &shy);
+    cval = expf(by - st.m) / st.l;
+  } else {
+    // The pool holds each chunk's candidates in token order, chunks in order, so pool order
+    // is token order; element q of thread t is pool entry t + 256 q.
+    constexpr int NP = kMaxTopKPool / kThreads;
+    const int pool = n_chunks * k;
+    uint32_t key[NP];
+    bool valid[NP];
+    float val[NP];
+    int32_t tok[NP];
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+      const int idx = threadIdx.x + kThreads * q;
+      const Cand t = idx < pool ? cand[(size_t)r * pool + idx] : Cand{-INFINITY, INT_MAX};
+      valid[q] = t.j != INT_MAX;
+      val[q] = t.y;
+      tok[q] = t.j;
+      key[q] = float_key(t.y);
+    }
+    for (int t = threadIdx.x; t < kMaxTopK; t += kThreads) sel_j[t] = INT_MAX;
+    __syncthreads();
+    block_select_topk<NP>(key, valid, k, hist, scan_sh, [&](int q, int slot) {
+      sel_y[slot] = val[q];
+      sel_j[slot] = tok[q];
+    });
+    __syncthreads();
+    // Gumbel-max over the selected set and the truncated normaliser (fixed-order sum).
+    float e_sum = 0.f;
+    for (int t = threadIdx.x; t < k; t += kThreads) {
+      const int32_t j = sel_j[t];
+      if (j == INT_MAX) continue;
+      const float yy = sel_y[t];
+      const u32x4 w = gumbel_block((uint32_t)(j >> 2), (uint32_t)i, (uint32_t)b,
+                                   (uint32_t)step[b], seed);
+      const float v = yy + gumbel_from_word(word_of(w, j & 3));
+      if (better(v, j, bv, bj)) {
+        bv = v;
+        bj = j;
+        by = yy;
+      }
+      e_sum += expf(yy - st.m);
+    }
+    e_sum = block_sum(e_sum, shf);
+    block_best(bv, bj, by, shv, shj, &shy);
+    cval = expf(by - st.m) / e_sum;
+  }
+  if (threadIdx.x == 0) {
+    sampled[r] = bj;
+    conf[r] = cval;
+    entropy[r] = st.ent;
+    argmax[r] = st.arg;
+  }
+}
+
+__global__ void k_reduce_s(const float* __restrict__ Opart, int S, int R, int d, int L,
+                           const uint8_t* __restrict__ done, const RowStat* __restrict__ rs,
+                           float* __restrict__ s) {
+  const int64_t n4 = (int64_t)R * d / 4;
+  const int64_t plane = (int64_t)R * d;
+  for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < n4;
+       q += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)((q * 4) / d);
+    if (done && done[r / L]) continue;
+    float4 acc = *reinterpret_cast<const float4*>(Opart + q * 4);
+    for (int sp = 1; sp < S; ++sp) {
+      const float4 t = *reinterpret_cast<const float4*>(Opart + sp * plane + q * 4);
+      acc.x += t.x;
+      acc.y += t.y;
+      acc.z += t.z;
+      acc.w += t.w;
+    }
+    const float l = rs[r].l;
+    acc.x /= l;
+    acc.y /= l;
+    acc.z /= l;
+    acc.w /= l;
+    *reinterpret_cast<float4*>(s + q * 4) = acc;
+  }
+}
+
+// Lock / re-noise / stop for one sequence per CTA (blockDim = L).
+__global__ void k_lock(int L, uint32_t V, int max_steps, uint64_t seed,
+                       const float* __restrict__ tau, const int32_t* __restrict__ sampled,
+                       const float* __restrict__ conf, int32_t* __restrict__ step,
+                       int32_t* __restrict__ canvas, uint8_t* __restrict__ lock,
+                       uint8_t* __restrict__ done) {
+  __shared__ float shv[32];
+  __shared__ int32_t shj[32];
+  const int b = blockIdx.x, i = threadIdx.x;
+  if (done[b]) return;
+  const int st = step[b];
+  const bool final_step = st + 1 >= max_steps;
+  const size_t at = (size_t)b * L + i;
+  const bool locked = lock[at] != 0;
+  const float c = conf[at];
+  const bool pass = !locked && (final_step || c >= tau[b]);
+  const int any_pass = __syncthreads_or(pass);
+  const int any_open = __syncthreads_or(!locked);
+  bool forced = false;
+  if (!any_pass && any_open) {
+    float v = locked ? -INFINITY : c;
+    int32_t j = locked ? INT_MAX : i;
+    warp_best(v, j);
+    const int w = i >> 5, ln = i & 31;
+    if (ln == 0) {
+      shv[w] = v;
+      shj[w] = j;
+    }
+    __syncthreads();
+    if (w == 0) {
+      v = ln < (int)(blockDim.x >> 5) ? shv[ln] : -INFINITY;
+      j = ln < (int)(blockDim.x >> 5) ? shj[ln] : INT_MAX;
+      warp_best(v, j);
+      if (ln == 0) shj[0] = j;
+    }
+    __syncthreads();
+    forced = (i == shj[0]);
+  }
+  const bool newly = pass || forced;
+  if (newly) {
+    canvas[at] = sampled[at];
+    lock[at] = 1;
+  } else if (!locked) {
+    const u32x4 w = philox4x32_10(u32x4{(uint32_t)(i >> 2), 0u, (uint32_t)b,
+                                        ((uint32_t)st << 2) | kRenoiseStream},
+                                  (uint32_t)seed, (uint32_t)(seed >> 32));
+    canvas[at] = token_from_word(word_of(w, i & 3), V);
+  }
+  const int all_locked = __syncthreads_and(locked || newly);
+  if (i == 0) {
+    step[b] = st + 1;
+    done[b] = all_locked ? 1 : 0;
+  }
+}
+
+__global__ void k_philox(const uint32_t* __restrict__ ctr, uint64_t seed, uint32_t* __restrict__ out,
+                         int64_t n) {
+  for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < n;
+       q += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 c = reinterpret_cast<const uint4*>(ctr)[q];
+    const u32x4 v = philox4x32_10(u32x4{c.x, c.y, c.z, c.w}, (uint32_t)seed, (uint32_t)(seed >> 32));
+    reinterpret_cast<uint4*>(out)[q] = make_uint4(v.x, v.y, v.z, v.w);
+  }
+}
+
+__global__ void k_loop_begin(const uint8_t* __restrict__ done, int B, int32_t* iter, int max_iters,
+                             cudaGraphConditionalHandle h) {
+  int open = 0;
+  for (int b = threadIdx.x; b < B; b += 32) open |= (done[b] == 0);
+  open = __any_sync(0xffffffffu, open);
+  if (threadIdx.x == 0) {
+    *iter = 0;
+    cudaGraphSetConditional(h, (open && max_iters > 0) ? 1u : 0u);
+  }
+}
+
+__global__ void k_loop_end(const uint8_t* __restrict__ done, int B, int32_t* iter, int max_iters,
+                           cudaGraphConditionalHandle h) {
+  int open = 0;
+  for (int b = threadIdx.x; b < B; b += 32) open |= (done[b] == 0);
+  open = __any_sync(0xffffffffu, open);
+  if (threadIdx.x == 0) {
+    const int it = *iter + 1;
+    *iter = it;
+    cudaGraphSetConditional(h, (open && it < max_iters) ? 1u : 0u);
+  }
+}
+
+}  // namespace
+
+void launch_chunk_stats(const float* Y, int R, int64_t V, int L, const uint8_t* done,
+                        ChunkStat* cs, cudaStream_t st) {
+  const int nc = n_chunks_of(V);
+  k_chunk_stats<<<dim3(nc, R), kThreads, 0, st>>>(Y, V, L, done, cs, nc);
+}
+
+void launch_row_merge(const ChunkStat* cs, int n_chunks, int R, int L, const uint8_t* done,
+                      RowStat* rs, cudaStream_t st) {
+  k_row_merge<<<(R + 7) / 8, 256, 0, st>>>(cs, n_chunks, R, L, done, rs);
+}
+
+void launch_convert(const float* Y, const RowStat* rs, int R, int64_t V, int L,
+                    const uint8_t* done, const int32_t* step, uint64_t seed, bool gumbel,
+                    uint16_t* Phi, uint16_t* Plo, Best* best, cudaStream_t st) {
+  const int nc = n_chunks_of(V);
+  k_convert<<<dim3(nc, R), kThreads, 0, st>>>(Y, rs, V, L, done, step, seed, gumbel ? 1 : 0, Phi,
+                                              Plo, best, nc);
+}
+
+void launch_topk_chunk(const float* Y, int R, int64_t V, int L, const uint8_t* done, int k,
+                       Cand* cand, cudaStream_t st) {
+  const int nc = n_chunks_of(V);
+  k_topk_chunk<<<dim3(nc, R), kThreads, 0, st>>>(Y, V, L, done, k, cand, nc);
+}
+
+void launch_finalize(const RowStat* rs, const Best* best, const Cand* cand, int n_chunks, int k,
+                     int R, int L, const uint8_t* done, const int32_t* step, uint64_t seed,
+                     int32_t* sampled, float* conf, float* entropy, int32_t* argmax,
+                     cudaStream_t st) {
+  k_finalize<<<R, kThreads, 0, st>>>(rs, best, cand, n_chunks, k, L, done, step, seed, sampled,
+                                     conf, entropy, argmax);
+}
+
+void launch_reduce_s(const float* Opart, int S, int R, int d, int L, const uint8_t* done,
+                     const RowStat* rs, float* s, cudaStream_t st) {
+  const int64_t n4 = (int64_t)R * d / 4;
+  const int blocks = (int)std::min<int64_t>((n4 + 255) / 256, 4096);
+  k_reduce_s<<<blocks, 256, 0, st>>>(Opart, S, R, d, L, done, rs, s);
+}
+
+void launch_lock(int B, int L, int64_t V, int max_steps, uint64_t seed, const float* tau,
+                 const int32_t* sampled, const float* conf, int32_t* step, int32_t* canvas,
+                 uint8_t* lock, uint8_t* done, cudaStream_t st) {
+  k_lock<<<B, L, 0, st>>>(L, (uint32_t)V, max_steps, seed, tau, sampled, conf, step, canvas, lock,
+                          done);
+}
+
+void launch_philox(const uint32_t* ctr, uint64_t seed, uint32_t* out, int64_t n, cudaStream_t st) {
+  const int blocks = (int)std::min<int64_t>((n + 255) / 256, 4096);
+  if (n > 0) k_philox<<<blocks, 256, 0, st>>>(ctr, seed, out, n);
+}
+
+void launch_loop_begin(const uint8_t* done, int B, int32_t* iter, int max_iters,
+                       cudaGraphConditionalHandle h, cudaStream_t st) {
+  k_loop_begin<<<1, 32, 0, st>>>(done, B, iter, max_iters, h);
+}
+
+void launch_loop_end(const uint8_t* done, int B, int32_t* iter, int max_iters,
+                     cudaGraphConditionalHandle h, cudaStream_t st) {
+  k_loop_end<<<1, 32, 0, st>>>(done, B, iter, max_iters, h);
+}
+
+}  // namespace ds

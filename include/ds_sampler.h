@@ -1,0 +1,218 @@
+/*
+ * ds_sampler.h -- C ABI of the GB300 (sm_103a) canvas sampler for uniform-state text diffusion.
+ *
+ * One sampler step over a batch of 256-token canvases:
+ *   logits  z = H . E^T over the whole vocabulary, y = z / T;
+ *   full-precision softmax over the vocabulary and the self-conditioning vector
+ *   s = softmax(y) . E                       -- DiffusionGemma Technical Report, section 6,
+ *                                               "Sampling" (softmax over the full canvas, a
+ *                                               "self-conditioning embedding matmul", vocabulary
+ *                                               262k, full precision); section 8, "Finetuning
+ *                                               procedure" (z_t from a previous forward pass);
+ *   Gumbel-max sample x with its probability c, optional top-k truncation of the sampling step
+ *                                            -- report section 6, "Multi-user throughput";
+ *   lock positions with c >= tau (at least one per step), re-noise every other position with a
+ *   uniform token, stop per sequence when all positions are locked or the step budget is spent
+ *                                            -- "DiffusionGemma: Google's open diffusion LLM",
+ *                                               sections "A diffusion language model refines 256
+ *                                               tokens in 12 steps" and "Tokens stay editable
+ *                                               within a canvas, then freeze"; "Google DeepMind's
+ *                                               DiffusionGemma Generates Text 4x Faster by
+ *                                               Ditching Tokens", "How text diffusion actually
+ *                                               works";
+ *   the loop runs on the GPU with no host synchronisation
+ *                                            -- report section 6, "Eliminating CPU-GPU
+ *                                               synchronization".
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked [device] are CUDA device pointers on the device the sampler was created
+ *     on; [host] pointers are ordinary host memory. The caller owns every buffer it passes;
+ *     the library owns its workspace and any CUDA graphs it instantiates.
+ *   - Layouts are dense row-major. B = batch (sequences), L = canvas length, V = vocabulary,
+ *     d = hidden width. bf16 values are IEEE bfloat16 bit patterns (uint16).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Step and
+ *     loop calls only enqueue work; they return before the GPU finishes.
+ *   - Argument errors are found synchronously and returned as a ds_status; nothing is
+ *     enqueued then. Errors found by a kernel (a bounded wait that ran out) set a device error
+ *     word that ds_sampler_device_status reports. No call throws across the ABI.
+ *   - One sampler must not be used from two streams at once (its workspace is shared).
+ */
+#ifndef DS_SAMPLER_H
+#define DS_SAMPLER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DS_SAMPLER_ABI_VERSION 1
+
+typedef enum ds_status {
+  DS_OK = 0,
+  DS_ERR_INVALID_ARG = 1,  /* null pointer, bad size or bad enum value */
+  DS_ERR_UNSUPPORTED = 2,  /* valid request this build cannot serve (e.g. shape constraints) */
+  DS_ERR_CUDA = 3,         /* a CUDA runtime call failed; the sampler may be unusable */
+  DS_ERR_TIMEOUT = 4,      /* a kernel's bounded wait ran out (reported by device_status) */
+  DS_ERR_OOM = 5,          /* workspace allocation failed */
+  DS_ERR_DEVICE = 6        /* another device-side check failed (reported by device_status) */
+} ds_status;
+
+enum { DS_DTYPE_BF16 = 0, DS_DTYPE_FP32 = 1 };
+/* Kernel family: TENSOR = tcgen05/TMEM/TMA tensor-core kernels (bf16 inputs, d % 64 == 0);
+ * SIMT = CUDA-core fp32 kernels (any supported dtype); AUTO = TENSOR where it applies. */
+enum { DS_IMPL_AUTO = 0, DS_IMPL_TENSOR = 1, DS_IMPL_SIMT = 2 };
+enum { DS_H_FIXED = 0, DS_H_STANDIN = 1 };
+
+/* Sampler shape and options, fixed at creation.
+ *   canvas_len  L, a multiple of 128 and at most 1024 (256 on the pages);
+ *   vocab       V, a multiple of 256, at most 2^24;
+ *   d_model     d, a multiple of 64, at most 16384;
+ *   max_batch   largest B a call may pass (the workspace is sized for it);
+ *   dtype       storage type of H and E (DS_DTYPE_*);
+ *   top_k       0 = sample from the full softmax, else 1..256: sample among the k largest logits;
+ *   max_steps   step budget per canvas (48 on the pages); the last step locks every position;
+ *   impl        DS_IMPL_*. */
+typedef struct ds_sampler_config {
+  int32_t max_batch;
+  int32_t canvas_len;
+  int32_t d_model;
+  int32_t dtype;
+  int64_t vocab;
+  int32_t top_k;
+  int32_t max_steps;
+  int32_t impl;
+  int32_t reserved;
+} ds_sampler_config;
+
+typedef struct ds_sampler ds_sampler;
+
+/* Arguments of one step. All pointers [device] unless a host entry point says otherwise.
+ *   H           [B, L, d] dtype     hidden states of the canvas positions (input)
+ *   E           [V, d] dtype        embedding table, used as both keys and values (input)
+ *   temperature [B] float           T_b > 0 (input)
+ *   tau         [B] float           lock threshold (input)
+ *   step        [B] int32           steps already taken by each sequence (in/out)
+ *   canvas      [B, L] int32        canvas tokens in [0, V) (in/out)
+ *   lock        [B, L] uint8        1 = locked (in/out)
+ *   done        [B] uint8           1 = finished; finished sequences are left untouched (in/out)
+ *   s           [B, L, d] float     self-conditioning vector (out)
+ *   sampled     [B, L] int32        Gumbel-max sample x (out)
+ *   conf        [B, L] float        probability of x under the sampled distribution (out)
+ *   entropy     [B, L] float        softmax entropy in nats (out)
+ *   argmax      [B, L] int32        most likely token, lowest index on ties (out)
+ *   seed        key of the counter-based generator (Philox4x32-10); draws depend only on
+ *               (seed, sequence, position, token, step), so any step boundary is a checkpoint. */
+typedef struct ds_step_args {
+  int32_t batch;
+  int32_t reserved;
+  uint64_t seed;
+  const void* H;
+  const void* E;
+  const float* temperature;
+  const float* tau;
+  int32_t* step;
+  int32_t* canvas;
+  uint8_t* lock;
+  uint8_t* done;
+  float* s;
+  int32_t* sampled;
+  float* conf;
+  float* entropy;
+  int32_t* argmax;
+} ds_step_args;
+
+/* Arguments of a denoising loop: steps repeat on the GPU until every sequence is done or
+ * max_iters steps have run.
+ *   h_mode   DS_H_FIXED: every step uses step.H;
+ *            DS_H_STANDIN: before each step H = bf16(tanh(W . [bf16(s); E[canvas]])) is written
+ *            to H_buf (a stand-in for the model's decoder, which is out of scope); `s` must hold
+ *            the previous step's self-conditioning vector (zeros for a fresh canvas).
+ *   W        [d, 2d] bf16 [device] (DS_H_STANDIN only)
+ *   H_buf    [B, L, d] bf16 [device] work buffer (DS_H_STANDIN only)
+ *   max_iters 1 .. max_steps
+ *   use_graph 1: the whole loop is one CUDA graph launch whose while-node condition is set by
+ *            the lock kernel (no host synchronisation); 0: plain launches of the same kernels.
+ * Graphs are cached per argument set; buffers must outlive the sampler or the next call with
+ * different pointers. */
+typedef struct ds_loop_args {
+  ds_step_args step;
+  int32_t h_mode;
+  int32_t max_iters;
+  int32_t use_graph;
+  int32_t reserved;
+  const void* W;
+  void* H_buf;
+} ds_loop_args;
+
+/* Version of this ABI (DS_SAMPLER_ABI_VERSION). */
+int32_t ds_abi_version(void);
+
+/* Static string for a status code; never NULL. */
+const char* ds_status_string(ds_status status);
+
+/* Create a sampler on the current CUDA device: validates `cfg`, allocates the workspace for
+ * cfg->max_batch. On success *out owns the sampler (free it with ds_sampler_destroy). */
+ds_status ds_sampler_create(const ds_sampler_config* cfg, ds_sampler** out);
+
+/* Free the workspace and graphs. Synchronises the device first. NULL is accepted. */
+ds_status ds_sampler_destroy(ds_sampler* sampler);
+
+/* Bytes of device workspace the sampler holds. */
+ds_status ds_sampler_workspace_bytes(const ds_sampler* sampler, size_t* bytes);
+
+/* The kernel family the sampler runs (DS_IMPL_TENSOR or DS_IMPL_SIMT after AUTO is resolved). */
+ds_status ds_sampler_impl(const ds_sampler* sampler, int32_t* impl);
+
+/* Enqueue one sampler step on `stream` (see ds_step_args). 1 <= batch <= max_batch. */
+ds_status ds_sampler_step(ds_sampler* sampler, const ds_step_args* args, void* stream);
+
+/* The same step with every per-step buffer in [host] memory (page-locked memory gives
+ * asynchronous copies) and only E on the device: copies the inputs in, runs the step, copies
+ * the outputs and the updated state back, and synchronises `stream` before returning. */
+ds_status ds_sampler_step_host(ds_sampler* sampler, const ds_step_args* host_args, void* stream);
+
+/* Enqueue a denoising loop on `stream` (see ds_loop_args). */
+ds_status ds_denoise_loop(ds_sampler* sampler, const ds_loop_args* args, void* stream);
+
+/* Enqueue the hidden-state stand-in alone: H_out = bf16(tanh(W . [bf16(s_prev); E[canvas]]))
+ * for sequences with done == 0 (done may be NULL). W [d, 2d] bf16, s_prev [B, L, d] float,
+ * E [V, d] bf16, canvas [B, L] int32, H_out [B, L, d] bf16, all [device]. */
+ds_status ds_standin_hidden(ds_sampler* sampler, const void* W, const float* s_prev,
+                            const void* E, const int32_t* canvas, const uint8_t* done,
+                            void* H_out, int32_t batch, void* stream);
+
+/* Synchronise the sampler's device and report (then clear) the device error word:
+ * DS_OK, DS_ERR_TIMEOUT or DS_ERR_DEVICE. */
+ds_status ds_sampler_device_status(ds_sampler* sampler, ds_status* out);
+
+/* Philox4x32-10 blocks on the device, for checking the generator: out[i] = Philox(ctr[i], key)
+ * with key = (seed low word, seed high word). ctr and out are [n, 4] uint32 [device]. */
+ds_status ds_philox4x32_10(const uint32_t* ctr, uint64_t seed, uint32_t* out, int64_t n,
+                           void* stream);
+
+/* Per-phase device timing of ds_sampler_step, for profiling. While enabled, every step records
+ * CUDA events on its stream around each phase and accumulates the elapsed times:
+ *   0 logits GEMM, 1 softmax statistics, 2 top-k candidates, 3 exp(y - m) split + Gumbel-max,
+ *   4 self-conditioning GEMM, 5 reduction of s + finalize, 6 lock / re-noise / stop.
+ * ds_sampler_phase_times synchronises the stream of the last timed step, writes up to n
+ * accumulated milliseconds (per phase, summed over *steps steps) and resets the totals.
+ * Not for use inside stream capture. */
+ds_status ds_sampler_set_phase_timing(ds_sampler* sampler, int32_t enable);
+ds_status ds_sampler_phase_times(ds_sampler* sampler, float* ms, int32_t n, int32_t* steps);
+
+/* Number of kernels the sampler has enqueued since creation (steps, loops, stand-in calls;
+ * a loop captured in a graph counts its kernels once per capture). */
+ds_status ds_sampler_launch_count(const ds_sampler* sampler, int64_t* count);
+
+/* Read-only view of an internal buffer of the last step, for tests and profiling.
+ * which: 0 = scaled logits y [B*L, V] float; 1 = row statistics [B*L] x {m, l, entropy, argmax};
+ * 2 = bf16 high part of exp(y - m) [B*L, V]; 3 = bf16 low part. *ptr is [device]. */
+ds_status ds_sampler_debug_buffer(ds_sampler* sampler, int32_t which, const void** ptr,
+                                  size_t* bytes);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DS_SAMPLER_H */

@@ -149,7 +149,8 @@ def sampler_step(H, E, T, tau, canvas, lock, step, done, seed, *, top_k=0, max_s
     Returns a dict of the outputs for active sequences (done ones keep NaN / -1 outputs and
     unchanged state): s [B, L, d], sampled, conf, entropy, argmax, pmax (= 1 / l_i), and the
     updated canvas, lock, step, done, plus diagnostics used to exclude near-ties from exact
-    comparisons: gumbel_margin (top-two perturbed logits) and top-k boundary gaps.
+    comparisons: gumbel_margin (top-two perturbed logits), argmax_gap (top-two logits) and
+    top-k boundary gaps.
 
     With ``positions`` set, only those positions are computed and the lock update is
     skipped (it needs the whole canvas)."""
@@ -167,6 +168,7 @@ def sampler_step(H, E, T, tau, canvas, lock, step, done, seed, *, top_k=0, max_s
         "pmax": np.full((B, L), np.nan),
         "gumbel_margin": np.full((B, L), np.inf),
         "topk_gap": np.full((B, L), np.inf),
+        "argmax_gap": np.full((B, L), np.inf),
     }
     for b in range(B):
         if done[b]:
@@ -179,6 +181,9 @@ def sampler_step(H, E, T, tau, canvas, lock, step, done, seed, *, top_k=0, max_s
             out["entropy"][b, rows] = ent
             out["argmax"][b, rows] = am
             out["pmax"][b, rows] = 1.0 / l
+            if V > 1:
+                top2 = np.partition(y, -2, axis=1)[:, -2:]
+                out["argmax_gap"][b, rows] = top2[:, 1] - top2[:, 0]
             u = gumbel_uniforms(seed, b, rows, int(step[b]), V)
             g = -np.log(-np.log(u))
             for r, i in enumerate(rows):
