@@ -213,7 +213,7 @@ class Sampler:
 
         class _View:
             __cuda_array_interface__ = {"shape": (nbytes,), "typestr": "|u1",
-                                        "data": (ptr, True), "version": 3}
+                                        "data": (ptr, False), "version": 3}
 
         return torch.as_tensor(_View(), device="cuda").clone()
 

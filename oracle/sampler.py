@@ -119,8 +119,14 @@ def _top_k_set(y_row: np.ndarray, k: int) -> np.ndarray:
     return np.sort(order[:k])
 
 
-def _sample_row(y_row, g_row, p_row, top_k):
-    """Gumbel-max over the row (or its top-k set): (x, c, margin of the top two)."""
+def _sample_row(y_row, g_row, p_row, top_k, band=1e-4):
+    """Gumbel-max over the row (or its top-k set).
+
+    Returns (x, c, margin of the top two perturbed logits, top-k risk). The risk flag is a
+    diagnostic for comparisons only: it is set when a token whose logit lies within `band` of
+    the k-th largest (so that a slightly different logit could move it across the top-k
+    boundary) has a perturbed logit within `band` of the winner's."""
+    risk = False
     if top_k and top_k < y_row.shape[0]:
         cand = _top_k_set(y_row, top_k)
         v = y_row[cand] + g_row[cand]
@@ -129,6 +135,8 @@ def _sample_row(y_row, g_row, p_row, top_k):
         w = np.exp(y_row[cand] - y_row[cand].max())
         c = float(w[best] / w.sum())
         vs = np.sort(v)
+        near = np.abs(y_row - y_row[cand].min()) < band
+        risk = bool(np.any(near & (y_row + g_row >= v[best] - band)))
     else:
         v = y_row + g_row
         x = int(np.argmax(v))
@@ -136,7 +144,7 @@ def _sample_row(y_row, g_row, p_row, top_k):
         vs = np.partition(v, -2)[-2:] if v.shape[0] > 1 else np.array([-np.inf, v[0]])
         vs = np.sort(vs)
     margin = float(vs[-1] - vs[-2]) if vs.shape[0] > 1 else np.inf
-    return x, c, margin
+    return x, c, margin, risk
 
 
 def sampler_step(H, E, T, tau, canvas, lock, step, done, seed, *, top_k=0, max_steps=48,
@@ -169,6 +177,7 @@ def sampler_step(H, E, T, tau, canvas, lock, step, done, seed, *, top_k=0, max_s
         "gumbel_margin": np.full((B, L), np.inf),
         "topk_gap": np.full((B, L), np.inf),
         "argmax_gap": np.full((B, L), np.inf),
+        "topk_risk": np.zeros((B, L), bool),
     }
     for b in range(B):
         if done[b]:
@@ -187,7 +196,8 @@ def sampler_step(H, E, T, tau, canvas, lock, step, done, seed, *, top_k=0, max_s
             u = gumbel_uniforms(seed, b, rows, int(step[b]), V)
             g = -np.log(-np.log(u))
             for r, i in enumerate(rows):
-                x, c, margin = _sample_row(y[r], g[r], p[r], top_k)
+                x, c, margin, risk = _sample_row(y[r], g[r], p[r], top_k)
+                out["topk_risk"][b, i] = risk
                 out["sampled"][b, i] = x
                 out["conf"][b, i] = c
                 out["gumbel_margin"][b, i] = margin

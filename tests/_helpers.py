@@ -6,7 +6,8 @@ Tolerances (fp32 kernels against the fp64 oracle):
   conf (probability) relative error <= 2e-5
   entropy            absolute error <= 2e-5 * max(1, H)
   sampled / argmax   identical, except positions whose top-two (perturbed) logits are within
-                     1e-4 of each other (and, with top-k, whose k-th / (k+1)-th logits are)
+                     1e-4 of each other (and, with top-k, where a token within 1e-4 of the k-th
+                     logit could also win: see the oracle's topk_risk)
   lock / canvas      identical, except where a lock decision is ambiguous: |c - tau| <= 2e-5 tau,
                      an ambiguous sample, or (forced lock) top-two unlocked confidences within
                      2e-5 relative; those sequences are checked against the lock rule applied to
@@ -95,7 +96,7 @@ def compare_outputs(gpu: dict, ref: dict, active_rows, *, top_k=0):
             f"entropy at {(b, i)}: {gpu['entropy'][b, i]} vs {H_r}")
         if ref["argmax_gap"][b, i] >= MARGIN:
             assert gpu["argmax"][b, i] == ref["argmax"][b, i], f"argmax at {(b, i)}"
-        ambiguous = ref["gumbel_margin"][b, i] < MARGIN or (top_k and ref["topk_gap"][b, i] < MARGIN)
+        ambiguous = ref["gumbel_margin"][b, i] < MARGIN or (top_k and ref["topk_risk"][b, i])
         if ambiguous:
             n_excl += 1
             continue
@@ -130,7 +131,7 @@ def check_lock_update(pre: dict, gpu_out: dict, gpu_post: dict, ref: dict | None
         c = ref["conf"][b]
         unl = pre["lock"][b] == 0
         amb = unl & ((np.abs(c - float(tau[b])) <= REL_TOL * float(tau[b])) |
-                     (ref["gumbel_margin"][b] < MARGIN))
+                     (ref["gumbel_margin"][b] < MARGIN) | ref["topk_risk"][b])
         passing = unl & (c >= float(tau[b]))
         forced_amb = False
         if not passing.any() and unl.any() and int(pre["step"][b]) + 1 < max_steps:
@@ -143,6 +144,24 @@ def check_lock_update(pre: dict, gpu_out: dict, gpu_post: dict, ref: dict | None
         assert np.array_equal(gpu_post["canvas"][b], ref["canvas"][b]), f"canvas vs oracle, seq {b}"
         assert gpu_post["done"][b] == ref["done"][b]
     return n_undecidable
+
+
+def standin_close(got_bits, W_bits, s_prev, E64, canvas):
+    """GPU stand-in H (bf16 bits) against the oracle's: within one bf16 rounding of the exact
+    value plus the fp32 accumulation error of the 2d-term dot product (bounded by
+    2d * 2^-24 * sum |W||u|). Returns the fraction of elements that differ at all."""
+    W = oracle.bf16_bits_to_f64(W_bits)
+    s_b = oracle.bf16_bits_to_f64(oracle.f64_to_bf16_bits(s_prev))
+    u = np.concatenate([s_b, E64[np.asarray(canvas)]], axis=-1)
+    x = u @ W.T
+    scale = np.abs(u) @ np.abs(W).T
+    exact = np.tanh(x)
+    got = oracle.bf16_bits_to_f64(got_bits)
+    n_terms = W.shape[1]
+    bound = np.abs(exact) * 2.0 ** -8 + n_terms * 2.0 ** -24 * scale + 1e-30
+    assert np.all(np.abs(got - exact) <= bound), float(np.max(np.abs(got - exact) / bound))
+    want = oracle.f64_to_bf16_bits(exact)
+    return float(np.mean(got_bits != want))
 
 
 def oracle_step(case: GpuCase, pre: dict, H64=None, positions=None):

@@ -1,0 +1,132 @@
+"""The configured workloads at their full sizes, in the launch configuration the bench times.
+
+The oracle recomputes sampled positions one by one (full vocabulary, fp64); the rest of each
+step is checked through properties that hold at any size, and the lock / re-noise / stop
+update is checked exactly against the rule applied to the GPU's own confidences.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from canvas_sampler_gb300 import workloads as W
+from canvas_sampler_gb300.sampler import StepOutputs
+
+from _helpers import GpuCase, check_lock_update, compare_outputs, exact_f64, out_np, oracle_step, standin_close, state_np
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+def _properties(g, w, active):
+    for b in np.nonzero(active)[0]:
+        assert np.all((g["sampled"][b] >= 0) & (g["sampled"][b] < w.V))
+        assert np.all((g["argmax"][b] >= 0) & (g["argmax"][b] < w.V))
+        assert np.all((g["conf"][b] > 0) & (g["conf"][b] <= 1.0 + 1e-6))
+        assert np.all((g["entropy"][b] >= -1e-5) & (g["entropy"][b] <= math.log(w.V) + 1e-4))
+        assert np.all(np.isfinite(g["s"][b]))
+
+
+def _sample_positions(g, b, n):
+    """Spread sample: both ends, lowest and highest confidence, and evenly spaced positions."""
+    c = g["conf"][b]
+    pos = {0, len(c) - 1, int(np.argmin(c)), int(np.argmax(c))}
+    pos |= set(np.linspace(0, len(c) - 1, n).astype(int).tolist())
+    return sorted(pos)
+
+
+@pytest.mark.parametrize("name,per_seq", [("step_bf16_b1_v262144_d2816", 12),
+                                          ("step_bf16_b8_v262144_d2816", 3)])
+def test_full_size_step(name, per_seq):
+    w = W.WORKLOADS[name]
+    case = GpuCase(w)
+    state = case.state()
+    pre = state_np(state)
+    out = case.run_step(state)
+    g, post = out_np(out), state_np(state)
+    active = pre["done"] == 0
+    _properties(g, w, active)
+    check_lock_update(pre, g, post, None, case.inp["tau"], case.inp["seed"], w.V, w.max_steps)
+    rows = []
+    for b in range(w.B):
+        pos = _sample_positions(g, b, per_seq)
+        rows += [(b, i) for i in pos]
+    # oracle per sampled position, one sequence at a time (the others marked done)
+    H64 = exact_f64(case.inp["H"], w.dtype)
+    checked = 0
+    for b in range(w.B):
+        pos = np.array([i for bb, i in rows if bb == b])
+        only_b = np.ones(w.B, np.uint8)
+        only_b[b] = 0
+        ref = oracle.sampler_step(H64, case.E64, case.inp["T"].astype(np.float64),
+                                  case.inp["tau"].astype(np.float64), pre["canvas"], pre["lock"],
+                                  pre["step"], only_b, case.inp["seed"], top_k=w.top_k,
+                                  max_steps=w.max_steps, positions=pos)
+        checked += compare_outputs(g, ref, [(b, int(i)) for i in pos], top_k=w.top_k)["checked"]
+    assert checked == len(rows)
+
+
+def test_short_loop_full_size_teacher_forced():
+    w = W.WORKLOADS["loop8_bf16_b1_v32768_d1024"]
+    case = GpuCase(w)
+    state = case.state()
+    excl = 0
+    for _ in range(w.steps):
+        pre = state_np(state)
+        if pre["done"].all():
+            break
+        out = case.run_step(state)
+        g, post = out_np(out), state_np(state)
+        ref = oracle_step(case, pre)
+        excl += compare_outputs(g, ref, [(0, i) for i in range(w.L)])["excluded"]
+        check_lock_update(pre, g, post, ref, case.inp["tau"], case.inp["seed"], w.V, w.max_steps)
+    assert excl <= 8
+
+
+def test_adaptive_topk_standin_loop_full_size():
+    w = W.WORKLOADS["loop48_topk64_bf16_b4_v262144_d2816"]
+    case = GpuCase(w)
+    Wt = torch.from_numpy(case.inp["W"].view(np.int16)).view(torch.bfloat16).cuda()
+    # graph loop and plain launches agree bit for bit
+    results = []
+    for use_graph in (True, False):
+        state = case.state()
+        out = StepOutputs.empty(w.B, w.L, w.d)
+        Hbuf = torch.zeros(w.B, w.L, w.d, dtype=torch.bfloat16, device="cuda")
+        case.sampler.loop(case.E, case.T, case.tau, state, case.inp["seed"], out, W=Wt, H_buf=Hbuf,
+                          use_graph=use_graph)
+        torch.cuda.synchronize()
+        results.append((state_np(state), out_np(out)))
+    (sa, oa), (sb, ob) = results
+    for k in sa:
+        assert np.array_equal(sa[k], sb[k]), k
+    assert np.array_equal(oa["sampled"], ob["sampled"])
+    assert sa["done"].all() and sa["step"].max() <= w.max_steps
+    assert case.sampler.device_status() == 0
+    # teacher-forced first step on sampled positions: stand-in H, then the step
+    state = case.state()
+    pre = state_np(state)
+    s0 = torch.zeros(w.B, w.L, w.d, dtype=torch.float32, device="cuda")
+    Hbuf = torch.zeros(w.B, w.L, w.d, dtype=torch.bfloat16, device="cuda")
+    case.sampler.standin_hidden(Wt, s0, case.E, state.canvas, state.done, Hbuf)
+    out = StepOutputs.empty(w.B, w.L, w.d)
+    case.sampler.step(Hbuf, case.E, case.T, case.tau, state, case.inp["seed"], out=out)
+    torch.cuda.synchronize()
+    g, post = out_np(out), state_np(state)
+    check_lock_update(pre, g, post, None, case.inp["tau"], case.inp["seed"], w.V, w.max_steps)
+    H_bits = Hbuf.view(torch.int16).cpu().numpy().view(np.uint16)
+    pos = np.array([0, 77, 255])
+    E64 = case.E64
+    for b in range(w.B):
+        standin_close(H_bits[b, pos], case.inp["W"], np.zeros((len(pos), w.d)), E64,
+                      pre["canvas"][b, pos])
+    mask = np.ones(w.B, np.uint8)
+    for b in range(w.B):
+        m = mask.copy()
+        m[b] = 0
+        ref = oracle.sampler_step(oracle.bf16_bits_to_f64(H_bits), E64, case.inp["T"],
+                                  case.inp["tau"], pre["canvas"], pre["lock"], pre["step"], m,
+                                  case.inp["seed"], top_k=w.top_k, max_steps=w.max_steps,
+                                  positions=pos)
+        compare_outputs(g, ref, [(b, int(i)) for i in pos], top_k=w.top_k)

@@ -15,7 +15,7 @@ from canvas_sampler_gb300 import _lib as C
 from canvas_sampler_gb300 import workloads as W
 from canvas_sampler_gb300.sampler import CanvasState, Sampler, StepOutputs, philox4x32_10
 
-from _helpers import GpuCase, compare_outputs, full_step_check, out_np, oracle_step, state_np
+from _helpers import GpuCase, compare_outputs, full_step_check, out_np, oracle_step, standin_close, state_np
 
 pytestmark = pytest.mark.gpu
 
@@ -212,8 +212,5 @@ def test_standin_hidden_matches_oracle():
     case.sampler.standin_hidden(Wt, torch.from_numpy(s_prev).cuda(), case.E, canvas, None, Hout)
     torch.cuda.synchronize()
     got = Hout.view(torch.int16).cpu().numpy().view(np.uint16)
-    want = oracle.standin_hidden(inp["W"], s_prev.astype(np.float64), case.E64, inp["canvas"])
-    # fp32 accumulation + tanhf before the bf16 rounding: allow one bf16 step where they differ
-    diff = np.abs(got.astype(np.int32) - want.astype(np.int32))
-    assert diff.max() <= 1
-    assert (diff > 0).mean() < 1e-3
+    frac = standin_close(got, inp["W"], s_prev.astype(np.float64), case.E64, inp["canvas"])
+    assert frac < 1e-2
