@@ -1,0 +1,155 @@
+// The sampler step without any device allocation.
+//
+// Some callers cannot allocate device memory when they want a step: a serving engine that
+// reserves (almost) all HBM for its own pools at start-up and forbids later allocations, or a
+// latency-critical path where cudaMalloc / cudaFree would synchronise the device and stall
+// other streams. ds_sampler_create allocates a workspace, so such callers get this entry
+// point instead: it needs no sampler object and takes its scratch from one fixed array below.
+//
+// The scratch array is a file-scope __device__ array, so every GPU that loads the library
+// holds it until the process exits. Host code cannot use the array's name as a device
+// address (on the host it names a stand-in object); the address is looked up once per device
+// with cudaGetSymbolAddress while that device is current, and passed to the kernels.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/ds_sampler.h"
+#include "ds_internal.h"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 64ull << 20;  // 64 MiB
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up on first use).
+ds_status scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DS_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return DS_ERR_CUDA;
+    }
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return DS_OK;
+}
+
+struct Carver {
+  unsigned char* base;
+  size_t used = 0;
+  template <class T>
+  T* take(size_t count) {
+    T* p = reinterpret_cast<T*>(base + used);
+    used += (count * sizeof(T) + 255) & ~size_t(255);
+    return p;
+  }
+};
+
+}  // namespace
+
+extern "C" ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg,
+                                             const ds_step_args* a, void* stream) {
+  using namespace ds;
+  if (!cfg || !a) return DS_ERR_INVALID_ARG;
+  const ds_sampler_config& c = *cfg;
+  if (c.canvas_len < 128 || c.canvas_len > 1024 || c.canvas_len % 128) return DS_ERR_INVALID_ARG;
+  if (c.vocab < 256 || c.vocab > (1 << 24) || c.vocab % 256) return DS_ERR_INVALID_ARG;
+  if (c.d_model < 64 || c.d_model > 16384 || c.d_model % 64) return DS_ERR_INVALID_ARG;
+  if (c.dtype != DS_DTYPE_BF16 && c.dtype != DS_DTYPE_FP32) return DS_ERR_INVALID_ARG;
+  if (c.top_k < 0 || c.top_k > kMaxTopK || c.max_steps < 1) return DS_ERR_INVALID_ARG;
+  if (c.impl != DS_IMPL_AUTO && c.impl != DS_IMPL_TENSOR && c.impl != DS_IMPL_SIMT)
+    return DS_ERR_INVALID_ARG;
+  if (a->batch < 1 || (int64_t)a->batch * c.canvas_len > 65535) return DS_ERR_INVALID_ARG;
+  if (!a->H || !a->E || !a->temperature || !a->tau || !a->step || !a->canvas || !a->lock ||
+      !a->done || !a->s || !a->sampled || !a->conf || !a->entropy || !a->argmax)
+    return DS_ERR_INVALID_ARG;
+  auto aligned16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  if (!aligned16(a->H) || !aligned16(a->E) || !aligned16(a->s)) return DS_ERR_INVALID_ARG;
+  const int nc = n_chunks_of(c.vocab);
+  if (c.top_k > 0 && (int64_t)nc * c.top_k > kMaxTopKPool) return DS_ERR_UNSUPPORTED;
+
+  bool tensor = false;
+  if (c.impl != DS_IMPL_SIMT) {
+    const bool ok = c.dtype == DS_DTYPE_BF16 && tc_available();
+    if (c.impl == DS_IMPL_TENSOR && !ok) return DS_ERR_UNSUPPORTED;
+    tensor = ok;
+  }
+  int dev = 0, sms = 1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DS_ERR_CUDA;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  sms = std::max(1, sms);
+
+  const int L = c.canvas_len, d = c.d_model, B = a->batch, R = B * L, k = c.top_k;
+  const int64_t V = c.vocab;
+  int S;
+  if (tensor) {
+    S = selfcond_tc_splits(R, V, d, sms);
+  } else {
+    const long tiles = (long)(d / 64) * (R / 128);
+    long s = (4L * sms + tiles - 1) / tiles;
+    S = (int)std::max(1L, std::min(s, std::min(64L, (long)(V / 1024))));
+  }
+
+  // The scratch this step needs, laid out with 256-byte alignment; refuse what does not fit.
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t RV = (size_t)R * (size_t)V;
+  const size_t need = up(RV * 4) + 2 * up(RV * 2) + up((size_t)R * nc * sizeof(ChunkStat)) +
+                      up((size_t)R * sizeof(RowStat)) + up((size_t)R * nc * sizeof(Best)) +
+                      (k > 0 ? up((size_t)R * nc * k * sizeof(Cand)) : 0) +
+                      up((size_t)S * R * d * 4) + 256;
+  if (need > kNoAllocScratchBytes) return DS_ERR_UNSUPPORTED;
+
+  void* base = nullptr;
+  ds_status st = scratch_address(&base);
+  if (st != DS_OK) return st;
+  Carver cv{static_cast<unsigned char*>(base)};
+  float* Y = cv.take<float>(RV);
+  uint16_t* Phi = cv.take<uint16_t>(RV);
+  uint16_t* Plo = cv.take<uint16_t>(RV);
+  ChunkStat* cs = cv.take<ChunkStat>((size_t)R * nc);
+  RowStat* rs = cv.take<RowStat>((size_t)R);
+  Best* best = cv.take<Best>((size_t)R * nc);
+  Cand* cand = k > 0 ? cv.take<Cand>((size_t)R * nc * k) : nullptr;
+  float* Opart = cv.take<float>((size_t)S * R * d);
+  uint32_t* err = cv.take<uint32_t>(64);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The array keeps the previous call's contents: the error word must start at zero. Every
+  // other region is fully written before it is read in this step.
+  if (cudaMemsetAsync(err, 0, sizeof(uint32_t), s) != cudaSuccess) return DS_ERR_CUDA;
+  const bool fp32 = c.dtype == DS_DTYPE_FP32;
+  if (tensor) {
+    if (launch_logits_tc(static_cast<const uint16_t*>(a->H), static_cast<const uint16_t*>(a->E), R,
+                         V, d, L, a->temperature, a->done, Y, err, s) != cudaSuccess)
+      return DS_ERR_CUDA;
+  } else {
+    launch_logits_simt(a->H, a->E, fp32, R, V, d, L, a->temperature, a->done, Y, s);
+  }
+  launch_chunk_stats(Y, R, V, L, a->done, cs, s);
+  launch_row_merge(cs, nc, R, L, a->done, rs, s);
+  if (k > 0) launch_topk_chunk(Y, R, V, L, a->done, k, cand, s);
+  launch_convert(Y, rs, R, V, L, a->done, a->step, a->seed, k == 0, Phi, Plo, best, s);
+  if (tensor) {
+    if (launch_selfcond_tc(Phi, Plo, static_cast<const uint16_t*>(a->E), R, V, d, L, a->done, S,
+                           Opart, err, s) != cudaSuccess)
+      return DS_ERR_CUDA;
+  } else {
+    launch_selfcond_simt(Phi, Plo, a->E, fp32, R, V, d, L, a->done, S, Opart, s);
+  }
+  launch_reduce_s(Opart, S, R, d, L, a->done, rs, a->s, s);
+  launch_finalize(rs, best, cand, nc, k, R, L, a->done, a->step, a->seed, a->sampled, a->conf,
+                  a->entropy, a->argmax, s);
+  launch_lock(B, L, V, c.max_steps, a->seed, a->tau, a->sampled, a->conf, a->step, a->canvas,
+              a->lock, a->done, s);
+  return cudaGetLastError() == cudaSuccess ? DS_OK : DS_ERR_CUDA;
+}

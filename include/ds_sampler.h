@@ -206,6 +206,28 @@ ds_status ds_sampler_phase_times(ds_sampler* sampler, float* ms, int32_t n, int3
  * a loop captured in a graph counts its kernels once per capture). */
 ds_status ds_sampler_launch_count(const ds_sampler* sampler, int64_t* count);
 
+/* One sampler step that allocates no device memory.
+ * The paper has no counterpart to this entry point; it exists for callers that cannot allocate
+ * when they run a step: a serving engine that reserves (almost) all HBM for its own pools at
+ * start-up and forbids later allocations, or a latency-critical path where cudaMalloc/cudaFree
+ * would synchronise the device and stall other streams. Such callers cannot use
+ * ds_sampler_create (it allocates a workspace), so this call needs no sampler at all.
+ *   cfg   shapes and options as for ds_sampler_create (max_batch is not used);
+ *   args  inputs and outputs exactly as for ds_sampler_step (all [device]); args->batch >= 1.
+ * The step's scratch (logits, statistics, the probability split, partial sums) is carved from
+ * one fixed 64 MiB array inside the library, which every GPU that loads the library holds until
+ * the process exits. A step whose scratch would not fit returns DS_ERR_UNSUPPORTED and enqueues
+ * nothing; the scratch is about 8*B*L*V + 4*S*B*L*d bytes (S = vocabulary splits of the
+ * self-conditioning GEMM), e.g. B=1, L=256, V=32768, d=1024 does not fit and V=16384 does.
+ * The first call on a device looks up the array's device address (a one-time set-up with that
+ * device current); make that first call before any stream capture. Every call shares the one
+ * array and it keeps the last call's contents (the call clears what must start at zero): calls
+ * whose work overlaps on the GPU -- two streams, or two host threads -- race on it and must be
+ * serialised by the caller. Nothing is allocated: no cudaMalloc, cudaFree or allocating library
+ * routine is called. */
+ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg, const ds_step_args* args,
+                                  void* stream);
+
 /* Read-only view of an internal buffer of the last step, for tests and profiling.
  * which: 0 = scaled logits y [B*L, V] float; 1 = row statistics [B*L] x {m, l, entropy, argmax};
  * 2 = bf16 high part of exp(y - m) [B*L, V]; 3 = bf16 low part. *ptr is [device]. */

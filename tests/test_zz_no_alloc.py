@@ -1,0 +1,80 @@
+"""The no-allocation step entry point against the regular one.
+
+ds_sampler_step_noalloc serves callers that cannot allocate device memory at step time (a
+serving engine that has reserved nearly all HBM for its own pools, or a latency-critical path
+that must not let cudaMalloc synchronise the device); it keeps its scratch in one fixed array
+inside the library instead of a sampler's workspace. This file runs last so that a failure here
+cannot hide failures elsewhere, and it passes both alone and after the other tests.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from canvas_sampler_gb300 import _lib as C
+from canvas_sampler_gb300 import workloads as W
+from canvas_sampler_gb300.sampler import CanvasState, Sampler, StepOutputs
+
+pytestmark = pytest.mark.gpu
+
+REL_TOL = 2e-5
+
+
+def _inputs(B=2, V=8192, d=256):
+    w = W.scaled(W.WORKLOADS["step_bf16_b8_v262144_d2816"], V=V, d=d, B=B)
+    inp = W.make_inputs(w)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    return w, inp, dev(inp["E"]), dev(inp["H"]), torch.from_numpy(inp["T"]).cuda(), \
+        torch.from_numpy(inp["tau"]).cuda()
+
+
+def _args(sampler, H, E, T, tau, state, out, seed):
+    return sampler._step_args(H, E, T, tau, state, out, seed)
+
+
+def _close(a: StepOutputs, b: StepOutputs):
+    for k in ("sampled", "argmax"):
+        assert torch.equal(getattr(a, k), getattr(b, k)), k
+    for k in ("conf", "entropy"):
+        x, y = getattr(a, k).double(), getattr(b, k).double()
+        assert torch.all((x - y).abs() <= REL_TOL * y.abs().clamp_min(1.0)), k
+    rel = (a.s.double() - b.s.double()).norm(dim=-1) / b.s.double().norm(dim=-1)
+    assert rel.max().item() <= REL_TOL
+
+
+def test_no_alloc_step_matches_the_sampler_step_twice_in_a_row():
+    lib = C.load_library()
+    w, inp, E, H, T, tau = _inputs()
+    ref = Sampler(w.V, w.d, canvas_len=w.L, max_batch=w.B, dtype="bf16", max_steps=w.max_steps)
+    cfg = ref._cfg
+    st_ref = CanvasState.from_numpy(inp["canvas"], inp["lock"], inp["step"], inp["done"])
+    st_new = st_ref.clone()
+    for call in range(2):  # the second call continues the canvas from the first call's state
+        out_ref = ref.step(H, E, T, tau, st_ref, inp["seed"])
+        out_new = StepOutputs.empty(w.B, w.L, w.d)
+        a = _args(ref, H, E, T, tau, st_new, out_new, inp["seed"])
+        rc = lib.ds_sampler_step_noalloc(ctypes.byref(cfg), ctypes.byref(a),
+                                         torch.cuda.current_stream().cuda_stream)
+        assert rc == C.DS_OK, C.status_string(rc)
+        torch.cuda.synchronize()
+        _close(out_new, out_ref)
+        for k in ("canvas", "lock", "step", "done"):
+            assert torch.equal(getattr(st_new, k), getattr(st_ref, k)), (call, k)
+    assert int(st_new.step[0]) == 2
+
+
+def test_no_alloc_step_rejects_what_does_not_fit():
+    lib = C.load_library()
+    w, inp, E, H, T, tau = _inputs(B=1, V=32768, d=256)
+    ref = Sampler(w.V, w.d, canvas_len=w.L, max_batch=1, dtype="bf16")
+    st = CanvasState.from_numpy(inp["canvas"], inp["lock"], inp["step"], inp["done"])
+    out = StepOutputs.empty(1, w.L, w.d)
+    out.sampled.fill_(-3)
+    cfg = C.ds_sampler_config(max_batch=1, canvas_len=w.L, d_model=w.d, dtype=0, vocab=w.V,
+                              top_k=0, max_steps=48, impl=0, reserved=0)
+    a = _args(ref, H, E, T, tau, st, out, 1)
+    rc = lib.ds_sampler_step_noalloc(ctypes.byref(cfg), ctypes.byref(a), None)
+    assert rc == C.DS_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert torch.all(out.sampled == -3)  # nothing was enqueued
