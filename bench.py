@@ -46,6 +46,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=W.BENCH_WORKLOAD, choices=sorted(W.WORKLOADS))
     ap.add_argument("--kernel-impl", default="auto", choices=["auto", "tensor", "simt"])
+    ap.add_argument("--vocab", type=int, default=None, help="override V (profiling runs)")
+    ap.add_argument("--batch", type=int, default=None, help="override B (profiling runs)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-positions", type=int, default=32,
@@ -166,11 +168,18 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def workload_of(args) -> W.Workload:
+    w = W.WORKLOADS[args.workload]
+    if args.vocab or args.batch:
+        w = W.scaled(w, V=args.vocab or w.V, B=args.batch or w.B)
+    return w
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    w = W.WORKLOADS[args.workload]
+    w = workload_of(args)
     inp = W.make_inputs(w)
     import oracle
     E64 = oracle.bf16_bits_to_f64(inp["E"]) if w.dtype == "bf16" else inp["E"].astype(np.float64)
@@ -211,7 +220,7 @@ def run_ours(args):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = W.WORKLOADS[args.workload]
+    w = workload_of(args)
     inp = W.make_inputs(w)
     seed = inp["seed"] + rank  # each rank samples its own canvas
 
