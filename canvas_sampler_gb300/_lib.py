@@ -52,6 +52,7 @@ class ds_loop_args(ctypes.Structure):
 SIGNATURES = {
     "ds_abi_version": (c_int32, []),
     "ds_status_string": (c_char_p, [c_int32]),
+    "ds_last_cuda_error": (c_char_p, []),
     "ds_sampler_create": (c_int32, [POINTER(ds_sampler_config), POINTER(c_void_p)]),
     "ds_sampler_destroy": (c_int32, [c_void_p]),
     "ds_sampler_workspace_bytes": (c_int32, [c_void_p, POINTER(c_size_t)]),
@@ -104,6 +105,8 @@ def status_string(status: int) -> str:
 
 def check(status: int, what: str) -> None:
     if status != DS_OK:
+        if status in (DS_ERR_CUDA, DS_ERR_OOM):
+            what = f"{what} [{load_library().ds_last_cuda_error().decode()}]"
         raise DsError(status, what)
 
 

@@ -100,8 +100,11 @@ int splits_for(const ds_sampler* s, int batch) {
   return (int)std::max(1L, S);
 }
 
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
 ds_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return DS_OK;
+  t_last_cuda_error = e;
   if (e == cudaErrorMemoryAllocation) return DS_ERR_OOM;
   return DS_ERR_CUDA;
 }
@@ -130,14 +133,16 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
   if (s->impl == DS_IMPL_TENSOR) {
     cudaError_t e = launch_logits_tc(static_cast<const uint16_t*>(a->H),
                                      static_cast<const uint16_t*>(a->E), R, V, d, L,
-                                     a->temperature, a->done, s->Y, s->err, st);
+                                     a->temperature, a->done, s->Y, s->cs, s->err, st);
     if (e != cudaSuccess) return cuda_status(e);
+    mark(s, 0, st);
+    launch_row_merge(s->cs, (int)(V / kTcSegment), R, L, a->done, s->rs, st);
   } else {
     launch_logits_simt(a->H, a->E, fp32, R, V, d, L, a->temperature, a->done, s->Y, st);
+    mark(s, 0, st);
+    launch_chunk_stats(s->Y, R, V, L, a->done, s->cs, st);
+    launch_row_merge(s->cs, s->n_chunks, R, L, a->done, s->rs, st);
   }
-  mark(s, 0, st);
-  launch_chunk_stats(s->Y, R, V, L, a->done, s->cs, st);
-  launch_row_merge(s->cs, s->n_chunks, R, L, a->done, s->rs, st);
   mark(s, 1, st);
   if (k > 0) launch_topk_chunk(s->Y, R, V, L, a->done, k, s->cand, st);
   mark(s, 2, st);
@@ -163,7 +168,7 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
     ++s->timed_steps;
     s->timed_stream = st;
   }
-  s->launches += 8 + (k > 0 ? 1 : 0);
+  s->launches += (s->impl == DS_IMPL_TENSOR ? 7 : 8) + (k > 0 ? 1 : 0);
   return cuda_status(cudaGetLastError());
 }
 
@@ -222,6 +227,8 @@ void free_all(ds_sampler* s) {
 extern "C" {
 
 int32_t ds_abi_version(void) { return DS_SAMPLER_ABI_VERSION; }
+
+const char* ds_last_cuda_error(void) { return cudaGetErrorString(t_last_cuda_error); }
 
 const char* ds_status_string(ds_status status) {
   switch (status) {
@@ -284,7 +291,7 @@ ds_status ds_sampler_create(const ds_sampler_config* cfg, ds_sampler** out) {
   s->Y = carve<float>(s, Rm * V, &e);
   s->Phi = carve<uint16_t>(s, Rm * V, &e);
   s->Plo = carve<uint16_t>(s, Rm * V, &e);
-  s->cs = carve<ChunkStat>(s, Rm * n_chunks, &e);
+  s->cs = carve<ChunkStat>(s, Rm * std::max<size_t>(n_chunks, V / kTcSegment), &e);
   s->rs = carve<RowStat>(s, Rm, &e);
   s->best = carve<Best>(s, Rm * n_chunks, &e);
   if (c.top_k > 0) s->cand = carve<Cand>(s, Rm * n_chunks * c.top_k, &e);

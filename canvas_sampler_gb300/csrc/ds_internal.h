@@ -57,9 +57,12 @@ void launch_standin_simt(const uint16_t* W, const float* s_prev, const uint16_t*
 // Resolves the driver's tensor-map encoder; false when unavailable.
 bool tc_available();
 int tc_num_sms();
+// Also writes the softmax statistics of every 128-token segment of every row:
+// seg_stats [R, V / kTcSegment].
+constexpr int kTcSegment = 128;
 cudaError_t launch_logits_tc(const uint16_t* H, const uint16_t* E, int R, int64_t V, int d, int L,
-                             const float* T, const uint8_t* done, float* Y, uint32_t* err,
-                             cudaStream_t st);
+                             const float* T, const uint8_t* done, float* Y, ChunkStat* seg_stats,
+                             uint32_t* err, cudaStream_t st);
 cudaError_t launch_selfcond_tc(const uint16_t* Phi, const uint16_t* Plo, const uint16_t* E, int R,
                                int64_t V, int d, int L, const uint8_t* done, int S, float* Opart,
                                uint32_t* err, cudaStream_t st);

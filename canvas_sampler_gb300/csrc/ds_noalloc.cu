@@ -103,7 +103,8 @@ extern "C" ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg,
   // The scratch this step needs, laid out with 256-byte alignment; refuse what does not fit.
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   const size_t RV = (size_t)R * (size_t)V;
-  const size_t need = up(RV * 4) + 2 * up(RV * 2) + up((size_t)R * nc * sizeof(ChunkStat)) +
+  const size_t nstat = std::max<size_t>(nc, (size_t)(V / kTcSegment));
+  const size_t need = up(RV * 4) + 2 * up(RV * 2) + up((size_t)R * nstat * sizeof(ChunkStat)) +
                       up((size_t)R * sizeof(RowStat)) + up((size_t)R * nc * sizeof(Best)) +
                       (k > 0 ? up((size_t)R * nc * k * sizeof(Cand)) : 0) +
                       up((size_t)S * R * d * 4) + 256;
@@ -116,7 +117,7 @@ extern "C" ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg,
   float* Y = cv.take<float>(RV);
   uint16_t* Phi = cv.take<uint16_t>(RV);
   uint16_t* Plo = cv.take<uint16_t>(RV);
-  ChunkStat* cs = cv.take<ChunkStat>((size_t)R * nc);
+  ChunkStat* cs = cv.take<ChunkStat>((size_t)R * nstat);
   RowStat* rs = cv.take<RowStat>((size_t)R);
   Best* best = cv.take<Best>((size_t)R * nc);
   Cand* cand = k > 0 ? cv.take<Cand>((size_t)R * nc * k) : nullptr;
@@ -130,13 +131,14 @@ extern "C" ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg,
   const bool fp32 = c.dtype == DS_DTYPE_FP32;
   if (tensor) {
     if (launch_logits_tc(static_cast<const uint16_t*>(a->H), static_cast<const uint16_t*>(a->E), R,
-                         V, d, L, a->temperature, a->done, Y, err, s) != cudaSuccess)
+                         V, d, L, a->temperature, a->done, Y, cs, err, s) != cudaSuccess)
       return DS_ERR_CUDA;
+    launch_row_merge(cs, (int)(V / kTcSegment), R, L, a->done, rs, s);
   } else {
     launch_logits_simt(a->H, a->E, fp32, R, V, d, L, a->temperature, a->done, Y, s);
+    launch_chunk_stats(Y, R, V, L, a->done, cs, s);
+    launch_row_merge(cs, nc, R, L, a->done, rs, s);
   }
-  launch_chunk_stats(Y, R, V, L, a->done, cs, s);
-  launch_row_merge(cs, nc, R, L, a->done, rs, s);
   if (k > 0) launch_topk_chunk(Y, R, V, L, a->done, k, cand, s);
   launch_convert(Y, rs, R, V, L, a->done, a->step, a->seed, k == 0, Phi, Plo, best, s);
   if (tensor) {

@@ -8,13 +8,13 @@
 // Definitions: DiffusionGemma Technical Report, section 6 "Sampling" (logits and softmax over
 // the full vocabulary in full precision; the self-conditioning embedding matmul).
 //
-// Structure (both kernels): one persistent CTA per SM, 6 warps.
+// Structure (both kernels): one persistent CTA per SM, 10 warps.
 //   warp 0  one thread issues TMA copies of the operand tiles into a ring of shared-memory
 //           stages (128-byte swizzle), completion counted on "full" mbarriers;
 //   warp 1  allocates 512 TMEM columns; one thread issues tcgen05.mma into one of two TMEM
 //           accumulators and commits "empty" (stage reusable) and "tmem full" barriers;
-//   warps 2-5 drain the other accumulator (tcgen05.ld, lane = row) while the next tile's
-//           MMAs run, then arrive on "tmem empty".
+//   warps 2-9 drain the other accumulator (tcgen05.ld, lane = row) into fp32 registers while
+//           the next chunk's MMAs run, then arrive on "tmem empty".
 // Every wait is bounded; on a time-out the CTA raises an abort flag, records the device error
 // word, waits (bounded) for its copies and MMAs in flight, frees TMEM and exits.
 #include <cudaTypedefs.h>
@@ -27,8 +27,9 @@
 namespace ds {
 namespace {
 
-constexpr int kThreadsTC = 192;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
+constexpr int kEpiWarps = 8;
+constexpr int kThreadsTC = 64 + 32 * kEpiWarps;
 
 struct Ctl {
   uint64_t full[4];
@@ -60,7 +61,7 @@ DS_DEV void ctl_init(Ctl& c, int stages) {
   }
   for (int b = 0; b < 2; ++b) {
     mbar_init(smem_u32(&c.tfull[b]), 1);
-    mbar_init(smem_u32(&c.tempty[b]), 128);
+    mbar_init(smem_u32(&c.tempty[b]), 32 * kEpiWarps);
   }
   mbar_init(smem_u32(&c.mma_done), 1);
   c.abort = 0;
@@ -76,9 +77,34 @@ DS_DEV void producer_drain(Ctl& c, int issued, int stages) {
 }
 
 // ------------------------------------------------------------------------------------------
-// logits
+// Two-level accumulation. The tensor core's fp32 accumulator rounds toward zero, so its error
+// grows linearly with the number of MMAs accumulated into it. Each tile is therefore
+// accumulated in short chunks: the MMA thread accumulates one chunk into one of two TMEM
+// buffers while the epilogue warps add the other buffer into fp32 registers (round to nearest),
+// so no TMEM accumulation chain is longer than one chunk.
+// Epilogue warps: warp w >= 2 reads TMEM lane quadrant (w % 4) and column half (w - 2) / 4.
 // ------------------------------------------------------------------------------------------
-constexpr int LG_BM = 128, LG_BN = 256, LG_BK = 64, LG_STAGES = 4;
+
+// Add COLS fp32 TMEM columns starting at taddr (this warp's 32 lanes) to acc[0..COLS).
+// Loads go 16 columns at a time to keep register pressure low next to the accumulator
+// (registers are charged per group of four warps, so a 10-warp CTA gets at most 168 each).
+template <int COLS>
+DS_DEV void tmem_accumulate(uint32_t taddr, float (&acc)[COLS]) {
+#pragma unroll
+  for (int c = 0; c < COLS / 16; ++c) {
+    uint32_t r[16];
+    tmem_ld_16cols(taddr + (uint32_t)(c * 16), r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[c * 16 + i] += __uint_as_float(r[i]);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// logits (+ softmax statistics of each 128-token segment of a row)
+// ------------------------------------------------------------------------------------------
+constexpr int LG_BM = 128, LG_BN = 256, LG_BK = 64, LG_STAGES = 4, LG_CHUNK_KB = 2;
+constexpr int LG_COLS = LG_BN / 2;
 constexpr uint32_t LG_A_BYTES = LG_BM * LG_BK * 2;
 constexpr uint32_t LG_B_BYTES = LG_BN * LG_BK * 2;
 constexpr uint32_t LG_STAGE_BYTES = LG_A_BYTES + LG_B_BYTES;
@@ -87,15 +113,18 @@ constexpr size_t LG_SMEM = (size_t)LG_STAGES * LG_STAGE_BYTES + 1024;
 __global__ void __launch_bounds__(kThreadsTC, 1)
     k_logits_tc(const __grid_constant__ CUtensorMap mapH, const __grid_constant__ CUtensorMap mapE,
                 int R, int64_t V, int d, int L, const float* __restrict__ T,
-                const uint8_t* __restrict__ done, float* __restrict__ Y, uint32_t* err) {
+                const uint8_t* __restrict__ done, float* __restrict__ Y,
+                ChunkStat* __restrict__ seg_stats, uint32_t* err) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Ctl ctl;
   uint8_t* smem = align1024(dyn_smem);
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_rt = R / LG_BM;
-  const int n_tiles = n_rt * (int)(V / LG_BN);
+  const int n_ct = (int)(V / LG_BN);
+  const int n_tiles = n_rt * n_ct;
   const int nk = d / LG_BK;
+  const int n_ch = (nk + LG_CHUNK_KB - 1) / LG_CHUNK_KB;
   if (threadIdx.x == 0) ctl_init(ctl, LG_STAGES);
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&mapH);
@@ -142,71 +171,107 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(LG_BM, LG_BN, false, false);
-      int stage = 0, it = 0;
+      int stage = 0, cc = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
         const int rt = tile % n_rt;
         if (done && done[(rt * LG_BM) / L]) continue;
-        const int buf = it & 1;
-        const uint32_t par = (uint32_t)((it >> 1) & 1);
-        if (!mbar_wait(smem_u32(&ctl.tempty[buf]), par ^ 1, abort_flag, err)) break;
-        tc_fence_after();
-        const uint32_t dt = tmem + (uint32_t)(buf * LG_BN);
-        for (int kc = 0; kc < nk; ++kc) {
-          if (!mbar_wait(smem_u32(&ctl.full[stage]), phase, abort_flag, err)) {
+        for (int ch = 0; ch < n_ch && ok; ++ch, ++cc) {
+          const int buf = cc & 1;
+          const uint32_t par = (uint32_t)((cc >> 1) & 1);
+          if (!mbar_wait(smem_u32(&ctl.tempty[buf]), par ^ 1, abort_flag, err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          *(volatile int*)&ctl.consumed = ctl.consumed + 1;
-          const uint32_t sa = sbase + stage * LG_STAGE_BYTES, sb = sa + LG_A_BYTES;
+          const uint32_t dt = tmem + (uint32_t)(buf * LG_BN);
+          const int kc0 = ch * LG_CHUNK_KB, kc1 = min(nk, kc0 + LG_CHUNK_KB);
+          for (int kc = kc0; kc < kc1; ++kc) {
+            if (!mbar_wait(smem_u32(&ctl.full[stage]), phase, abort_flag, err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            *(volatile int*)&ctl.consumed = ctl.consumed + 1;
+            const uint32_t sa = sbase + stage * LG_STAGE_BYTES, sb = sa + LG_A_BYTES;
 #pragma unroll
-          for (int k = 0; k < LG_BK / 16; ++k)
-            umma_bf16(dt, sdesc_sw128(sa + 32 * k, 16, 1024), sdesc_sw128(sb + 32 * k, 16, 1024),
-                      idesc, (kc | k) ? 1u : 0u);
-          umma_commit(smem_u32(&ctl.empty[stage]));
-          if (++stage == LG_STAGES) {
-            stage = 0;
-            phase ^= 1;
+            for (int k = 0; k < LG_BK / 16; ++k)
+              umma_bf16(dt, sdesc_sw128(sa + 32 * k, 16, 1024),
+                        sdesc_sw128(sb + 32 * k, 16, 1024), idesc, (kc != kc0 || k) ? 1u : 0u);
+            umma_commit(smem_u32(&ctl.empty[stage]));
+            if (++stage == LG_STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
+          if (!ok) break;
+          umma_commit(smem_u32(&ctl.tfull[buf]));
         }
-        if (!ok) break;
-        umma_commit(smem_u32(&ctl.tfull[buf]));
-        ++it;
       }
       umma_commit(smem_u32(&ctl.mma_done));
       mbar_wait_quiet(smem_u32(&ctl.mma_done), 0);
     }
   } else {
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int q = warp & 3;              // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;    // column half of the tile
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    int it = 0;
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    int cc = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
       const int rt = tile % n_rt, ct = tile / n_rt;
       const int b = (rt * LG_BM) / L;
       if (done && done[b]) continue;
-      const int buf = it & 1;
-      const uint32_t par = (uint32_t)((it >> 1) & 1);
-      if (!mbar_wait(smem_u32(&ctl.tfull[buf]), par, abort_flag, err)) break;
-      tc_fence_after();
+      float acc[LG_COLS];
+#pragma unroll
+      for (int i = 0; i < LG_COLS; ++i) acc[i] = 0.f;
+      for (int ch = 0; ch < n_ch; ++ch, ++cc) {
+        const int buf = cc & 1;
+        const uint32_t par = (uint32_t)((cc >> 1) & 1);
+        if (!mbar_wait(smem_u32(&ctl.tfull[buf]), par, abort_flag, err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_accumulate<LG_COLS>(tmem + (uint32_t)(buf * LG_BN + half * LG_COLS) + lane_base, acc);
+        tc_fence_before();
+        mbar_arrive(smem_u32(&ctl.tempty[buf]));
+      }
+      if (!ok) break;
+      // y = z / T (as z * (1/T)); the segment's max, argmax (lowest token), sum of exp(y - m)
+      // and sum of exp(y - m) (y - m)
       const float invT = 1.0f / T[b];
       const int row = rt * LG_BM + q * 32 + lane;
-      float* yrow = Y + (size_t)row * V + (size_t)ct * LG_BN;
-#pragma unroll 1
-      for (int c = 0; c < LG_BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32cols(tmem + (uint32_t)(buf * LG_BN + c * 32) + lane_base, r);
-        tmem_ld_wait();
+      const int64_t j0 = (int64_t)ct * LG_BN + half * LG_COLS;
+      // (x * invT is monotone in x for invT > 0, so the max of the scaled values is the
+      // scaled max, at the same lowest index)
+      float zmax = -INFINITY;
+      int arg = 0;
 #pragma unroll
-        for (int v = 0; v < 8; ++v)
-          *reinterpret_cast<float4*>(yrow + c * 32 + 4 * v) =
-              make_float4(__uint_as_float(r[4 * v]) * invT, __uint_as_float(r[4 * v + 1]) * invT,
-                          __uint_as_float(r[4 * v + 2]) * invT, __uint_as_float(r[4 * v + 3]) * invT);
+      for (int i = 0; i < LG_COLS; ++i) {
+        if (acc[i] > zmax) {
+          zmax = acc[i];
+          arg = i;
+        }
       }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&ctl.tempty[buf]));
-      ++it;
+      const float m = zmax * invT;
+      float l = 0.f, a = 0.f;
+      float* yrow = Y + (size_t)row * V + j0;
+#pragma unroll
+      for (int v = 0; v < LG_COLS / 4; ++v) {
+        float y4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          y4[e] = acc[4 * v + e] * invT;
+          const float t = y4[e] - m;
+          const float x = expf(t);
+          l += x;
+          a = fmaf(x, t, a);
+        }
+        *reinterpret_cast<float4*>(yrow + 4 * v) = make_float4(y4[0], y4[1], y4[2], y4[3]);
+      }
+      seg_stats[(size_t)row * (V / LG_COLS) + (j0 / LG_COLS)] =
+          ChunkStat{m, l, a, (int32_t)(j0 + arg)};
     }
   }
   tc_fence_before();
@@ -220,7 +285,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 // ------------------------------------------------------------------------------------------
 // self-conditioning partials
 // ------------------------------------------------------------------------------------------
-constexpr int SC_BM = 128, SC_BK = 64, SC_STAGES = 3, SC_BN_MAX = 256;
+constexpr int SC_BM = 128, SC_BK = 64, SC_STAGES = 3, SC_BN_MAX = 256, SC_CHUNK_KB = 4;
 constexpr uint32_t SC_A_BYTES = SC_BM * SC_BK * 2;        // one of hi / lo
 constexpr uint32_t SC_BOX_BYTES = 64 * SC_BK * 2;          // 64 d-columns x 64 tokens
 constexpr uint32_t SC_STAGE_BYTES = 2 * SC_A_BYTES + (SC_BN_MAX / 64) * SC_BOX_BYTES;
@@ -233,6 +298,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                   const __grid_constant__ CUtensorMap mapE, int R, int64_t V, int d, int L,
                   int S, int kb_per_split, const uint8_t* __restrict__ done,
                   float* __restrict__ Opart, uint32_t* err) {
+  constexpr int COLS = BN / 2;
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Ctl ctl;
   uint8_t* smem = align1024(dyn_smem);
@@ -304,77 +370,86 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(SC_BM, BN, false, true);
-      int stage = 0, it = 0;
+      int stage = 0, cc = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
         int split, rt, dt, kb0, kb1;
         item_coords(w, split, rt, dt, kb0, kb1);
         if (done && done[(rt * SC_BM) / L]) continue;
-        const int buf = it & 1;
-        const uint32_t par = (uint32_t)((it >> 1) & 1);
-        if (!mbar_wait(smem_u32(&ctl.tempty[buf]), par ^ 1, abort_flag, err)) break;
-        tc_fence_after();
-        const uint32_t dtm = tmem + (uint32_t)(buf * BN);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(smem_u32(&ctl.full[stage]), phase, abort_flag, err)) {
+        for (int c0 = kb0; c0 < kb1 && ok; c0 += SC_CHUNK_KB, ++cc) {
+          const int buf = cc & 1;
+          const uint32_t par = (uint32_t)((cc >> 1) & 1);
+          if (!mbar_wait(smem_u32(&ctl.tempty[buf]), par ^ 1, abort_flag, err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          *(volatile int*)&ctl.consumed = ctl.consumed + 1;
-          const uint32_t sa = sbase + stage * SC_STAGE_BYTES;
-          const uint32_t sb = sa + 2 * SC_A_BYTES;
+          const uint32_t dtm = tmem + (uint32_t)(buf * BN);
+          const int c1 = min(kb1, c0 + SC_CHUNK_KB);
+          for (int kb = c0; kb < c1; ++kb) {
+            if (!mbar_wait(smem_u32(&ctl.full[stage]), phase, abort_flag, err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            *(volatile int*)&ctl.consumed = ctl.consumed + 1;
+            const uint32_t sa = sbase + stage * SC_STAGE_BYTES;
+            const uint32_t sb = sa + 2 * SC_A_BYTES;
 #pragma unroll
-          for (int k = 0; k < SC_BK / 16; ++k) {
-            // B = E tile, tokens x d-columns with d contiguous: MN-major, 64-column boxes
-            // SC_BOX_BYTES apart (leading offset), 8-token groups 1024 B apart (stride offset).
-            const uint64_t bdesc = sdesc_sw128(sb + k * 16 * 128, SC_BOX_BYTES, 1024);
-            umma_bf16(dtm, sdesc_sw128(sa + 32 * k, 16, 1024), bdesc, idesc,
-                      (kb != kb0 || k != 0) ? 1u : 0u);
-            umma_bf16(dtm, sdesc_sw128(sa + SC_A_BYTES + 32 * k, 16, 1024), bdesc, idesc, 1u);
+            for (int k = 0; k < SC_BK / 16; ++k) {
+              // B = E tile, tokens x d-columns with d contiguous: MN-major, 64-column boxes
+              // SC_BOX_BYTES apart (leading offset), 8-token groups 1024 B apart (stride offset).
+              const uint64_t bdesc = sdesc_sw128(sb + k * 16 * 128, SC_BOX_BYTES, 1024);
+              umma_bf16(dtm, sdesc_sw128(sa + 32 * k, 16, 1024), bdesc, idesc,
+                        (kb != c0 || k != 0) ? 1u : 0u);
+              umma_bf16(dtm, sdesc_sw128(sa + SC_A_BYTES + 32 * k, 16, 1024), bdesc, idesc, 1u);
+            }
+            umma_commit(smem_u32(&ctl.empty[stage]));
+            if (++stage == SC_STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
-          umma_commit(smem_u32(&ctl.empty[stage]));
-          if (++stage == SC_STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
+          if (!ok) break;
+          umma_commit(smem_u32(&ctl.tfull[buf]));
         }
-        if (!ok) break;
-        umma_commit(smem_u32(&ctl.tfull[buf]));
-        ++it;
       }
       umma_commit(smem_u32(&ctl.mma_done));
       mbar_wait_quiet(smem_u32(&ctl.mma_done), 0);
     }
   } else {
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    int it = 0;
-    for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
+    int cc = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
       int split, rt, dt, kb0, kb1;
       item_coords(w, split, rt, dt, kb0, kb1);
       if (done && done[(rt * SC_BM) / L]) continue;
-      const int buf = it & 1;
-      const uint32_t par = (uint32_t)((it >> 1) & 1);
-      if (!mbar_wait(smem_u32(&ctl.tfull[buf]), par, abort_flag, err)) break;
-      tc_fence_after();
-      const int row = rt * SC_BM + q * 32 + lane;
-      float* orow = Opart + ((size_t)split * R + row) * d + (size_t)dt * BN;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32cols(tmem + (uint32_t)(buf * BN + c * 32) + lane_base, r);
-        tmem_ld_wait();
+      float acc[COLS];
 #pragma unroll
-        for (int v = 0; v < 8; ++v)
-          *reinterpret_cast<float4*>(orow + c * 32 + 4 * v) =
-              make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                          __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+      for (int i = 0; i < COLS; ++i) acc[i] = 0.f;
+      for (int c0 = kb0; c0 < kb1; c0 += SC_CHUNK_KB, ++cc) {
+        const int buf = cc & 1;
+        const uint32_t par = (uint32_t)((cc >> 1) & 1);
+        if (!mbar_wait(smem_u32(&ctl.tfull[buf]), par, abort_flag, err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_accumulate<COLS>(tmem + (uint32_t)(buf * BN + half * COLS) + lane_base, acc);
+        tc_fence_before();
+        mbar_arrive(smem_u32(&ctl.tempty[buf]));
       }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&ctl.tempty[buf]));
-      ++it;
+      if (!ok) break;
+      const int row = rt * SC_BM + q * 32 + lane;
+      float* orow = Opart + ((size_t)split * R + row) * d + (size_t)dt * BN + half * COLS;
+#pragma unroll
+      for (int v = 0; v < COLS / 4; ++v)
+        *reinterpret_cast<float4*>(orow + 4 * v) =
+            make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
     }
   }
   tc_fence_before();
@@ -460,8 +535,8 @@ int selfcond_tc_splits(int R, int64_t V, int d, int num_sms) {
 }
 
 cudaError_t launch_logits_tc(const uint16_t* H, const uint16_t* E, int R, int64_t V, int d, int L,
-                             const float* T, const uint8_t* done, float* Y, uint32_t* err,
-                             cudaStream_t st) {
+                             const float* T, const uint8_t* done, float* Y, ChunkStat* seg_stats,
+                             uint32_t* err, cudaStream_t st) {
   if (!tc_available()) return cudaErrorNotSupported;
   CUtensorMap mH, mE;
   if (!make_map(&mH, H, (uint64_t)R, (uint64_t)d, LG_BM, LG_BK) ||
@@ -469,7 +544,7 @@ cudaError_t launch_logits_tc(const uint16_t* H, const uint16_t* E, int R, int64_
     return cudaErrorInvalidValue;
   const int n_tiles = (R / LG_BM) * (int)(V / LG_BN);
   const int grid = std::max(1, std::min(n_tiles, g_sms));
-  k_logits_tc<<<grid, kThreadsTC, LG_SMEM, st>>>(mH, mE, R, V, d, L, T, done, Y, err);
+  k_logits_tc<<<grid, kThreadsTC, LG_SMEM, st>>>(mH, mE, R, V, d, L, T, done, Y, seg_stats, err);
   return cudaGetLastError();
 }
 

@@ -152,6 +152,10 @@ int32_t ds_abi_version(void);
 /* Static string for a status code; never NULL. */
 const char* ds_status_string(ds_status status);
 
+/* Message of the last CUDA runtime error seen by an entry point on the calling thread (the
+ * detail behind DS_ERR_CUDA / DS_ERR_OOM); "no error" if none. Static storage; never NULL. */
+const char* ds_last_cuda_error(void);
+
 /* Create a sampler on the current CUDA device: validates `cfg`, allocates the workspace for
  * cfg->max_batch. On success *out owns the sampler (free it with ds_sampler_destroy). */
 ds_status ds_sampler_create(const ds_sampler_config* cfg, ds_sampler** out);

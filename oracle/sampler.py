@@ -123,9 +123,8 @@ def _sample_row(y_row, g_row, p_row, top_k, band=1e-4):
     """Gumbel-max over the row (or its top-k set).
 
     Returns (x, c, margin of the top two perturbed logits, top-k risk). The risk flag is a
-    diagnostic for comparisons only: it is set when a token whose logit lies within `band` of
-    the k-th largest (so that a slightly different logit could move it across the top-k
-    boundary) has a perturbed logit within `band` of the winner's."""
+    diagnostic for comparisons only: it is set when logits that differ by less than `band`
+    could change the top-k set in a way that changes the sample."""
     risk = False
     if top_k and top_k < y_row.shape[0]:
         cand = _top_k_set(y_row, top_k)
@@ -135,8 +134,16 @@ def _sample_row(y_row, g_row, p_row, top_k, band=1e-4):
         w = np.exp(y_row[cand] - y_row[cand].max())
         c = float(w[best] / w.sum())
         vs = np.sort(v)
-        near = np.abs(y_row - y_row[cand].min()) < band
-        risk = bool(np.any(near & (y_row + g_row >= v[best] - band)))
+        # the set is ambiguous only if a token outside it comes within `band` of its k-th
+        # logit; then the sample is at risk if the winner sits in that band (it could drop
+        # out) or an outside token in the band would beat it
+        yk = y_row[cand].min()
+        outside = np.ones(y_row.shape[0], bool)
+        outside[cand] = False
+        near_out = outside & (y_row > yk - band)
+        if near_out.any():
+            risk = bool(y_row[x] < yk + band or
+                        np.any(near_out & (y_row + g_row >= v[best] - band)))
     else:
         v = y_row + g_row
         x = int(np.argmax(v))
