@@ -129,9 +129,21 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def measured_traffic(kernel_src: str):
+KERNEL_SOURCES = [os.path.join(ROOT, "canvas_sampler_gb300", "csrc", f)
+                  for f in ("ds_tc_selfcond.cu", "ds_tc_common.cuh", "ds_common.cuh")]
+
+
+def kernel_source_hash() -> str:
+    """sha256 over the self-conditioning kernel's sources (the files it is compiled from)."""
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()
+
+
+def measured_traffic():
     """DRAM bytes per launch of the self-conditioning kernel from the committed ncu summary,
-    if the kernel source has not changed since the capture (else None)."""
+    if the kernel's sources have not changed since the capture (else None)."""
     try:
         text = open(PROFILE_FILE).read()
     except OSError:
@@ -140,8 +152,7 @@ def measured_traffic(kernel_src: str):
     m_h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
     if not (m_b and m_h):
         return None
-    h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
-    return float(m_b.group(1)) if h == m_h.group(1) else None
+    return float(m_b.group(1)) if kernel_source_hash() == m_h.group(1) else None
 
 
 def algorithmic_flops(w: W.Workload) -> float:
@@ -332,7 +343,7 @@ def run_ours(args):
     roof = None
     if dom_flops and dom_ms > 0:
         ach = dom_flops / (dom_ms / 1e3) / 1e12
-        traffic = measured_traffic(os.path.join(ROOT, "canvas_sampler_gb300", "csrc", "ds_tc.cu"))
+        traffic = measured_traffic()
         roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": ach / peak_tf, "traffic": traffic,
                 "peak_source": f"bf16_tflops ({peak_src}, burst)"}

@@ -157,9 +157,9 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
     launch_selfcond_simt(s->Phi, s->Plo, a->E, fp32, R, V, d, L, a->done, S, s->Opart, st);
   }
   mark(s, 4, st);
-  launch_reduce_s(s->Opart, S, R, d, L, a->done, s->rs, a->s, st);
-  launch_finalize(s->rs, s->best, s->cand, s->n_chunks, k, R, L, a->done, a->step, a->seed,
-                  a->sampled, a->conf, a->entropy, a->argmax, st);
+  launch_finalize_with_s(s->rs, s->best, s->cand, s->n_chunks, k, R, L, a->done, a->step,
+                         a->seed, a->sampled, a->conf, a->entropy, a->argmax, s->Opart, S, d, a->s,
+                         st);
   mark(s, 5, st);
   launch_lock(B, L, V, s->cfg.max_steps, a->seed, a->tau, a->sampled, a->conf, a->step, a->canvas,
               a->lock, a->done, st);
@@ -168,7 +168,7 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
     ++s->timed_steps;
     s->timed_stream = st;
   }
-  s->launches += (s->impl == DS_IMPL_TENSOR ? 7 : 8) + (k > 0 ? 1 : 0);
+  s->launches += (s->impl == DS_IMPL_TENSOR ? 6 : 7) + (k > 0 ? 1 : 0);
   return cuda_status(cudaGetLastError());
 }
 

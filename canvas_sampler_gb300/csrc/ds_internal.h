@@ -32,6 +32,12 @@ void launch_finalize(const RowStat* rs, const Best* best, const Cand* cand, int 
                      int R, int L, const uint8_t* done, const int32_t* step, uint64_t seed,
                      int32_t* sampled, float* conf, float* entropy, int32_t* argmax,
                      cudaStream_t st);
+// launch_finalize plus the reduction of s (launch_reduce_s) in the same per-row kernel.
+void launch_finalize_with_s(const RowStat* rs, const Best* best, const Cand* cand, int n_chunks,
+                            int k, int R, int L, const uint8_t* done, const int32_t* step,
+                            uint64_t seed, int32_t* sampled, float* conf, float* entropy,
+                            int32_t* argmax, const float* Opart, int S, int d, float* s,
+                            cudaStream_t st);
 void launch_reduce_s(const float* Opart, int S, int R, int d, int L, const uint8_t* done,
                      const RowStat* rs, float* s, cudaStream_t st);
 void launch_lock(int B, int L, int64_t V, int max_steps, uint64_t seed, const float* tau,
@@ -53,10 +59,17 @@ void launch_standin_simt(const uint16_t* W, const float* s_prev, const uint16_t*
                          const int32_t* canvas, const uint8_t* done, int R, int d, int L,
                          uint16_t* H_out, cudaStream_t st);
 
-// ---- tensor-core GEMMs (ds_tc.cu) ----
+// ---- tensor-core GEMMs (ds_tc.cu host side, ds_tc_logits.cu, ds_tc_selfcond.cu) ----
 // Resolves the driver's tensor-map encoder; false when unavailable.
 bool tc_available();
 int tc_num_sms();
+// 2-D tensor maps (128-byte swizzle) over a row-major [rows, cols] array, box [box_rows, box_cols].
+bool tc_make_map_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                      uint32_t box_rows, uint32_t box_cols);
+bool tc_make_map_f32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows, uint32_t box_cols);
+void tc_prepare_logits();
+void tc_prepare_selfcond();
 // Also writes the softmax statistics of every 128-token segment of every row:
 // seg_stats [R, V / kTcSegment].
 constexpr int kTcSegment = 128;

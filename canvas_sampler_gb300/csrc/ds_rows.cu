@@ -187,35 +187,72 @@ __global__ void __launch_bounds__(kThreads) k_chunk_stats(const float* __restric
   if (threadIdx.x == 0) cs[(size_t)r * n_chunks + c] = ChunkStat{m, l, a, arg};
 }
 
-// One warp per row; fp64 merge of the chunk statistics.
-__global__ void k_row_merge(const ChunkStat* __restrict__ cs, int n_chunks, int R, int L,
-                            const uint8_t* __restrict__ done, RowStat* __restrict__ rs) {
-  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int ln = threadIdx.x & 31;
-  if (r >= R) return;
+// One CTA per row: merge of the chunk statistics (max and lowest argmax, then the rescaled
+// sums in fp64; the rescale factors exp(m_c - m) <= 1 are taken in fp32, relative error ~1e-7,
+// because GB300's fp64 units are slow). Each thread takes every 256th chunk; all its loads
+// are issued before any arithmetic.
+__global__ void __launch_bounds__(kThreads) k_row_merge(const ChunkStat* __restrict__ cs,
+                                                        int n_chunks, int L,
+                                                        const uint8_t* __restrict__ done,
+                                                        RowStat* __restrict__ rs) {
+  constexpr int kPer = 16;  // chunks per thread per batch (one batch up to 4096 chunks)
+  __shared__ float shv[32], shy;
+  __shared__ int32_t shj[32];
+  __shared__ double shd[2][32];
+  const int r = blockIdx.x;
   if (done && done[r / L]) return;
   const ChunkStat* c = cs + (size_t)r * n_chunks;
-  float m = -INFINITY;
-  int32_t arg = INT_MAX;
-  for (int q = ln; q < n_chunks; q += 32)
-    if (better(c[q].m, c[q].arg, m, arg)) {
-      m = c[q].m;
-      arg = c[q].arg;
+  auto load_batch = [&](int base, ChunkStat (&mine)[kPer]) {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int q = base + threadIdx.x + kThreads * k;
+      mine[k] = q < n_chunks ? c[q] : ChunkStat{-INFINITY, 0.f, 0.f, INT_MAX};
     }
-  warp_best(m, arg);
+  };
+  float m = -INFINITY, dummy_y = 0.f;
+  int32_t arg = INT_MAX;
+  ChunkStat mine[kPer];
+  for (int base = 0; base < n_chunks; base += kThreads * kPer) {
+    load_batch(base, mine);
+#pragma unroll
+    for (int k = 0; k < kPer; ++k)
+      if (better(mine[k].m, mine[k].arg, m, arg)) {
+        m = mine[k].m;
+        arg = mine[k].arg;
+      }
+  }
+  block_best(m, arg, dummy_y, shv, shj, &shy);
   double l = 0.0, a = 0.0;
-  for (int q = ln; q < n_chunks; q += 32) {
-    const double dm = (double)c[q].m - (double)m;
-    const double sc = exp(dm);
-    l += (double)c[q].l * sc;
-    a += ((double)c[q].a + (double)c[q].l * dm) * sc;
+  for (int base = 0; base < n_chunks; base += kThreads * kPer) {
+    if (base > 0 || n_chunks > kThreads * kPer) load_batch(base, mine);
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      if (mine[k].arg == INT_MAX) continue;
+      const float dm = mine[k].m - m;
+      const double sc = (double)expf(dm);
+      l += (double)mine[k].l * sc;
+      a += ((double)mine[k].a + (double)mine[k].l * (double)dm) * sc;
+    }
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
     l += __shfl_xor_sync(0xffffffffu, l, o);
     a += __shfl_xor_sync(0xffffffffu, a, o);
   }
-  if (ln == 0) rs[r] = RowStat{m, (float)l, (float)(log(l) - a / l), arg};
+  const int w = threadIdx.x >> 5, ln = threadIdx.x & 31;
+  if (ln == 0) {
+    shd[0][w] = l;
+    shd[1][w] = a;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double tl = 0.0, ta = 0.0;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) {
+      tl += shd[0][i];
+      ta += shd[1][i];
+    }
+    rs[r] = RowStat{m, (float)tl, (float)(log(tl) - ta / tl), arg};
+  }
 }
 
 __device__ __forceinline__ void split_bf16(float p, uint16_t& hi, uint16_t& lo) {
@@ -225,9 +262,19 @@ __device__ __forceinline__ void split_bf16(float p, uint16_t& hi, uint16_t& lo) 
   lo = __bfloat16_as_ushort(q);
 }
 
-// exp(y - m) as bf16 hi + lo (the A operand of the self-conditioning GEMM) and the chunk's
-// best Gumbel-perturbed logit.
-__global__ void __launch_bounds__(kThreads) k_convert(const float* __restrict__ Y,
+// exp(y - m) as bf16 hi + lo (the A operand of the self-conditioning GEMM) and, when `gumbel`
+// is set, the chunk's Gumbel-max winner.
+//
+// Gumbel-max in its exponential-race form: with E_j = -ln u_j and p_j = exp(y_j - m),
+//   argmax_j (y_j - ln(-ln u_j)) = argmin_j E_j / p_j,
+// because ln(E_j / p_j) = m - (y_j + g_j) is decreasing in the perturbed logit. p_j is already
+// at hand for the split, and the logarithm is only needed for a token that can beat the
+// thread's best key so far: -ln u >= 1 - u, so 1 - u > key_best * p_j proves E_j / p_j >
+// key_best without it. A whole group of four is skipped when even the smallest possible
+// E (2^-24 < -ln(1 - 2^-24)) over its largest p_j cannot beat key_best, or when all four logits
+// are more than kGumbelReach below the row maximum. The chunk's winner is written as
+// v = -key (larger is better), comparable across the chunks of a row.
+__global__ void __launch_bounds__(kThreads, 4) k_convert(const float* __restrict__ Y,
                                                       const RowStat* __restrict__ rs, int64_t V,
                                                       int L, const uint8_t* __restrict__ done,
                                                       const int32_t* __restrict__ step,
@@ -246,42 +293,65 @@ __global__ void __launch_bounds__(kThreads) k_convert(const float* __restrict__ 
   uint16_t* ph = Phi + (size_t)r * V;
   uint16_t* pl = Plo + (size_t)r * V;
   const int64_t j0 = (int64_t)c * kChunk, j1 = min(V, j0 + kChunk);
-  float bv = -INFINITY, by = 0.f;
+  const float floor_y = m - kGumbelReach;
+  float kbest = INFINITY, by = 0.f;
   int32_t bj = INT_MAX;
-#pragma unroll 2
+  // loads in two batches of four 16-byte loads: the second batch is in flight while the
+  // first is processed (four CTAs per SM overlap the rest)
+  constexpr int kBatch = kGroups / 2;
+  float4 ld[kBatch];
+  auto load_batch = [&](int g0) {
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int64_t j = j0 + 4 * (threadIdx.x + kThreads * (g0 + u));
+      ld[u] = j < j1 ? __ldcs(reinterpret_cast<const float4*>(y + j))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  load_batch(0);
+#pragma unroll
   for (int g = 0; g < kGroups; ++g) {
     const int64_t j = j0 + 4 * (threadIdx.x + kThreads * g);
+    const float4 cur = ld[g % kBatch];
+    if (g + 1 == kBatch) load_batch(kBatch);
     if (j >= j1) continue;
-    const float4 t = *reinterpret_cast<const float4*>(y + j);
-    const float yy[4] = {t.x, t.y, t.z, t.w};
+    const float yy[4] = {cur.x, cur.y, cur.z, cur.w};
+    float p[4];
     uint16_t hi[4], lo[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) split_bf16(expf(yy[e] - m), hi[e], lo[e]);
-    *reinterpret_cast<uint2*>(ph + j) =
-        make_uint2((uint32_t)hi[0] | ((uint32_t)hi[1] << 16), (uint32_t)hi[2] | ((uint32_t)hi[3] << 16));
-    *reinterpret_cast<uint2*>(pl + j) =
-        make_uint2((uint32_t)lo[0] | ((uint32_t)lo[1] << 16), (uint32_t)lo[2] | ((uint32_t)lo[3] << 16));
-    if (gumbel) {
-      const float floor_y = m - kGumbelReach;
-      if (fmaxf(fmaxf(yy[0], yy[1]), fmaxf(yy[2], yy[3])) >= floor_y) {
-        const u32x4 w = gumbel_block((uint32_t)(j >> 2), (uint32_t)i, (uint32_t)b, st, seed);
+    for (int e = 0; e < 4; ++e) {
+      p[e] = expf(yy[e] - m);
+      split_bf16(p[e], hi[e], lo[e]);
+    }
+    *reinterpret_cast<uint2*>(ph + j) = make_uint2((uint32_t)hi[0] | ((uint32_t)hi[1] << 16),
+                                                   (uint32_t)hi[2] | ((uint32_t)hi[3] << 16));
+    *reinterpret_cast<uint2*>(pl + j) = make_uint2((uint32_t)lo[0] | ((uint32_t)lo[1] << 16),
+                                                   (uint32_t)lo[2] | ((uint32_t)lo[3] << 16));
+    if (!gumbel) continue;
+    const float pmax = fmaxf(fmaxf(p[0], p[1]), fmaxf(p[2], p[3]));
+    const float ymax = fmaxf(fmaxf(yy[0], yy[1]), fmaxf(yy[2], yy[3]));
+    if (ymax < floor_y || !(pmax > 0.f) || 5.9604645e-8f >= kbest * pmax) continue;
+    const u32x4 w = gumbel_block((uint32_t)(j >> 2), (uint32_t)i, (uint32_t)b, st, seed);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (yy[e] >= floor_y) {
-            const float v = yy[e] + gumbel_from_word(word_of(w, e));
-            if (better(v, (int32_t)(j + e), bv, bj)) {
-              bv = v;
-              bj = (int32_t)(j + e);
-              by = yy[e];
-            }
-          }
-        }
+    for (int e = 0; e < 4; ++e) {
+      if (!(p[e] > 0.f)) continue;
+      const uint32_t q = word_of(w, e) >> 9;
+      // 1 - u for u = (2q + 1) / 2^24, exact in fp32
+      const float one_minus_u = (float)(0xFFFFFFu - 2u * q) * 5.9604644775390625e-8f;
+      if (one_minus_u * (1.0f - 9.5367431640625e-7f) > kbest * p[e]) continue;
+      const float key = -logf(word_to_uniform(word_of(w, e))) / p[e];
+      const int32_t jj = (int32_t)(j + e);
+      if (key < kbest || (key == kbest && jj < bj)) {
+        kbest = key;
+        bj = jj;
+        by = yy[e];
       }
     }
   }
   if (gumbel) {
-    block_best(bv, bj, by, shv, shj, &shy);
-    if (threadIdx.x == 0) best[(size_t)r * n_chunks + c] = Best{bv, bj, by, 0};
+    float v = -kbest;
+    block_best(v, bj, by, shv, shj, &shy);
+    if (threadIdx.x == 0) best[(size_t)r * n_chunks + c] = Best{v, bj, by, 0};
   }
 }
 
@@ -317,11 +387,14 @@ __global__ void __launch_bounds__(kThreads) k_topk_chunk(const float* __restrict
 }
 
 // Per row: the sampled token, its confidence, the entropy and the argmax.
+// With Opart set, it also writes s for the row: the sum of the vocabulary-split partials in
+// split order, divided by the softmax normaliser.
 __global__ void __launch_bounds__(kThreads) k_finalize(
     const RowStat* __restrict__ rs, const Best* __restrict__ best, const Cand* __restrict__ cand,
     int n_chunks, int k, int L, const uint8_t* __restrict__ done, const int32_t* __restrict__ step,
     uint64_t seed, int32_t* __restrict__ sampled, float* __restrict__ conf,
-    float* __restrict__ entropy, int32_t* __restrict__ argmax) {
+    float* __restrict__ entropy, int32_t* __restrict__ argmax, const float* __restrict__ Opart,
+    int S, int R, int d, float* __restrict__ s_out) {
   __shared__ float shv[32], shy, shf[32];
   __shared__ int32_t shj[32];
   __shared__ int hist[256];
@@ -332,6 +405,22 @@ __global__ void __launch_bounds__(kThreads) k_finalize(
   const int b = r / L, i = r % L;
   if (done && done[b]) return;
   const RowStat st = rs[r];
+  if (Opart) {
+    const int64_t plane = (int64_t)R * d;
+    const float4* src = reinterpret_cast<const float4*>(Opart + (size_t)r * d);
+    float4* dst = reinterpret_cast<float4*>(s_out + (size_t)r * d);
+    for (int q = threadIdx.x; q < d / 4; q += kThreads) {
+      float4 acc = src[q];
+      for (int sp = 1; sp < S; ++sp) {
+        const float4 t = src[sp * plane / 4 + q];
+        acc.x += t.x;
+        acc.y += t.y;
+        acc.z += t.z;
+        acc.w += t.w;
+      }
+      dst[q] = make_float4(acc.x / st.l, acc.y / st.l, acc.z / st.l, acc.w / st.l);
+    }
+  }
   float bv = -INFINITY, by = 0.f;
   int32_t bj = INT_MAX;
   float cval;
@@ -523,7 +612,7 @@ void launch_chunk_stats(const float* Y, int R, int64_t V, int L, const uint8_t* 
 
 void launch_row_merge(const ChunkStat* cs, int n_chunks, int R, int L, const uint8_t* done,
                       RowStat* rs, cudaStream_t st) {
-  k_row_merge<<<(R + 7) / 8, 256, 0, st>>>(cs, n_chunks, R, L, done, rs);
+  k_row_merge<<<R, kThreads, 0, st>>>(cs, n_chunks, L, done, rs);
 }
 
 void launch_convert(const float* Y, const RowStat* rs, int R, int64_t V, int L,
@@ -532,6 +621,7 @@ void launch_convert(const float* Y, const RowStat* rs, int R, int64_t V, int L,
   const int nc = n_chunks_of(V);
   k_convert<<<dim3(nc, R), kThreads, 0, st>>>(Y, rs, V, L, done, step, seed, gumbel ? 1 : 0, Phi,
                                               Plo, best, nc);
+
 }
 
 void launch_topk_chunk(const float* Y, int R, int64_t V, int L, const uint8_t* done, int k,
@@ -545,7 +635,16 @@ void launch_finalize(const RowStat* rs, const Best* best, const Cand* cand, int 
                      int32_t* sampled, float* conf, float* entropy, int32_t* argmax,
                      cudaStream_t st) {
   k_finalize<<<R, kThreads, 0, st>>>(rs, best, cand, n_chunks, k, L, done, step, seed, sampled,
-                                     conf, entropy, argmax);
+                                     conf, entropy, argmax, nullptr, 0, R, 0, nullptr);
+}
+
+void launch_finalize_with_s(const RowStat* rs, const Best* best, const Cand* cand, int n_chunks,
+                            int k, int R, int L, const uint8_t* done, const int32_t* step,
+                            uint64_t seed, int32_t* sampled, float* conf, float* entropy,
+                            int32_t* argmax, const float* Opart, int S, int d, float* s,
+                            cudaStream_t st) {
+  k_finalize<<<R, kThreads, 0, st>>>(rs, best, cand, n_chunks, k, L, done, step, seed, sampled,
+                                     conf, entropy, argmax, Opart, S, R, d, s);
 }
 
 void launch_reduce_s(const float* Opart, int S, int R, int d, int L, const uint8_t* done,

@@ -1,0 +1,237 @@
+// Tensor-core logits of the sampler step on sm_103a, with the softmax statistics of every
+// 128-token segment of each row fused into the epilogue:
+//   Y[r, j] = (sum_k H[r, k] E[j, k]) / T_b        bf16 x bf16 -> fp32 (H [B*L, d], E [V, d])
+//   for each row and segment: max, lowest argmax, sum exp(y - max), sum exp(y - max)(y - max)
+// Definitions: DiffusionGemma Technical Report, section 6 "Sampling" (softmax over the full
+// vocabulary in full precision). Pipeline structure: ds_tc_common.cuh.
+#include <algorithm>
+
+#include "ds_tc_common.cuh"
+
+namespace ds {
+namespace {
+
+using namespace tcpipe;
+
+// ------------------------------------------------------------------------------------------
+// logits (+ softmax statistics of each 128-token segment of a row)
+// ------------------------------------------------------------------------------------------
+constexpr int LG_BM = 128, LG_BN = 256, LG_BK = 64, LG_STAGES = 4, LG_CHUNK_KB = 2;
+constexpr int LG_COLS = LG_BN / 2;
+constexpr uint32_t LG_A_BYTES = LG_BM * LG_BK * 2;
+constexpr uint32_t LG_B_BYTES = LG_BN * LG_BK * 2;
+constexpr uint32_t LG_STAGE_BYTES = LG_A_BYTES + LG_B_BYTES;
+// y leaves through one 32 x 32 fp32 staging box per epilogue warp (128-byte swizzle, written
+// by the warp, stored by one TMA bulk store), so the global stores are full lines.
+constexpr uint32_t LG_STG_BYTES = 32 * 32 * 4;
+constexpr size_t LG_SMEM =
+    (size_t)LG_STAGES * LG_STAGE_BYTES + (size_t)kEpiWarps * LG_STG_BYTES + 1024;
+
+__global__ void __launch_bounds__(kThreadsTC, 1)
+    k_logits_tc(const __grid_constant__ CUtensorMap mapH, const __grid_constant__ CUtensorMap mapE,
+                const __grid_constant__ CUtensorMap mapY, int R, int64_t V, int d, int L, const float* __restrict__ T,
+                const uint8_t* __restrict__ done, float* __restrict__ Y,
+                ChunkStat* __restrict__ seg_stats, uint32_t* err) {
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ Ctl ctl;
+  uint8_t* smem = align1024(dyn_smem);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_rt = R / LG_BM;
+  const int n_ct = (int)(V / LG_BN);
+  const int n_tiles = n_rt * n_ct;
+  const int nk = d / LG_BK;
+  const int n_ch = (nk + LG_CHUNK_KB - 1) / LG_CHUNK_KB;
+  if (threadIdx.x == 0) ctl_init(ctl, LG_STAGES);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mapH);
+    tma_prefetch_desc(&mapE);
+    tma_prefetch_desc(&mapY);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  volatile int* abort_flag = &ctl.abort;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_E = policy_evict_first(), pol_H = policy_evict_last();
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        const int rt = tile % n_rt, ct = tile / n_rt;
+        if (done && done[(rt * LG_BM) / L]) continue;
+        for (int kc = 0; kc < nk; ++kc) {
+          if (!mbar_wait(smem_u32(&ctl.empty[stage]), phase ^ 1, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = sbase + stage * LG_STAGE_BYTES, sb = sa + LG_A_BYTES;
+          const uint32_t fb = smem_u32(&ctl.full[stage]);
+          mbar_arrive_expect_tx(fb, LG_STAGE_BYTES);
+          tma_load_2d(sa, &mapH, fb, kc * LG_BK, rt * LG_BM, pol_H);
+          tma_load_2d(sb, &mapE, fb, kc * LG_BK, ct * LG_BN, pol_E);
+          ++issued;
+          if (++stage == LG_STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) producer_drain(ctl, issued, LG_STAGES);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(LG_BM, LG_BN, false, false);
+      int stage = 0, cc = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        const int rt = tile % n_rt;
+        if (done && done[(rt * LG_BM) / L]) continue;
+        for (int ch = 0; ch < n_ch && ok; ++ch, ++cc) {
+          const int buf = cc & 1;
+          const uint32_t par = (uint32_t)((cc >> 1) & 1);
+          if (!mbar_wait(smem_u32(&ctl.tempty[buf]), par ^ 1, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t dt = tmem + (uint32_t)(buf * LG_BN);
+          const int kc0 = ch * LG_CHUNK_KB, kc1 = min(nk, kc0 + LG_CHUNK_KB);
+          for (int kc = kc0; kc < kc1; ++kc) {
+            if (!mbar_wait(smem_u32(&ctl.full[stage]), phase, abort_flag, err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            *(volatile int*)&ctl.consumed = ctl.consumed + 1;
+            const uint32_t sa = sbase + stage * LG_STAGE_BYTES, sb = sa + LG_A_BYTES;
+#pragma unroll
+            for (int k = 0; k < LG_BK / 16; ++k)
+              umma_bf16(dt, sdesc_sw128(sa + 32 * k, 16, 1024),
+                        sdesc_sw128(sb + 32 * k, 16, 1024), idesc, (kc != kc0 || k) ? 1u : 0u);
+            umma_commit(smem_u32(&ctl.empty[stage]));
+            if (++stage == LG_STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (!ok) break;
+          umma_commit(smem_u32(&ctl.tfull[buf]));
+        }
+      }
+      umma_commit(smem_u32(&ctl.mma_done));
+      mbar_wait_quiet(smem_u32(&ctl.mma_done), 0);
+    }
+  } else {
+    const int q = warp & 3;              // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;    // column half of the tile
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    int cc = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+      const int rt = tile % n_rt, ct = tile / n_rt;
+      const int b = (rt * LG_BM) / L;
+      if (done && done[b]) continue;
+      float acc[LG_COLS];
+#pragma unroll
+      for (int i = 0; i < LG_COLS; ++i) acc[i] = 0.f;
+      for (int ch = 0; ch < n_ch; ++ch, ++cc) {
+        const int buf = cc & 1;
+        const uint32_t par = (uint32_t)((cc >> 1) & 1);
+        if (!mbar_wait(smem_u32(&ctl.tfull[buf]), par, abort_flag, err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_accumulate<LG_COLS>(tmem + (uint32_t)(buf * LG_BN + half * LG_COLS) + lane_base, acc);
+        tc_fence_before();
+        mbar_arrive(smem_u32(&ctl.tempty[buf]));
+      }
+      if (!ok) break;
+      // y = z / T (as z * (1/T)); the segment's max, argmax (lowest token), sum of exp(y - m)
+      // and sum of exp(y - m) (y - m). x * invT is monotone in x for invT > 0, so the max of
+      // the scaled values is the scaled max, at the same lowest index.
+      const float invT = 1.0f / T[b];
+      const int row0 = rt * LG_BM + q * 32;
+      const int64_t j0 = (int64_t)ct * LG_BN + half * LG_COLS;
+      float zmax = -INFINITY;
+      int arg = 0;
+#pragma unroll
+      for (int i = 0; i < LG_COLS; ++i) {
+        if (acc[i] > zmax) {
+          zmax = acc[i];
+          arg = i;
+        }
+      }
+      const float m = zmax * invT;
+      float l = 0.f, a = 0.f;
+      const uint32_t stg = sbase + LG_STAGES * LG_STAGE_BYTES + (uint32_t)(warp - 2) * LG_STG_BYTES;
+#pragma unroll
+      for (int bx = 0; bx < LG_COLS / 32; ++bx) {
+        if (lane == 0) bulk_wait_read_all();  // the previous store has read the staging box
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          float y4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            y4[e] = acc[bx * 32 + c * 4 + e] * invT;
+            const float t = y4[e] - m;
+            const float x = __expf(t);
+            l += x;
+            a = fmaf(x, t, a);
+          }
+          // row `lane` of the box, 16-byte chunk c at its 128-byte-swizzled position
+          st_shared_f4(stg + lane * 128 + ((c ^ (lane & 7)) << 4), y4[0], y4[1], y4[2], y4[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&mapY, stg, (int32_t)(j0 + bx * 32), row0);
+          bulk_commit();
+        }
+      }
+      seg_stats[(size_t)(row0 + lane) * (V / LG_COLS) + (j0 / LG_COLS)] =
+          ChunkStat{m, l, a, (int32_t)(j0 + arg)};
+    }
+    if (lane == 0) bulk_wait_all();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+void tc_prepare_logits() {
+  cudaFuncSetAttribute(k_logits_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LG_SMEM);
+}
+
+cudaError_t launch_logits_tc(const uint16_t* H, const uint16_t* E, int R, int64_t V, int d, int L,
+                             const float* T, const uint8_t* done, float* Y, ChunkStat* seg_stats,
+                             uint32_t* err, cudaStream_t st) {
+  if (!tc_available()) return cudaErrorNotSupported;
+  CUtensorMap mH, mE, mY;
+  if (!tc_make_map_bf16(&mH, H, (uint64_t)R, (uint64_t)d, LG_BM, LG_BK) ||
+      !tc_make_map_bf16(&mE, E, (uint64_t)V, (uint64_t)d, LG_BN, LG_BK) ||
+      !tc_make_map_f32(&mY, Y, (uint64_t)R, (uint64_t)V, 32, 32))
+    return cudaErrorInvalidValue;
+  const int n_tiles = (R / LG_BM) * (int)(V / LG_BN);
+  const int grid = std::max(1, std::min(n_tiles, tc_num_sms()));
+  k_logits_tc<<<grid, kThreadsTC, LG_SMEM, st>>>(mH, mE, mY, R, V, d, L, T, done, Y, seg_stats,
+                                                  err);
+  return cudaGetLastError();
+}
+
+}  // namespace ds
