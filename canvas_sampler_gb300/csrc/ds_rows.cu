@@ -255,12 +255,22 @@ __global__ void __launch_bounds__(kThreads) k_row_merge(const ChunkStat* __restr
   }
 }
 
-__device__ __forceinline__ void split_bf16(float p, uint16_t& hi, uint16_t& lo) {
-  const __nv_bfloat16 h = __float2bfloat16_rn(p);
-  const __nv_bfloat16 q = __float2bfloat16_rn(p - __bfloat162float(h));
-  hi = __bfloat16_as_ushort(h);
-  lo = __bfloat16_as_ushort(q);
+// 2^x on the special-function unit (ex2.approx.ftz: results below 2^-126 flush to zero).
+__device__ __forceinline__ float exp2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
 }
+
+// (a, b) -> bf16x2 hi = RN(a, b) and lo = RN(a - hi_a, b - hi_b), packed (a in the low half).
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const __nv_bfloat162 l =
+      __floats2bfloat162_rn(a - __low2float(h), b - __high2float(h));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 
 // exp(y - m) as bf16 hi + lo (the A operand of the self-conditioning GEMM) and, when `gumbel`
 // is set, the chunk's Gumbel-max winner.
@@ -316,17 +326,17 @@ __global__ void __launch_bounds__(kThreads, 4) k_convert(const float* __restrict
     if (g + 1 == kBatch) load_batch(kBatch);
     if (j >= j1) continue;
     const float yy[4] = {cur.x, cur.y, cur.z, cur.w};
+    // p = exp(y - m) = 2^((y - m) log2 e): the argument carries a relative rounding error of
+    // ~2^-23 and ex2.approx ~2^-22, so p is within ~3e-6 relative for y - m > -30 (smaller
+    // terms do not matter at that precision); p of the row maximum is exactly 1.
     float p[4];
-    uint16_t hi[4], lo[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      p[e] = expf(yy[e] - m);
-      split_bf16(p[e], hi[e], lo[e]);
-    }
-    *reinterpret_cast<uint2*>(ph + j) = make_uint2((uint32_t)hi[0] | ((uint32_t)hi[1] << 16),
-                                                   (uint32_t)hi[2] | ((uint32_t)hi[3] << 16));
-    *reinterpret_cast<uint2*>(pl + j) = make_uint2((uint32_t)lo[0] | ((uint32_t)lo[1] << 16),
-                                                   (uint32_t)lo[2] | ((uint32_t)lo[3] << 16));
+    for (int e = 0; e < 4; ++e) p[e] = exp2_approx((yy[e] - m) * 1.4426950408889634f);
+    uint2 hi, lo;
+    split_bf16x2(p[0], p[1], hi.x, lo.x);
+    split_bf16x2(p[2], p[3], hi.y, lo.y);
+    *reinterpret_cast<uint2*>(ph + j) = hi;
+    *reinterpret_cast<uint2*>(pl + j) = lo;
     if (!gumbel) continue;
     const float pmax = fmaxf(fmaxf(p[0], p[1]), fmaxf(p[2], p[3]));
     const float ymax = fmaxf(fmaxf(yy[0], yy[1]), fmaxf(yy[2], yy[3]));
@@ -337,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_convert(const float* __restrict
       if (!(p[e] > 0.f)) continue;
       const uint32_t q = word_of(w, e) >> 9;
       // 1 - u for u = (2q + 1) / 2^24, exact in fp32
-      const float one_minus_u = (float)(0xFFFFFFu - 2u * q) * 5.9604644775390625e-8f;
+      const float one_minus_u = __uint2float_rn(0xFFFFFFu - 2u * q) * 5.9604644775390625e-8f;
       if (one_minus_u * (1.0f - 9.5367431640625e-7f) > kbest * p[e]) continue;
       const float key = -logf(word_to_uniform(word_of(w, e))) / p[e];
       const int32_t jj = (int32_t)(j + e);
