@@ -41,8 +41,8 @@ PROFILE_FILE = os.path.join(ROOT, "profiles", "selfcond_tc_step_v262144_d2816.md
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=W.BENCH_WORKLOAD, choices=sorted(W.WORKLOADS))
     ap.add_argument("--kernel-impl", default="auto", choices=["auto", "tensor", "simt"])
@@ -62,6 +62,21 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank samples its own canvas: the sampler seed is offset by the rank."""
+    return int(seed) + int(rank)
+
+
+def reduce_max(value: float, dist, device) -> float:
+    """The slowest rank's value (the job's time); a no-op for a single process."""
+    import torch
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def load_peaks():
@@ -233,7 +248,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     w = workload_of(args)
     inp = W.make_inputs(w)
-    seed = inp["seed"] + rank  # each rank samples its own canvas
+    seed = rank_seed(inp["seed"], rank)
 
     def upload(a):
         if w.dtype == "fp32":
@@ -299,10 +314,7 @@ def run_ours(args):
     sampler.set_phase_timing(False)
     launches = sampler.launch_count - launches0
     clk = clocks.stop()
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(ms, dist if world > 1 else None, dev)
     status = sampler.device_status()
 
     # end to end through the public API: pinned host buffers in, results back, every step
@@ -324,10 +336,7 @@ def run_ours(args):
         hs.lock.zero_(); hs.done.zero_(); hs.step.zero_()
         sampler.step_host(Hh, E, Th, tauh, hs, seed, hout, stream=stream)
     e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = reduce_max(e2e_s, dist if world > 1 else None, dev)
 
     step_s = ms / 1e3 / args.steps
     value = world * args.steps / (ms / 1e3)
