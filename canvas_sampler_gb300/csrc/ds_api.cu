@@ -48,6 +48,7 @@ struct ds_sampler {
   Cand* cand = nullptr;
   float* Opart = nullptr;
   size_t opart_floats = 0;
+  uint16_t* U = nullptr;  // stand-in operand [B*L, 2d] (tensor-core path)
   uint32_t* err = nullptr;
   int32_t* iter = nullptr;
   int last_batch = 0;
@@ -175,6 +176,15 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
 ds_status enqueue_standin(ds_sampler* s, const void* W, const float* s_prev, const void* E,
                           const int32_t* canvas, const uint8_t* done, void* H_out, int batch,
                           cudaStream_t st) {
+  const int d = s->cfg.d_model, L = s->cfg.canvas_len, R = batch * L;
+  if (s->impl == DS_IMPL_TENSOR && s->U && d % 256 == 0) {
+    launch_standin_gather(s_prev, static_cast<const uint16_t*>(E), canvas, done, R, d, L, s->U,
+                          st);
+    cudaError_t e = launch_standin_tc(s->U, static_cast<const uint16_t*>(W), R, d, L, done,
+                                      static_cast<uint16_t*>(H_out), s->err, st);
+    s->launches += 2;
+    return cuda_status(e == cudaSuccess ? cudaGetLastError() : e);
+  }
   launch_standin_simt(static_cast<const uint16_t*>(W), s_prev, static_cast<const uint16_t*>(E),
                       canvas, done, batch * s->cfg.canvas_len, s->cfg.d_model, s->cfg.canvas_len,
                       static_cast<uint16_t*>(H_out), st);
@@ -296,6 +306,7 @@ ds_status ds_sampler_create(const ds_sampler_config* cfg, ds_sampler** out) {
   s->best = carve<Best>(s, Rm * n_chunks, &e);
   if (c.top_k > 0) s->cand = carve<Cand>(s, Rm * n_chunks * c.top_k, &e);
   s->Opart = carve<float>(s, opart, &e);
+  if (s->impl == DS_IMPL_TENSOR && c.d_model % 256 == 0) s->U = carve<uint16_t>(s, Rm * 2 * d, &e);
   s->opart_floats = opart;
   s->err = carve<uint32_t>(s, 4, &e);
   s->iter = carve<int32_t>(s, 4, &e);

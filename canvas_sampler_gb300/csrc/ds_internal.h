@@ -76,6 +76,14 @@ constexpr int kTcSegment = 128;
 cudaError_t launch_logits_tc(const uint16_t* H, const uint16_t* E, int R, int64_t V, int d, int L,
                              const float* T, const uint8_t* done, float* Y, ChunkStat* seg_stats,
                              uint32_t* err, cudaStream_t st);
+// H = bf16(tanh(U . W^T)) for U [R, 2d] bf16, W [d, 2d] bf16 (d % 256 == 0).
+cudaError_t launch_standin_tc(const uint16_t* U, const uint16_t* W, int R, int d, int L,
+                              const uint8_t* done, uint16_t* H_out, uint32_t* err,
+                              cudaStream_t st);
+// U [R, 2d] = [bf16(s_prev) | E[canvas]] for the stand-in (rows of done sequences skipped).
+void launch_standin_gather(const float* s_prev, const uint16_t* E, const int32_t* canvas,
+                           const uint8_t* done, int R, int d, int L, uint16_t* U,
+                           cudaStream_t st);
 cudaError_t launch_selfcond_tc(const uint16_t* Phi, const uint16_t* Plo, const uint16_t* E, int R,
                                int64_t V, int d, int L, const uint8_t* done, int S, float* Opart,
                                uint32_t* err, cudaStream_t st);

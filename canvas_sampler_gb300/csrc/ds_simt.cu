@@ -7,6 +7,8 @@
 // vocabulary and the self-conditioning embedding matmul).
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "ds_internal.h"
 
 namespace ds {
@@ -163,7 +165,40 @@ __global__ void __launch_bounds__(THREADS) k_standin_simt(const uint16_t* __rest
       });
 }
 
+// U[r, k] = k < d ? bf16(s_prev[r, k]) : E[canvas[r], k - d], eight bf16 per thread.
+__global__ void k_standin_gather(const float* __restrict__ s_prev, const uint16_t* __restrict__ E,
+                                 const int32_t* __restrict__ canvas,
+                                 const uint8_t* __restrict__ done, int R, int d, int L,
+                                 uint16_t* __restrict__ U) {
+  const int per_row = (2 * d) / 8;
+  for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < (int64_t)R * per_row;
+       q += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(q / per_row), k = (int)(q % per_row) * 8;
+    if (done && done[r / L]) continue;
+    uint4 out;
+    if (k < d) {
+      const float4 a = *reinterpret_cast<const float4*>(s_prev + (size_t)r * d + k);
+      const float4 b = *reinterpret_cast<const float4*>(s_prev + (size_t)r * d + k + 4);
+      const __nv_bfloat162 h0 = __floats2bfloat162_rn(a.x, a.y), h1 = __floats2bfloat162_rn(a.z, a.w);
+      const __nv_bfloat162 h2 = __floats2bfloat162_rn(b.x, b.y), h3 = __floats2bfloat162_rn(b.z, b.w);
+      out = make_uint4(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1),
+                       *reinterpret_cast<const uint32_t*>(&h2), *reinterpret_cast<const uint32_t*>(&h3));
+    } else {
+      out = *reinterpret_cast<const uint4*>(E + (size_t)canvas[r] * d + (k - d));
+    }
+    *reinterpret_cast<uint4*>(U + (size_t)r * 2 * d + k) = out;
+  }
+}
+
 }  // namespace
+
+void launch_standin_gather(const float* s_prev, const uint16_t* E, const int32_t* canvas,
+                           const uint8_t* done, int R, int d, int L, uint16_t* U,
+                           cudaStream_t st) {
+  const int64_t n = (int64_t)R * (2 * d) / 8;
+  const int blocks = (int)std::min<int64_t>((n + 255) / 256, 4096);
+  k_standin_gather<<<blocks, 256, 0, st>>>(s_prev, E, canvas, done, R, d, L, U);
+}
 
 void launch_logits_simt(const void* H, const void* E, bool fp32_inputs, int R, int64_t V, int d,
                         int L, const float* T, const uint8_t* done, float* Y, cudaStream_t st) {

@@ -27,11 +27,14 @@ constexpr uint32_t LG_STG_BYTES = 32 * 32 * 4;
 constexpr size_t LG_SMEM =
     (size_t)LG_STAGES * LG_STAGE_BYTES + (size_t)kEpiWarps * LG_STG_BYTES + 1024;
 
+// STANDIN: the same GEMM with A = U [R, 2d] (bf16(s_prev) | E[canvas]), B = W [d, 2d] and the
+// epilogue H = bf16(tanh(acc)) instead of y and the statistics (V plays N = d, d plays K = 2d).
+template <bool STANDIN>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     k_logits_tc(const __grid_constant__ CUtensorMap mapH, const __grid_constant__ CUtensorMap mapE,
                 const __grid_constant__ CUtensorMap mapY, int R, int64_t V, int d, int L, const float* __restrict__ T,
                 const uint8_t* __restrict__ done, float* __restrict__ Y,
-                ChunkStat* __restrict__ seg_stats, uint32_t* err) {
+                ChunkStat* __restrict__ seg_stats, uint16_t* __restrict__ Hout, uint32_t* err) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Ctl ctl;
   uint8_t* smem = align1024(dyn_smem);
@@ -46,7 +49,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&mapH);
     tma_prefetch_desc(&mapE);
-    tma_prefetch_desc(&mapY);
+    if (!STANDIN) tma_prefetch_desc(&mapY);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&ctl.tmem_base), 512);
@@ -156,6 +159,22 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         mbar_arrive(smem_u32(&ctl.tempty[buf]));
       }
       if (!ok) break;
+      if constexpr (STANDIN) {
+        const int64_t n0 = (int64_t)ct * LG_BN + half * LG_COLS;
+        uint16_t* hrow = Hout + (size_t)(rt * LG_BM + q * 32 + lane) * V + n0;
+#pragma unroll
+        for (int v = 0; v < LG_COLS / 8; ++v) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 h2 =
+                __floats2bfloat162_rn(tanhf(acc[8 * v + 2 * e]), tanhf(acc[8 * v + 2 * e + 1]));
+            w4[e] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          *reinterpret_cast<uint4*>(hrow + 8 * v) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+        continue;
+      }
       // y = z / T (as z * (1/T)); the segment's max, argmax (lowest token), sum of exp(y - m)
       // and sum of exp(y - m) (y - m). x * invT is monotone in x for invT > 0, so the max of
       // the scaled values is the scaled max, at the same lowest index.
@@ -202,7 +221,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       seg_stats[(size_t)(row0 + lane) * (V / LG_COLS) + (j0 / LG_COLS)] =
           ChunkStat{m, l, a, (int32_t)(j0 + arg)};
     }
-    if (lane == 0) bulk_wait_all();
+    if (!STANDIN && lane == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -215,7 +234,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 }  // namespace
 
 void tc_prepare_logits() {
-  cudaFuncSetAttribute(k_logits_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LG_SMEM);
+  cudaFuncSetAttribute(k_logits_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)LG_SMEM);
+  cudaFuncSetAttribute(k_logits_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)LG_SMEM);
 }
 
 cudaError_t launch_logits_tc(const uint16_t* H, const uint16_t* E, int R, int64_t V, int d, int L,
@@ -229,8 +251,25 @@ cudaError_t launch_logits_tc(const uint16_t* H, const uint16_t* E, int R, int64_
     return cudaErrorInvalidValue;
   const int n_tiles = (R / LG_BM) * (int)(V / LG_BN);
   const int grid = std::max(1, std::min(n_tiles, tc_num_sms()));
-  k_logits_tc<<<grid, kThreadsTC, LG_SMEM, st>>>(mH, mE, mY, R, V, d, L, T, done, Y, seg_stats,
-                                                  err);
+  k_logits_tc<false><<<grid, kThreadsTC, LG_SMEM, st>>>(mH, mE, mY, R, V, d, L, T, done, Y,
+                                                         seg_stats, nullptr, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_standin_tc(const uint16_t* U, const uint16_t* W, int R, int d, int L,
+                              const uint8_t* done, uint16_t* H_out, uint32_t* err,
+                              cudaStream_t st) {
+  if (!tc_available()) return cudaErrorNotSupported;
+  if (d % LG_BN) return cudaErrorInvalidValue;
+  CUtensorMap mU, mW;
+  if (!tc_make_map_bf16(&mU, U, (uint64_t)R, (uint64_t)(2 * d), LG_BM, LG_BK) ||
+      !tc_make_map_bf16(&mW, W, (uint64_t)d, (uint64_t)(2 * d), LG_BN, LG_BK))
+    return cudaErrorInvalidValue;
+  const int n_tiles = (R / LG_BM) * (d / LG_BN);
+  const int grid = std::max(1, std::min(n_tiles, tc_num_sms()));
+  k_logits_tc<true><<<grid, kThreadsTC, LG_SMEM, st>>>(mU, mW, mU, R, (int64_t)d, 2 * d, L,
+                                                        nullptr, done, nullptr, nullptr, H_out,
+                                                        err);
   return cudaGetLastError();
 }
 
