@@ -68,6 +68,7 @@ SIGNATURES = {
     "ds_sampler_set_phase_timing": (c_int32, [c_void_p, c_int32]),
     "ds_sampler_phase_times": (c_int32, [c_void_p, POINTER(ctypes.c_float), c_int32, POINTER(c_int32)]),
     "ds_sampler_launch_count": (c_int32, [c_void_p, POINTER(c_int64)]),
+    "ds_sampler_selftest_wait": (c_int32, [c_void_p, c_int64, c_void_p]),
     "ds_sampler_step_noalloc": (c_int32, [POINTER(ds_sampler_config), POINTER(ds_step_args), c_void_p]),
 }
 

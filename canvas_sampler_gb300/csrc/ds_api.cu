@@ -569,6 +569,13 @@ ds_status ds_sampler_launch_count(const ds_sampler* s, int64_t* count) {
   return DS_OK;
 }
 
+ds_status ds_sampler_selftest_wait(ds_sampler* s, int64_t limit_ns, void* stream) {
+  if (!s || limit_ns < 1000 || limit_ns > 1000000000) return DS_ERR_INVALID_ARG;
+  launch_wait_selftest((uint64_t)limit_ns, s->err, static_cast<cudaStream_t>(stream));
+  s->launches += 1;
+  return cuda_status(cudaGetLastError());
+}
+
 ds_status ds_sampler_debug_buffer(ds_sampler* s, int32_t which, const void** ptr, size_t* bytes) {
   if (!s || !ptr || !bytes) return DS_ERR_INVALID_ARG;
   const size_t R = (size_t)std::max(1, s->last_batch) * s->cfg.canvas_len;

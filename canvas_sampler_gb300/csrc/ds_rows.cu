@@ -612,7 +612,27 @@ __global__ void k_loop_end(const uint8_t* __restrict__ done, int B, int32_t* ite
   }
 }
 
+// A wait that nothing will satisfy: one mbarrier expecting one arrival that never comes.
+__global__ void k_wait_selftest(uint64_t limit_ns, uint32_t* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_mbar_init();
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(b, 0)) {
+    if (globaltimer_ns() - t0 > limit_ns) {
+      atomicOr(err, kErrTimeout);
+      return;
+    }
+  }
+}
+
 }  // namespace
+
+void launch_wait_selftest(uint64_t limit_ns, uint32_t* err, cudaStream_t st) {
+  k_wait_selftest<<<1, 32, 0, st>>>(limit_ns, err);
+}
 
 void launch_chunk_stats(const float* Y, int R, int64_t V, int L, const uint8_t* done,
                         ChunkStat* cs, cudaStream_t st) {

@@ -232,6 +232,13 @@ ds_status ds_sampler_launch_count(const ds_sampler* sampler, int64_t* count);
 ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg, const ds_step_args* args,
                                   void* stream);
 
+/* Self-test of the kernels' bounded waits: enqueues one small kernel that waits on an
+ * mbarrier no thread will ever complete, gives up after limit_ns nanoseconds (1 us .. 1 s),
+ * records DS_ERR_TIMEOUT in the device error word and returns normally. The context stays
+ * usable; ds_sampler_device_status then reports (and clears) the time-out. This is how the
+ * time-out path of the pipelines is exercised without faulting or hanging a GPU. */
+ds_status ds_sampler_selftest_wait(ds_sampler* sampler, int64_t limit_ns, void* stream);
+
 /* Read-only view of an internal buffer of the last step, for tests and profiling.
  * which: 0 = scaled logits y [B*L, V] float; 1 = row statistics [B*L] x {m, l, entropy, argmax};
  * 2 = bf16 high part of exp(y - m) [B*L, V]; 3 = bf16 low part. *ptr is [device]. */

@@ -45,6 +45,10 @@ from .sampler import (  # noqa: F401
     softmax_stats,
     sampler_step,
     lock_update,
+    entropy_budget_update,
+    scheduled_temperature,
+    LOCK_THRESHOLD,
+    LOCK_ENTROPY_BUDGET,
     standin_hidden,
     denoise_loop,
 )

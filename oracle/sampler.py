@@ -27,6 +27,8 @@ The pages print no sampler listing; the readings taken where they are silent:
 * a sequence is done when every position is locked; done sequences are left untouched;
 * temperature divides the logits for the softmax, the entropy, s and the sample alike;
 * top-k keeps s and the entropy on the full softmax;
+* the pages' own default sampler (sokufu.com, "A diffusion language model refines 256 tokens
+  in 12 steps", and its Table 2) is the second lock rule, see entropy_budget_update;
 * random draws come from Philox4x32-10 keyed by the seed (low, high word), with counters
     Gumbel  (j >> 2, i, b, 4*step + 0), word j & 3, u = (2*(r >> 9) + 1) / 2**24,
     re-noise (i >> 2, 0, b, 4*step + 1), word i & 3, token = (r * V) >> 32.
@@ -41,6 +43,18 @@ from .philox import philox4x32_10, seed_key
 
 GUMBEL_STREAM = 0
 RENOISE_STREAM = 1
+
+LOCK_THRESHOLD = 0
+LOCK_ENTROPY_BUDGET = 1
+
+
+def scheduled_temperature(t_start: float, t_end: float, step: int, max_steps: int) -> float:
+    """Linear temperature schedule over the step budget: t_start at step 0, t_end at step
+    max_steps - 1 (Table 2 of the sokufu.com article: "Linear schedule from 0.8 down to 0.4";
+    the pages do not say over which steps, the budget is the plainest reading)."""
+    if max_steps <= 1:
+        return float(t_start)
+    return float(t_start) + (float(t_end) - float(t_start)) * float(step) / float(max_steps - 1)
 
 
 # --------------------------------------------------------------------------------------
@@ -155,7 +169,8 @@ def _sample_row(y_row, g_row, p_row, top_k, band=1e-4):
 
 
 def sampler_step(H, E, T, tau, canvas, lock, step, done, seed, *, top_k=0, max_steps=48,
-                 positions=None, row_chunk=64):
+                 positions=None, row_chunk=64, lock_rule=LOCK_THRESHOLD, entropy_budget=0.1,
+                 stop_entropy=0.005, t_schedule=None, prev_argmax=None):
     """One sampler step over a batch, in fp64.
 
     H [B, L, d] and E [V, d] are the exact input values as float64 (bf16 or fp32 inputs
@@ -168,7 +183,11 @@ def sampler_step(H, E, T, tau, canvas, lock, step, done, seed, *, top_k=0, max_s
     top-k boundary gaps.
 
     With ``positions`` set, only those positions are computed and the lock update is
-    skipped (it needs the whole canvas)."""
+    skipped (it needs the whole canvas).
+
+    lock_rule LOCK_ENTROPY_BUDGET replaces the threshold rule by entropy_budget_update
+    (prev_argmax [B, L] carries the previous step's argmax); t_schedule = (t_start, t_end)
+    replaces T by the scheduled temperature of each sequence's step."""
     H = np.asarray(H, dtype=np.float64)
     E = np.asarray(E, dtype=np.float64)
     B, L, d = H.shape
@@ -191,7 +210,9 @@ def sampler_step(H, E, T, tau, canvas, lock, step, done, seed, *, top_k=0, max_s
             continue
         for c0 in range(0, len(pos), row_chunk):
             rows = pos[c0:c0 + row_chunk]
-            y = (H[b, rows] @ E.T) / float(T[b])
+            Tb = (float(T[b]) if t_schedule is None else
+                  scheduled_temperature(t_schedule[0], t_schedule[1], int(step[b]), max_steps))
+            y = (H[b, rows] @ E.T) / Tb
             m, l, p, ent, am = softmax_stats(y)
             out["s"][b, rows] = p @ E
             out["entropy"][b, rows] = ent
@@ -213,16 +234,60 @@ def sampler_step(H, E, T, tau, canvas, lock, step, done, seed, *, top_k=0, max_s
                     out["topk_gap"][b, i] = ys[-top_k] - ys[-top_k - 1]
     new = {k: np.array(v, copy=True) for k, v in
            (("canvas", canvas), ("lock", lock), ("step", step), ("done", done))}
+    new["prev_argmax"] = (np.full((B, L), -1, np.int64) if prev_argmax is None
+                          else np.array(prev_argmax, copy=True))
     if positions is None:
         for b in range(B):
             if done[b]:
                 continue
-            cv, lk, st, dn = lock_update(new["canvas"][b], new["lock"][b], out["sampled"][b],
-                                         out["conf"][b], float(tau[b]), int(step[b]), seed, b,
-                                         V, max_steps)
+            if lock_rule == LOCK_ENTROPY_BUDGET:
+                cv, lk, st, dn, pa = entropy_budget_update(
+                    new["canvas"][b], out["sampled"][b], out["entropy"][b], out["argmax"][b],
+                    new["prev_argmax"][b], int(step[b]), seed, b, V, max_steps, entropy_budget,
+                    stop_entropy)
+                new["prev_argmax"][b] = pa
+            else:
+                cv, lk, st, dn = lock_update(new["canvas"][b], new["lock"][b], out["sampled"][b],
+                                             out["conf"][b], float(tau[b]), int(step[b]), seed,
+                                             b, V, max_steps)
             new["canvas"][b], new["lock"][b], new["step"][b], new["done"][b] = cv, lk, st, dn
     out.update(new)
     return out
+
+
+def entropy_budget_update(canvas_b, sampled_b, entropy_b, argmax_b, prev_argmax_b, step_b, seed,
+                          b, V, max_steps, budget=0.1, stop_entropy=0.005):
+    """The pages' default sampler step for one sequence (sokufu.com, "A diffusion language
+    model refines 256 tokens in 12 steps" and Table 2).
+
+    Tokens are accepted from the lowest to the highest entropy until the entropy budget is
+    spent (the longest prefix of the ascending order whose entropies sum to at most the budget,
+    and at least one position; equal entropies in position order); every other position is
+    re-noised uniformly. Acceptance is decided afresh every step (tokens stay editable).
+    The canvas stops when its mean entropy is below stop_entropy and the argmax predictions
+    equal those of the previous step; a stopped canvas, or one at its last allowed step, takes
+    the argmax predictions. Negative entropies from rounding count as zero.
+
+    Returns (canvas, lock = accepted this step, step + 1, done, argmax for the next step)."""
+    L = len(canvas_b)
+    H = np.maximum(np.asarray(entropy_b, dtype=np.float64), 0.0)
+    argmax_b = np.asarray(argmax_b)
+    stable = step_b > 0 and np.array_equal(argmax_b, np.asarray(prev_argmax_b))
+    stop = bool(H.mean() < stop_entropy and stable)
+    if stop or step_b + 1 >= max_steps:
+        return (argmax_b.astype(np.asarray(canvas_b).dtype), np.ones(L, np.uint8), step_b + 1, 1,
+                argmax_b.copy())
+    order = np.lexsort((np.arange(L), H))
+    cum = np.cumsum(H[order])
+    n_acc = max(1, int(np.count_nonzero(cum <= budget)))
+    accepted = np.zeros(L, bool)
+    accepted[order[:n_acc]] = True
+    canvas = np.array(canvas_b, copy=True)
+    canvas[accepted] = np.asarray(sampled_b)[accepted]
+    rest = np.nonzero(~accepted)[0]
+    if rest.size:
+        canvas[rest] = renoise_tokens(seed, b, rest, step_b, V)
+    return canvas, accepted.astype(np.uint8), step_b + 1, 0, argmax_b.copy()
 
 
 def lock_update(canvas_b, lock_b, sampled_b, conf_b, tau_b, step_b, seed, b, V, max_steps):
@@ -268,7 +333,8 @@ def standin_hidden(W_bits, s_prev, E, canvas):
 
 
 def denoise_loop(E, T, tau, canvas, lock, step, done, seed, *, H=None, W_bits=None,
-                 s_prev=None, top_k=0, max_steps=48, max_iters=None):
+                 s_prev=None, top_k=0, max_steps=48, max_iters=None, lock_rule=LOCK_THRESHOLD,
+                 entropy_budget=0.1, stop_entropy=0.005, t_schedule=None, prev_argmax=None):
     """Run steps until every sequence is done (or max_iters); returns the per-step records.
 
     Fixed-H mode passes H (fp64 [B, L, d]); stand-in mode passes W_bits and recomputes H
@@ -278,7 +344,9 @@ def denoise_loop(E, T, tau, canvas, lock, step, done, seed, *, H=None, W_bits=No
     d = E.shape[1]
     state = {"canvas": np.array(canvas), "lock": np.array(lock), "step": np.array(step),
              "done": np.array(done),
-             "s": np.zeros((B, L, d)) if s_prev is None else np.array(s_prev, np.float64)}
+             "s": np.zeros((B, L, d)) if s_prev is None else np.array(s_prev, np.float64),
+             "prev_argmax": (np.full((B, L), -1, np.int64) if prev_argmax is None
+                             else np.array(prev_argmax))}
     records = []
     iters = max_steps if max_iters is None else max_iters
     for _ in range(iters):
@@ -287,12 +355,15 @@ def denoise_loop(E, T, tau, canvas, lock, step, done, seed, *, H=None, W_bits=No
         Hs = H if W_bits is None else bf16_bits_to_f64(
             standin_hidden(W_bits, state["s"], E, state["canvas"]))
         out = sampler_step(Hs, E, T, tau, state["canvas"], state["lock"], state["step"],
-                           state["done"], seed, top_k=top_k, max_steps=max_steps)
+                           state["done"], seed, top_k=top_k, max_steps=max_steps,
+                           lock_rule=lock_rule, entropy_budget=entropy_budget,
+                           stop_entropy=stop_entropy, t_schedule=t_schedule,
+                           prev_argmax=state["prev_argmax"])
         out["H"] = Hs
         active = state["done"] == 0
         s_new = state["s"].copy()
         s_new[active] = out["s"][active]
         state = {"canvas": out["canvas"], "lock": out["lock"], "step": out["step"],
-                 "done": out["done"], "s": s_new}
+                 "done": out["done"], "s": s_new, "prev_argmax": out["prev_argmax"]}
         records.append(out)
     return state, records

@@ -335,3 +335,68 @@ def test_standin_hidden_brute_force():
             v = math.tanh(math.fsum(W[k, m] * u[m] for m in range(2 * d)))
             want = O.bf16_bits_to_f64(O.f64_to_bf16_bits(np.array([v])))[0]
             assert H[0, i, k] == want
+
+
+# ---------------------------------------------------------------- the pages' default sampler
+
+@pytest.mark.parametrize("case", _golden()["entropy_budget_cases"], ids=lambda c: c["name"])
+def test_closed_form_entropy_budget_cases(case):
+    V = 16
+    cv, lk, st, dn, pa = O.entropy_budget_update(
+        np.array(case["canvas"]), np.array(case["sampled"]), np.array(case["entropy"]),
+        np.array(case["argmax"]), np.array(case["prev_argmax"]), case["step"], 31, 1, V,
+        case["max_steps"], case["budget"], case["stop_entropy"])
+    assert lk.tolist() == case["lock_after"]
+    for i, tok in case["accepted_tokens"].items():
+        assert cv[int(i)] == tok
+    expect = O.renoise_tokens(31, 1, np.array(case["renoised"], dtype=np.int64), case["step"], V)
+    assert cv[case["renoised"]].tolist() == expect.tolist()
+    assert (st, dn) == (case["step_after"], case["done_after"])
+    assert pa.tolist() == case["argmax"]
+
+
+def test_closed_form_temperature_schedule():
+    t = _golden()["temperature_schedule"]
+    for k, want in t["points"].items():
+        got = O.scheduled_temperature(t["t_start"], t["t_end"], int(k), t["max_steps"])
+        assert got == pytest.approx(want, rel=1e-15)
+
+
+def test_entropy_budget_invariants_random():
+    rng = np.random.default_rng(17)
+    V, L = 500, 40
+    for _ in range(300):
+        H = rng.exponential(rng.choice([0.002, 0.02, 0.2]), L)
+        am = rng.integers(0, V, L)
+        prev = am.copy() if rng.random() < 0.5 else rng.integers(0, V, L)
+        step = int(rng.integers(0, 48))
+        sampled = rng.integers(0, V, L)
+        cv, lk, st, dn, pa = O.entropy_budget_update(rng.integers(0, V, L), sampled, H, am, prev,
+                                                     step, 3, 0, V, 48)
+        acc = lk == 1
+        assert acc.sum() >= 1 and st == step + 1
+        if dn:
+            assert np.array_equal(cv, am) and acc.all()
+        else:
+            assert np.array_equal(cv[acc], sampled[acc])
+            # accepted = a prefix of the ascending entropies within the budget
+            order = np.lexsort((np.arange(L), H))
+            k = acc.sum()
+            assert set(order[:k]) == set(np.nonzero(acc)[0])
+            assert k == 1 or H[order[:k]].sum() <= 0.1 + 1e-12
+            assert k == L or H[order[:k + 1]].sum() > 0.1
+
+
+def test_entropy_budget_loop_stops_on_a_confident_stable_canvas():
+    # a canvas whose logits are very peaked settles: argmax stable, entropies ~0 -> stops early
+    rng = np.random.default_rng(5)
+    V, d, L = 64, 16, 8
+    E = rng.standard_normal((V, d))
+    t = rng.integers(0, V, L)
+    H = (40.0 * E[t] / np.linalg.norm(E[t], axis=1, keepdims=True))[None]
+    state, recs = O.denoise_loop(E, [1.0], [0.9], rng.integers(0, V, (1, L)),
+                                 np.zeros((1, L), np.uint8), np.zeros(1, np.int64),
+                                 np.zeros(1, np.uint8), seed=8, H=H, max_steps=48,
+                                 lock_rule=O.LOCK_ENTROPY_BUDGET, t_schedule=(0.8, 0.4))
+    assert state["done"][0] == 1 and len(recs) == 2  # step 0 cannot stop; step 1 does
+    assert np.array_equal(state["canvas"][0], recs[-1]["argmax"][0])
