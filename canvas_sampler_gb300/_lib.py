@@ -27,12 +27,16 @@ DS_IMPL_TENSOR = 1
 DS_IMPL_SIMT = 2
 DS_H_FIXED = 0
 DS_H_STANDIN = 1
+DS_LOCK_THRESHOLD = 0
+DS_LOCK_ENTROPY_BUDGET = 1
 
 
 class ds_sampler_config(ctypes.Structure):
     _fields_ = [("max_batch", c_int32), ("canvas_len", c_int32), ("d_model", c_int32),
                 ("dtype", c_int32), ("vocab", c_int64), ("top_k", c_int32),
-                ("max_steps", c_int32), ("impl", c_int32), ("reserved", c_int32)]
+                ("max_steps", c_int32), ("impl", c_int32), ("lock_rule", c_int32),
+                ("entropy_budget", ctypes.c_float), ("stop_entropy", ctypes.c_float),
+                ("t_start", ctypes.c_float), ("t_end", ctypes.c_float)]
 
 
 class ds_step_args(ctypes.Structure):
@@ -40,7 +44,7 @@ class ds_step_args(ctypes.Structure):
                 ("E", c_void_p), ("temperature", c_void_p), ("tau", c_void_p), ("step", c_void_p),
                 ("canvas", c_void_p), ("lock", c_void_p), ("done", c_void_p), ("s", c_void_p),
                 ("sampled", c_void_p), ("conf", c_void_p), ("entropy", c_void_p),
-                ("argmax", c_void_p)]
+                ("argmax", c_void_p), ("prev_argmax", c_void_p)]
 
 
 class ds_loop_args(ctypes.Structure):

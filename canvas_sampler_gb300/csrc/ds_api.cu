@@ -49,6 +49,7 @@ struct ds_sampler {
   float* Opart = nullptr;
   size_t opart_floats = 0;
   uint16_t* U = nullptr;  // stand-in operand [B*L, 2d] (tensor-core path)
+  float* Teff = nullptr;  // scheduled temperatures [B]
   uint32_t* err = nullptr;
   int32_t* iter = nullptr;
   int last_batch = 0;
@@ -119,6 +120,7 @@ ds_status check_step_args(const ds_sampler* s, const ds_step_args* a) {
       !a->done || !a->s || !a->sampled || !a->conf || !a->entropy || !a->argmax)
     return DS_ERR_INVALID_ARG;
   if (!aligned(a->H, 16) || !aligned(a->E, 16) || !aligned(a->s, 16)) return DS_ERR_INVALID_ARG;
+  if (s->cfg.lock_rule == DS_LOCK_ENTROPY_BUDGET && !a->prev_argmax) return DS_ERR_INVALID_ARG;
   return DS_OK;
 }
 
@@ -131,15 +133,21 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
   const int S = splits_for(s, B);
   s->last_batch = B;
   mark(s, -1, st);
+  const float* T = a->temperature;
+  if (s->cfg.t_start > 0.f) {
+    launch_temperature(a->step, B, s->cfg.t_start, s->cfg.t_end, s->cfg.max_steps, s->Teff, st);
+    T = s->Teff;
+    s->launches += 1;
+  }
   if (s->impl == DS_IMPL_TENSOR) {
     cudaError_t e = launch_logits_tc(static_cast<const uint16_t*>(a->H),
-                                     static_cast<const uint16_t*>(a->E), R, V, d, L,
-                                     a->temperature, a->done, s->Y, s->cs, s->err, st);
+                                     static_cast<const uint16_t*>(a->E), R, V, d, L, T, a->done,
+                                     s->Y, s->cs, s->err, st);
     if (e != cudaSuccess) return cuda_status(e);
     mark(s, 0, st);
     launch_row_merge(s->cs, (int)(V / kTcSegment), R, L, a->done, s->rs, st);
   } else {
-    launch_logits_simt(a->H, a->E, fp32, R, V, d, L, a->temperature, a->done, s->Y, st);
+    launch_logits_simt(a->H, a->E, fp32, R, V, d, L, T, a->done, s->Y, st);
     mark(s, 0, st);
     launch_chunk_stats(s->Y, R, V, L, a->done, s->cs, st);
     launch_row_merge(s->cs, s->n_chunks, R, L, a->done, s->rs, st);
@@ -162,8 +170,13 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
                          a->seed, a->sampled, a->conf, a->entropy, a->argmax, s->Opart, S, d, a->s,
                          st);
   mark(s, 5, st);
-  launch_lock(B, L, V, s->cfg.max_steps, a->seed, a->tau, a->sampled, a->conf, a->step, a->canvas,
-              a->lock, a->done, st);
+  if (s->cfg.lock_rule == DS_LOCK_ENTROPY_BUDGET)
+    launch_lock_entropy(B, L, V, s->cfg.max_steps, a->seed, s->cfg.entropy_budget,
+                        s->cfg.stop_entropy, a->sampled, a->entropy, a->argmax, a->prev_argmax,
+                        a->step, a->canvas, a->lock, a->done, st);
+  else
+    launch_lock(B, L, V, s->cfg.max_steps, a->seed, a->tau, a->sampled, a->conf, a->step,
+                a->canvas, a->lock, a->done, st);
   mark(s, 6, st);
   if (s->timing) {
     ++s->timed_steps;
@@ -266,6 +279,11 @@ ds_status ds_sampler_create(const ds_sampler_config* cfg, ds_sampler** out) {
   if (c.max_steps < 1 || c.max_steps > (1 << 28)) return DS_ERR_INVALID_ARG;
   if (c.impl != DS_IMPL_AUTO && c.impl != DS_IMPL_TENSOR && c.impl != DS_IMPL_SIMT)
     return DS_ERR_INVALID_ARG;
+  if (c.lock_rule != DS_LOCK_THRESHOLD && c.lock_rule != DS_LOCK_ENTROPY_BUDGET)
+    return DS_ERR_INVALID_ARG;
+  if (!(c.entropy_budget >= 0.f) || !(c.stop_entropy >= 0.f) || !(c.t_end == c.t_end) ||
+      (c.t_start > 0.f && !(c.t_end > 0.f)))
+    return DS_ERR_INVALID_ARG;
   const int n_chunks = n_chunks_of(c.vocab);
   if (c.top_k > 0 && (int64_t)n_chunks * c.top_k > kMaxTopKPool) return DS_ERR_UNSUPPORTED;
 
@@ -306,6 +324,7 @@ ds_status ds_sampler_create(const ds_sampler_config* cfg, ds_sampler** out) {
   s->best = carve<Best>(s, Rm * n_chunks, &e);
   if (c.top_k > 0) s->cand = carve<Cand>(s, Rm * n_chunks * c.top_k, &e);
   s->Opart = carve<float>(s, opart, &e);
+  s->Teff = carve<float>(s, (size_t)c.max_batch, &e);
   if (s->impl == DS_IMPL_TENSOR && c.d_model % 256 == 0) s->U = carve<uint16_t>(s, Rm * 2 * d, &e);
   s->opart_floats = opart;
   s->err = carve<uint32_t>(s, 4, &e);
@@ -360,10 +379,10 @@ ds_status ds_sampler_step_host(ds_sampler* s, const ds_step_args* h, void* strea
   const size_t Bm = (size_t)s->cfg.max_batch;
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   // staging layout for max_batch: H | s | T | tau | step | canvas | lock | done | sampled | conf
-  // | entropy | argmax
+  // | entropy | argmax | prev_argmax
   const size_t nH = up(Bm * L * d * esize(s->cfg.dtype)), nS = up(Bm * L * d * 4);
   const size_t nB4 = up(Bm * 4), nBL4 = up(Bm * L * 4), nBL1 = up(Bm * L), nB1 = up(Bm);
-  const size_t total = nH + nS + 3 * nB4 + nBL4 + nBL1 + nB1 + 4 * nBL4;
+  const size_t total = nH + nS + 3 * nB4 + nBL4 + nBL1 + nB1 + 5 * nBL4;
   if (!s->stage) {
     cudaError_t e = cudaMalloc(&s->stage, total);
     if (e != cudaSuccess) {
@@ -389,6 +408,7 @@ ds_status ds_sampler_step_host(ds_sampler* s, const ds_step_args* h, void* strea
   a.conf = reinterpret_cast<float*>(p); p += nBL4;
   a.entropy = reinterpret_cast<float*>(p); p += nBL4;
   a.argmax = reinterpret_cast<int32_t*>(p); p += nBL4;
+  a.prev_argmax = h->prev_argmax ? reinterpret_cast<int32_t*>(p) : nullptr; p += nBL4;
   cudaError_t e = cudaSuccess;
   auto h2d = [&](const void* dst, const void* src, size_t n) {
     if (e == cudaSuccess)
@@ -404,6 +424,7 @@ ds_status ds_sampler_step_host(ds_sampler* s, const ds_step_args* h, void* strea
   h2d(a.canvas, h->canvas, B * L * 4);
   h2d(a.lock, h->lock, B * L);
   h2d(a.done, h->done, B);
+  if (a.prev_argmax) h2d(a.prev_argmax, h->prev_argmax, B * L * 4);
   if (e != cudaSuccess) return cuda_status(e);
   ds_status r = check_step_args(s, &a);
   if (r != DS_OK) return r;
@@ -418,6 +439,7 @@ ds_status ds_sampler_step_host(ds_sampler* s, const ds_step_args* h, void* strea
   d2h(h->canvas, a.canvas, B * L * 4);
   d2h(h->lock, a.lock, B * L);
   d2h(h->done, a.done, B);
+  if (a.prev_argmax) d2h(h->prev_argmax, a.prev_argmax, B * L * 4);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   return cuda_status(e);
 }

@@ -43,6 +43,12 @@ void launch_reduce_s(const float* Opart, int S, int R, int d, int L, const uint8
 void launch_lock(int B, int L, int64_t V, int max_steps, uint64_t seed, const float* tau,
                  const int32_t* sampled, const float* conf, int32_t* step, int32_t* canvas,
                  uint8_t* lock, uint8_t* done, cudaStream_t st);
+void launch_temperature(const int32_t* step, int B, float t_start, float t_end, int max_steps,
+                        float* T, cudaStream_t st);
+void launch_lock_entropy(int B, int L, int64_t V, int max_steps, uint64_t seed, float budget,
+                         float stop_entropy, const int32_t* sampled, const float* entropy,
+                         const int32_t* argmax, int32_t* prev_argmax, int32_t* step,
+                         int32_t* canvas, uint8_t* lock, uint8_t* done, cudaStream_t st);
 void launch_wait_selftest(uint64_t limit_ns, uint32_t* err, cudaStream_t st);
 void launch_philox(const uint32_t* ctr, uint64_t seed, uint32_t* out, int64_t n, cudaStream_t st);
 void launch_loop_begin(const uint8_t* done, int B, int32_t* iter, int max_iters,

@@ -69,6 +69,9 @@ extern "C" ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg,
   if (c.top_k < 0 || c.top_k > kMaxTopK || c.max_steps < 1) return DS_ERR_INVALID_ARG;
   if (c.impl != DS_IMPL_AUTO && c.impl != DS_IMPL_TENSOR && c.impl != DS_IMPL_SIMT)
     return DS_ERR_INVALID_ARG;
+  if (c.lock_rule != DS_LOCK_THRESHOLD && c.lock_rule != DS_LOCK_ENTROPY_BUDGET)
+    return DS_ERR_INVALID_ARG;
+  if (c.lock_rule == DS_LOCK_ENTROPY_BUDGET && !a->prev_argmax) return DS_ERR_INVALID_ARG;
   if (a->batch < 1 || (int64_t)a->batch * c.canvas_len > 65535) return DS_ERR_INVALID_ARG;
   if (!a->H || !a->E || !a->temperature || !a->tau || !a->step || !a->canvas || !a->lock ||
       !a->done || !a->s || !a->sampled || !a->conf || !a->entropy || !a->argmax)
@@ -107,7 +110,7 @@ extern "C" ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg,
   const size_t need = up(RV * 4) + 2 * up(RV * 2) + up((size_t)R * nstat * sizeof(ChunkStat)) +
                       up((size_t)R * sizeof(RowStat)) + up((size_t)R * nc * sizeof(Best)) +
                       (k > 0 ? up((size_t)R * nc * k * sizeof(Cand)) : 0) +
-                      up((size_t)S * R * d * 4) + 256;
+                      up((size_t)S * R * d * 4) + up((size_t)B * 4) + 256;
   if (need > kNoAllocScratchBytes) return DS_ERR_UNSUPPORTED;
 
   void* base = nullptr;
@@ -122,6 +125,7 @@ extern "C" ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg,
   Best* best = cv.take<Best>((size_t)R * nc);
   Cand* cand = k > 0 ? cv.take<Cand>((size_t)R * nc * k) : nullptr;
   float* Opart = cv.take<float>((size_t)S * R * d);
+  float* Teff = cv.take<float>((size_t)B);
   uint32_t* err = cv.take<uint32_t>(64);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -129,13 +133,18 @@ extern "C" ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg,
   // other region is fully written before it is read in this step.
   if (cudaMemsetAsync(err, 0, sizeof(uint32_t), s) != cudaSuccess) return DS_ERR_CUDA;
   const bool fp32 = c.dtype == DS_DTYPE_FP32;
+  const float* T = a->temperature;
+  if (c.t_start > 0.f) {
+    launch_temperature(a->step, B, c.t_start, c.t_end, c.max_steps, Teff, s);
+    T = Teff;
+  }
   if (tensor) {
     if (launch_logits_tc(static_cast<const uint16_t*>(a->H), static_cast<const uint16_t*>(a->E), R,
-                         V, d, L, a->temperature, a->done, Y, cs, err, s) != cudaSuccess)
+                         V, d, L, T, a->done, Y, cs, err, s) != cudaSuccess)
       return DS_ERR_CUDA;
     launch_row_merge(cs, (int)(V / kTcSegment), R, L, a->done, rs, s);
   } else {
-    launch_logits_simt(a->H, a->E, fp32, R, V, d, L, a->temperature, a->done, Y, s);
+    launch_logits_simt(a->H, a->E, fp32, R, V, d, L, T, a->done, Y, s);
     launch_chunk_stats(Y, R, V, L, a->done, cs, s);
     launch_row_merge(cs, nc, R, L, a->done, rs, s);
   }
@@ -151,7 +160,12 @@ extern "C" ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg,
   launch_reduce_s(Opart, S, R, d, L, a->done, rs, a->s, s);
   launch_finalize(rs, best, cand, nc, k, R, L, a->done, a->step, a->seed, a->sampled, a->conf,
                   a->entropy, a->argmax, s);
-  launch_lock(B, L, V, c.max_steps, a->seed, a->tau, a->sampled, a->conf, a->step, a->canvas,
-              a->lock, a->done, s);
+  if (c.lock_rule == DS_LOCK_ENTROPY_BUDGET)
+    launch_lock_entropy(B, L, V, c.max_steps, a->seed, c.entropy_budget, c.stop_entropy,
+                        a->sampled, a->entropy, a->argmax, a->prev_argmax, a->step, a->canvas,
+                        a->lock, a->done, s);
+  else
+    launch_lock(B, L, V, c.max_steps, a->seed, a->tau, a->sampled, a->conf, a->step, a->canvas,
+                a->lock, a->done, s);
   return cudaGetLastError() == cudaSuccess ? DS_OK : DS_ERR_CUDA;
 }

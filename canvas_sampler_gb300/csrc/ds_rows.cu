@@ -612,6 +612,102 @@ __global__ void k_loop_end(const uint8_t* __restrict__ done, int B, int32_t* ite
   }
 }
 
+// Per-sequence temperature of the linear schedule at each sequence's step.
+__global__ void k_temperature(const int32_t* __restrict__ step, int B, float t_start, float t_end,
+                              int max_steps, float* __restrict__ T) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  T[b] = max_steps > 1
+             ? t_start + (t_end - t_start) * ((float)step[b] / (float)(max_steps - 1))
+             : t_start;
+}
+
+// The pages' default sampler for one sequence per CTA (blockDim = L): accept positions from the
+// lowest to the highest entropy (ties in position order) until the budget is spent, at least
+// one; re-noise the others; stop on a confident (mean entropy < stop_entropy) and stable (argmax
+// unchanged) canvas, or at the last step, with the canvas set to the argmax. Entropies below zero
+// (rounding) count as zero. Sort: bitonic over the next power of two; the running sum is a
+// Hillis-Steele scan in a fixed order, so the result is deterministic.
+__global__ void __launch_bounds__(1024) k_lock_entropy(
+    int L, uint32_t V, int max_steps, uint64_t seed, float budget, float stop_entropy,
+    const int32_t* __restrict__ sampled, const float* __restrict__ entropy,
+    const int32_t* __restrict__ argmax, int32_t* __restrict__ prev_argmax,
+    int32_t* __restrict__ step, int32_t* __restrict__ canvas, uint8_t* __restrict__ lock,
+    uint8_t* __restrict__ done) {
+  __shared__ float key[1024];
+  __shared__ int32_t idx[1024];
+  __shared__ int32_t rank_of[1024];
+  __shared__ float shf[32];
+  const int b = blockIdx.x, i = threadIdx.x;
+  if (done[b]) return;
+  const size_t at = (size_t)b * L + i;
+  const int st = step[b];
+  const float h = fmaxf(entropy[at], 0.f);
+  const int32_t am = argmax[at];
+  const int same = __syncthreads_and(am == prev_argmax[at]);
+  const float mean = block_sum(h, shf) / (float)L;
+  const bool stop = st > 0 && same && mean < stop_entropy;
+  if (stop || st + 1 >= max_steps) {
+    canvas[at] = am;
+    lock[at] = 1;
+    prev_argmax[at] = am;
+    if (i == 0) {
+      step[b] = st + 1;
+      done[b] = 1;
+    }
+    return;
+  }
+  int P = 1;
+  while (P < L) P <<= 1;
+  for (int t = i; t < P; t += blockDim.x) {  // t < L only for t == i
+    key[t] = t < L ? h : INFINITY;
+    idx[t] = t;
+  }
+  __syncthreads();
+  for (int kk = 2; kk <= P; kk <<= 1) {
+    for (int j = kk >> 1; j > 0; j >>= 1) {
+      for (int t = i; t < P / 2; t += blockDim.x) {
+        const int i1 = 2 * j * (t / j) + (t % j), i2 = i1 + j;
+        const bool up = (i1 & kk) == 0;
+        const bool gt = key[i1] > key[i2] || (key[i1] == key[i2] && idx[i1] > idx[i2]);
+        if (gt == up) {
+          const float tk = key[i1];
+          key[i1] = key[i2];
+          key[i2] = tk;
+          const int32_t ti = idx[i1];
+          idx[i1] = idx[i2];
+          idx[i2] = ti;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // inclusive running sum of the sorted entropies, thread r holding rank r
+  float v = key[i];
+  rank_of[idx[i]] = i;
+  __syncthreads();
+  for (int off = 1; off < L; off <<= 1) {
+    const float t = i >= off ? key[i - off] : 0.f;
+    __syncthreads();
+    v += t;
+    key[i] = v;
+    __syncthreads();
+  }
+  const int n_acc = max(1, __syncthreads_count(v <= budget));
+  const bool accepted = rank_of[i] < n_acc;
+  if (accepted) {
+    canvas[at] = sampled[at];
+  } else {
+    const u32x4 w = philox4x32_10(u32x4{(uint32_t)(i >> 2), 0u, (uint32_t)b,
+                                        ((uint32_t)st << 2) | kRenoiseStream},
+                                  (uint32_t)seed, (uint32_t)(seed >> 32));
+    canvas[at] = token_from_word(word_of(w, i & 3), V);
+  }
+  lock[at] = accepted ? 1 : 0;
+  prev_argmax[at] = am;
+  if (i == 0) step[b] = st + 1;
+}
+
 // A wait that nothing will satisfy: one mbarrier expecting one arrival that never comes.
 __global__ void k_wait_selftest(uint64_t limit_ns, uint32_t* err) {
   __shared__ uint64_t bar;
@@ -629,6 +725,19 @@ __global__ void k_wait_selftest(uint64_t limit_ns, uint32_t* err) {
 }
 
 }  // namespace
+
+void launch_temperature(const int32_t* step, int B, float t_start, float t_end, int max_steps,
+                        float* T, cudaStream_t st) {
+  k_temperature<<<(B + 127) / 128, 128, 0, st>>>(step, B, t_start, t_end, max_steps, T);
+}
+
+void launch_lock_entropy(int B, int L, int64_t V, int max_steps, uint64_t seed, float budget,
+                         float stop_entropy, const int32_t* sampled, const float* entropy,
+                         const int32_t* argmax, int32_t* prev_argmax, int32_t* step,
+                         int32_t* canvas, uint8_t* lock, uint8_t* done, cudaStream_t st) {
+  k_lock_entropy<<<B, L, 0, st>>>(L, (uint32_t)V, max_steps, seed, budget, stop_entropy, sampled,
+                                  entropy, argmax, prev_argmax, step, canvas, lock, done);
+}
 
 void launch_wait_selftest(uint64_t limit_ns, uint32_t* err, cudaStream_t st) {
   k_wait_selftest<<<1, 32, 0, st>>>(limit_ns, err);

@@ -14,6 +14,7 @@ from . import _lib as C
 
 _DTYPES = {"bf16": (C.DS_DTYPE_BF16, torch.bfloat16), "fp32": (C.DS_DTYPE_FP32, torch.float32)}
 _IMPLS = {"auto": C.DS_IMPL_AUTO, "tensor": C.DS_IMPL_TENSOR, "simt": C.DS_IMPL_SIMT}
+_LOCK_RULES = {"threshold": C.DS_LOCK_THRESHOLD, "entropy_budget": C.DS_LOCK_ENTROPY_BUDGET}
 
 
 def _ptr(t: torch.Tensor | None) -> int | None:
@@ -33,17 +34,21 @@ class CanvasState:
     lock: torch.Tensor  # [B, L] uint8
     step: torch.Tensor  # [B] int32
     done: torch.Tensor  # [B] uint8
+    prev_argmax: torch.Tensor | None = None  # [B, L] int32 (entropy-budget rule)
 
     @staticmethod
-    def from_numpy(canvas, lock, step, done, device="cuda"):
-        return CanvasState(torch.as_tensor(canvas, dtype=torch.int32).to(device).contiguous(),
-                           torch.as_tensor(lock, dtype=torch.uint8).to(device).contiguous(),
+    def from_numpy(canvas, lock, step, done, device="cuda", prev_argmax=None):
+        c = torch.as_tensor(canvas, dtype=torch.int32).to(device).contiguous()
+        pa = (torch.full_like(c, -1) if prev_argmax is None else
+              torch.as_tensor(prev_argmax, dtype=torch.int32).to(device).contiguous())
+        return CanvasState(c, torch.as_tensor(lock, dtype=torch.uint8).to(device).contiguous(),
                            torch.as_tensor(step, dtype=torch.int32).to(device).contiguous(),
-                           torch.as_tensor(done, dtype=torch.uint8).to(device).contiguous())
+                           torch.as_tensor(done, dtype=torch.uint8).to(device).contiguous(), pa)
 
     def clone(self) -> "CanvasState":
         return CanvasState(self.canvas.clone(), self.lock.clone(), self.step.clone(),
-                           self.done.clone())
+                           self.done.clone(),
+                           None if self.prev_argmax is None else self.prev_argmax.clone())
 
 
 @dataclass
@@ -68,7 +73,9 @@ class Sampler:
     """One sampler (workspace + graphs) on one CUDA device."""
 
     def __init__(self, vocab: int, d_model: int, *, canvas_len: int = 256, max_batch: int = 1,
-                 dtype: str = "bf16", top_k: int = 0, max_steps: int = 48, impl: str = "auto"):
+                 dtype: str = "bf16", top_k: int = 0, max_steps: int = 48, impl: str = "auto",
+                 lock_rule: str = "threshold", entropy_budget: float = 0.1,
+                 stop_entropy: float = 0.005, t_schedule: tuple | None = None):
         self.lib = C.load_library()
         if not torch.cuda.is_available():
             raise RuntimeError("the canvas sampler needs a CUDA device")
@@ -76,9 +83,14 @@ class Sampler:
         self.dtype_name = dtype
         self.dtype_code, self.torch_dtype = _DTYPES[dtype]
         self.top_k, self.max_steps = int(top_k), int(max_steps)
+        self.lock_rule = lock_rule
+        t0, t1 = (0.0, 0.0) if t_schedule is None else (float(t_schedule[0]), float(t_schedule[1]))
         cfg = C.ds_sampler_config(max_batch=self.max_batch, canvas_len=self.L, d_model=self.d,
                                   dtype=self.dtype_code, vocab=self.vocab, top_k=self.top_k,
-                                  max_steps=self.max_steps, impl=_IMPLS[impl], reserved=0)
+                                  max_steps=self.max_steps, impl=_IMPLS[impl],
+                                  lock_rule=_LOCK_RULES[lock_rule],
+                                  entropy_budget=float(entropy_budget),
+                                  stop_entropy=float(stop_entropy), t_start=t0, t_end=t1)
         self._cfg = cfg
         handle = c_void_p()
         C.check(self.lib.ds_sampler_create(byref(cfg), byref(handle)), "ds_sampler_create")
@@ -109,6 +121,7 @@ class Sampler:
                                             _ptr(state.done))
         a.s, a.sampled, a.conf, a.entropy, a.argmax = (_ptr(out.s), _ptr(out.sampled), _ptr(out.conf),
                                                        _ptr(out.entropy), _ptr(out.argmax))
+        a.prev_argmax = _ptr(state.prev_argmax)
         return a
 
     def _check_tensors(self, H, E, state, out, device_side=True):

@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define DS_SAMPLER_ABI_VERSION 1
+#define DS_SAMPLER_ABI_VERSION 2
 
 typedef enum ds_status {
   DS_OK = 0,
@@ -64,6 +64,14 @@ enum { DS_DTYPE_BF16 = 0, DS_DTYPE_FP32 = 1 };
  * SIMT = CUDA-core fp32 kernels (any supported dtype); AUTO = TENSOR where it applies. */
 enum { DS_IMPL_AUTO = 0, DS_IMPL_TENSOR = 1, DS_IMPL_SIMT = 2 };
 enum { DS_H_FIXED = 0, DS_H_STANDIN = 1 };
+/* Lock rule. THRESHOLD: lock unlocked positions with c >= tau (at least one per step, sticky),
+ * re-noise the rest, done when all are locked. ENTROPY_BUDGET: the pages' default sampler --
+ * accept positions from the lowest to the highest entropy until entropy_budget is spent (at
+ * least one), re-noise all others, decided afresh every step; stop when the mean entropy is
+ * below stop_entropy and the argmax equals the previous step's, or at the last step, with the
+ * canvas set to the argmax ("DiffusionGemma: Google's open diffusion LLM", "A diffusion
+ * language model refines 256 tokens in 12 steps" and Table 2). */
+enum { DS_LOCK_THRESHOLD = 0, DS_LOCK_ENTROPY_BUDGET = 1 };
 
 /* Sampler shape and options, fixed at creation.
  *   canvas_len  L, a multiple of 128 and at most 1024 (256 on the pages);
@@ -73,7 +81,12 @@ enum { DS_H_FIXED = 0, DS_H_STANDIN = 1 };
  *   dtype       storage type of H and E (DS_DTYPE_*);
  *   top_k       0 = sample from the full softmax, else 1..256: sample among the k largest logits;
  *   max_steps   step budget per canvas (48 on the pages); the last step locks every position;
- *   impl        DS_IMPL_*. */
+ *   impl        DS_IMPL_*;
+ *   lock_rule   DS_LOCK_*; entropy_budget (0.1 on the pages) and stop_entropy (0.005) are used
+ *               by DS_LOCK_ENTROPY_BUDGET;
+ *   t_start, t_end  temperature schedule: when t_start > 0 the temperature of a sequence at
+ *               step k is t_start + (t_end - t_start) k / (max_steps - 1) (0.8 -> 0.4 on the
+ *               pages) and the per-call temperature is ignored; t_start <= 0 turns it off. */
 typedef struct ds_sampler_config {
   int32_t max_batch;
   int32_t canvas_len;
@@ -83,7 +96,11 @@ typedef struct ds_sampler_config {
   int32_t top_k;
   int32_t max_steps;
   int32_t impl;
-  int32_t reserved;
+  int32_t lock_rule;
+  float entropy_budget;
+  float stop_entropy;
+  float t_start;
+  float t_end;
 } ds_sampler_config;
 
 typedef struct ds_sampler ds_sampler;
@@ -102,6 +119,8 @@ typedef struct ds_sampler ds_sampler;
  *   conf        [B, L] float        probability of x under the sampled distribution (out)
  *   entropy     [B, L] float        softmax entropy in nats (out)
  *   argmax      [B, L] int32        most likely token, lowest index on ties (out)
+ *   prev_argmax [B, L] int32        the previous step's argmax (in/out; DS_LOCK_ENTROPY_BUDGET
+ *                                   only, else may be NULL; any values at step 0)
  *   seed        key of the counter-based generator (Philox4x32-10); draws depend only on
  *               (seed, sequence, position, token, step), so any step boundary is a checkpoint. */
 typedef struct ds_step_args {
@@ -121,6 +140,7 @@ typedef struct ds_step_args {
   float* conf;
   float* entropy;
   int32_t* argmax;
+  int32_t* prev_argmax;
 } ds_step_args;
 
 /* Arguments of a denoising loop: steps repeat on the GPU until every sequence is done or

@@ -175,7 +175,7 @@ def test_host_entry_point_matches_device_step():
 def test_invalid_arguments_are_rejected():
     lib = C.load_library()
     cfg = C.ds_sampler_config(max_batch=1, canvas_len=200, d_model=256, dtype=0, vocab=4096,
-                              top_k=0, max_steps=48, impl=0, reserved=0)
+                              top_k=0, max_steps=48, impl=0)
     h = ctypes.c_void_p()
     assert lib.ds_sampler_create(ctypes.byref(cfg), ctypes.byref(h)) == C.DS_ERR_INVALID_ARG
     cfg.canvas_len = 256

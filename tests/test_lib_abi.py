@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol():
 def test_version_and_status_strings_without_gpu():
     C = _lib()
     lib = C.load_library()
-    assert lib.ds_abi_version() == 1
+    assert lib.ds_abi_version() == 2
     for code in range(7):
         assert lib.ds_status_string(code)
     assert lib.ds_status_string(99) == b"unknown status"
@@ -51,7 +51,7 @@ def test_create_rejects_bad_config_before_touching_the_device():
     C = _lib()
     lib = C.load_library()
     cfg = C.ds_sampler_config(max_batch=1, canvas_len=100, d_model=256, dtype=0, vocab=4096,
-                              top_k=0, max_steps=48, impl=0, reserved=0)
+                              top_k=0, max_steps=48, impl=0)
     h = ctypes.c_void_p()
     assert lib.ds_sampler_create(ctypes.byref(cfg), ctypes.byref(h)) == C.DS_ERR_INVALID_ARG
     assert lib.ds_sampler_create(None, ctypes.byref(h)) == C.DS_ERR_INVALID_ARG
@@ -66,8 +66,9 @@ PROBE = r"""
 int main(void) {
   printf("ds_sampler_config %zu\nds_step_args %zu\nds_loop_args %zu\n",
          sizeof(ds_sampler_config), sizeof(ds_step_args), sizeof(ds_loop_args));
-  P(ds_sampler_config, vocab) P(ds_sampler_config, top_k) P(ds_sampler_config, reserved)
-  P(ds_step_args, seed) P(ds_step_args, H) P(ds_step_args, argmax)
+  P(ds_sampler_config, vocab) P(ds_sampler_config, top_k) P(ds_sampler_config, lock_rule)
+  P(ds_sampler_config, entropy_budget) P(ds_sampler_config, t_end)
+  P(ds_step_args, seed) P(ds_step_args, H) P(ds_step_args, argmax) P(ds_step_args, prev_argmax)
   P(ds_loop_args, h_mode) P(ds_loop_args, W) P(ds_loop_args, H_buf)
   return 0;
 }

@@ -72,7 +72,7 @@ def test_no_alloc_step_rejects_what_does_not_fit():
     out = StepOutputs.empty(1, w.L, w.d)
     out.sampled.fill_(-3)
     cfg = C.ds_sampler_config(max_batch=1, canvas_len=w.L, d_model=w.d, dtype=0, vocab=w.V,
-                              top_k=0, max_steps=48, impl=0, reserved=0)
+                              top_k=0, max_steps=48, impl=0)
     a = _args(ref, H, E, T, tau, st, out, 1)
     rc = lib.ds_sampler_step_noalloc(ctypes.byref(cfg), ctypes.byref(a), None)
     assert rc == C.DS_ERR_UNSUPPORTED
