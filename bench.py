@@ -35,7 +35,10 @@ from canvas_sampler_gb300 import workloads as W  # noqa: E402
 
 METRIC = "canvas sampler steps/s & TFLOP/s (B=1, 256×262144 vocab) vs roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-PROFILE_FILE = os.path.join(ROOT, "profiles", "selfcond_tc_step_v262144_d2816.md")
+PROFILE_FILES = {
+    "vocab_pass": os.path.join(ROOT, "profiles", "vocab_pass_tc_step_v262144_d2816.md"),
+    "selfcond": os.path.join(ROOT, "profiles", "selfcond_tc_step_v262144_d2816.md"),
+}
 
 
 def parse_args():
@@ -45,7 +48,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=W.BENCH_WORKLOAD, choices=sorted(W.WORKLOADS))
-    ap.add_argument("--kernel-impl", default="auto", choices=["auto", "tensor", "simt"])
+    ap.add_argument("--kernel-impl", default="auto", choices=["auto", "tensor", "simt", "fused"])
     ap.add_argument("--vocab", type=int, default=None, help="override V (profiling runs)")
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling runs)")
     ap.add_argument("--e2e-steps", type=int, default=10)
@@ -144,30 +147,34 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-KERNEL_SOURCES = [os.path.join(ROOT, "canvas_sampler_gb300", "csrc", f)
-                  for f in ("ds_tc_selfcond.cu", "ds_tc_common.cuh", "ds_common.cuh")]
+KERNEL_SOURCES = {
+    k: [os.path.join(ROOT, "canvas_sampler_gb300", "csrc", f)
+        for f in (main, "ds_tc_common.cuh", "ds_common.cuh")]
+    for k, main in (("vocab_pass", "ds_tc_fused.cu"), ("selfcond", "ds_tc_selfcond.cu"))}
 
 
-def kernel_source_hash() -> str:
-    """sha256 over the self-conditioning kernel's sources (the files it is compiled from)."""
+def kernel_source_hash(kernel: str = "vocab_pass") -> str:
+    """sha256 over a tensor-core kernel's sources (the files it is compiled from)."""
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[kernel]:
         h.update(open(f, "rb").read())
     return h.hexdigest()
 
 
-def measured_traffic():
-    """DRAM bytes per launch of the self-conditioning kernel from the committed ncu summary,
-    if the kernel's sources have not changed since the capture (else None)."""
+def measured_traffic(kernel: str):
+    """DRAM bytes per launch of a kernel from its committed ncu summary, if the kernel's
+    sources have not changed since the capture (else None)."""
+    if kernel not in PROFILE_FILES:
+        return None
     try:
-        text = open(PROFILE_FILE).read()
+        text = open(PROFILE_FILES[kernel]).read()
     except OSError:
         return None
     m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     m_h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
     if not (m_b and m_h):
         return None
-    return float(m_b.group(1)) if kernel_source_hash() == m_h.group(1) else None
+    return float(m_b.group(1)) if kernel_source_hash(kernel) == m_h.group(1) else None
 
 
 def algorithmic_flops(w: W.Workload) -> float:
@@ -342,20 +349,29 @@ def run_ours(args):
     value = world * args.steps / (ms / 1e3)
     flops = algorithmic_flops(w)
     peaks, peak_src = load_peaks()
-    # dominant kernel: the self-conditioning GEMM (tensor cores); algorithmic work per launch is
-    # 2 B L V d (the bf16 hi/lo doubling of the tensor work is not algorithmic)
+    # dominant kernel: the fused vocabulary pass (logits and self-conditioning GEMMs, 4 B L V d
+    # algorithmic FLOP per launch; the phase named "logits" spans it, the convert and selfcond
+    # phases are empty), or on the unfused path the self-conditioning GEMM (2 B L V d). The bf16
+    # hi/lo doubling of the self-conditioning tensor work is not algorithmic.
+    fused = nsteps > 0 and phases.get("selfcond", 0.0) == 0.0 and phases.get("convert", 0.0) == 0.0
     dom = max(phases, key=phases.get) if nsteps else "selfcond"
     dom_ms = phases.get(dom, 0.0) / max(1, nsteps)
-    dom_flops = {"logits": 2.0 * w.B * w.L * w.V * w.d,
-                 "selfcond": 2.0 * w.B * w.L * w.V * w.d}.get(dom)
-    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    if fused and dom == "logits":
+        dom, dom_flops = "vocab_pass", 4.0 * w.B * w.L * w.V * w.d
+    else:
+        dom_flops = {"logits": 2.0 * w.B * w.L * w.V * w.d,
+                     "selfcond": 2.0 * w.B * w.L * w.V * w.d}.get(dom)
+    # the kernel runs back to back for the whole timed region (seconds under the power cap):
+    # the sustained bf16 peak is its denominator
+    peak_key = "bf16_tflops_sustained" if "bf16_tflops_sustained" in peaks else "bf16_tflops"
+    peak_tf = float(peaks.get(peak_key, FALLBACK_PEAKS[peak_key]))
     roof = None
     if dom_flops and dom_ms > 0:
         ach = dom_flops / (dom_ms / 1e3) / 1e12
-        traffic = measured_traffic()
+        traffic = measured_traffic(dom)
         roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": ach / peak_tf, "traffic": traffic,
-                "peak_source": f"bf16_tflops ({peak_src}, burst)"}
+                "peak_source": f"{peak_key} ({peak_src})"}
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
@@ -368,7 +384,8 @@ def run_ours(args):
         "tflops": world * flops / step_s / 1e12,
         "step_roofline": {"bound": "tensor", "achieved": flops / step_s / 1e12, "peak": peak_tf,
                           "unit": "TFLOP/s", "frac": flops / step_s / 1e12 / peak_tf,
-                          "note": "4 B L V d algorithmic FLOP per step over the whole step"},
+                          "note": "4 B L V d algorithmic FLOP per step over the whole step, "
+                                  f"against {peak_key}"},
         "roofline": roof,
         "phase_ms_per_step": {k: v / max(1, nsteps) for k, v in phases.items()},
         "gpu_launches": launches,

@@ -25,6 +25,7 @@ DS_DTYPE_FP32 = 1
 DS_IMPL_AUTO = 0
 DS_IMPL_TENSOR = 1
 DS_IMPL_SIMT = 2
+DS_IMPL_FUSED = 3
 DS_H_FIXED = 0
 DS_H_STANDIN = 1
 DS_LOCK_THRESHOLD = 0

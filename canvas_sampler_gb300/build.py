@@ -20,7 +20,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB_NAME = "libds_sampler.so"
 SOURCES = ["ds_api.cu", "ds_rows.cu", "ds_simt.cu", "ds_tc.cu", "ds_tc_logits.cu",
-           "ds_tc_selfcond.cu", "ds_noalloc.cu"]
+           "ds_tc_selfcond.cu", "ds_tc_fused.cu", "ds_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

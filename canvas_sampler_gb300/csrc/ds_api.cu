@@ -1,7 +1,12 @@
 // C ABI of the canvas sampler (include/ds_sampler.h): argument validation, the workspace, the
 // order of kernel launches in a step, the host-buffer variant and the CUDA-graph denoising loop.
 //
-// A step enqueues, on the caller's stream:
+// A step enqueues, on the caller's stream, with the tensor cores and top_k = 0:
+//   fused vocabulary pass (ds_tc_fused.cu)    -> segment statistics and Gumbel winners, O
+//   row merge                                 -> m, l, entropy, argmax, sample per row
+//   finalize (s = O / l, confidence)
+//   lock / re-noise / stop
+// otherwise (top-k, or the CUDA-core path for fp32 inputs):
 //   logits GEMM (tensor cores or CUDA cores)  -> y [B*L, V] fp32
 //   chunk statistics, row merge               -> m, l, entropy, argmax per row
 //   [top-k candidates per chunk]
@@ -12,6 +17,7 @@
 // The loop (report section 6, "Eliminating CPU-GPU synchronization") is one graph launch: a
 // while node whose condition the last kernel of each iteration sets from the done flags.
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -36,6 +42,8 @@ struct ds_sampler {
   ds_sampler_config cfg{};
   int device = 0;
   int impl = DS_IMPL_SIMT;
+  bool fused = false;     // tensor cores, top_k = 0: the fused vocabulary pass
+  int vp_producers = 0;   // CTAs that start as producers in the fused pass (0: default)
   int num_sms = 1;
   int n_chunks = 1;
   size_t ws_bytes = 0;
@@ -50,6 +58,10 @@ struct ds_sampler {
   size_t opart_floats = 0;
   uint16_t* U = nullptr;  // stand-in operand [B*L, 2d] (tensor-core path)
   float* Teff = nullptr;  // scheduled temperatures [B]
+  ChunkStat* seg = nullptr;  // fused pass: segment statistics [B*L, V/128]
+  float* mseg_t = nullptr;   // fused pass: segment maxima [V/128, B*L]
+  float* mref = nullptr;     // fused pass: reference maxima of the range partials [Q, B*L]
+  uint32_t* vp_sync = nullptr;
   uint32_t* err = nullptr;
   int32_t* iter = nullptr;
   int last_batch = 0;
@@ -94,7 +106,7 @@ int splits_for(const ds_sampler* s, int batch) {
   const int R = batch * s->cfg.canvas_len;
   const int64_t V = s->cfg.vocab;
   const int d = s->cfg.d_model;
-  if (s->impl == DS_IMPL_TENSOR) return selfcond_tc_splits(R, V, d, s->num_sms);
+  if (s->impl != DS_IMPL_SIMT) return selfcond_tc_splits(R, V, d, s->num_sms);
   // CUDA-core GEMM: aim at about four waves of 128 x 64 tiles, >= 1024 tokens per split
   const long tiles = (long)(d / 64) * (R / 128);
   long S = (4L * s->num_sms + tiles - 1) / tiles;
@@ -139,7 +151,26 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
     T = s->Teff;
     s->launches += 1;
   }
-  if (s->impl == DS_IMPL_TENSOR) {
+  if (s->fused) {
+    const VocabPassShape sh = vocab_pass_shape(R, V, d, s->num_sms, s->vp_producers);
+    cudaError_t e = launch_vocab_pass_tc(
+        sh, static_cast<const uint16_t*>(a->H), static_cast<const uint16_t*>(a->E), R, V, d, L,
+        T, a->done, a->step, a->seed, s->Phi, s->Plo, s->seg, s->mseg_t, s->Opart, s->mref,
+        s->vp_sync, s->err, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    mark(s, 0, st);
+    launch_row_merge(s->seg, (int)(V / kVpSegment), R, L, a->done, s->rs, st);
+    mark(s, 1, st);
+    mark(s, 2, st);
+    launch_gumbel_seg(s->Phi, s->Plo, s->seg, s->rs, R, V, L, a->done, a->step, a->seed, s->best,
+                      st);
+    mark(s, 3, st);
+    mark(s, 4, st);
+    launch_finalize_with_s(s->rs, s->best, nullptr, s->n_chunks, 0, R, L, a->done, a->step,
+                           a->seed, a->sampled, a->conf, a->entropy, a->argmax, s->Opart,
+                           sh.n_ranges, d, a->s, s->mref, st);
+    s->launches += 4;
+  } else if (s->impl != DS_IMPL_SIMT) {
     cudaError_t e = launch_logits_tc(static_cast<const uint16_t*>(a->H),
                                      static_cast<const uint16_t*>(a->E), R, V, d, L, T, a->done,
                                      s->Y, s->cs, s->err, st);
@@ -152,23 +183,26 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
     launch_chunk_stats(s->Y, R, V, L, a->done, s->cs, st);
     launch_row_merge(s->cs, s->n_chunks, R, L, a->done, s->rs, st);
   }
-  mark(s, 1, st);
-  if (k > 0) launch_topk_chunk(s->Y, R, V, L, a->done, k, s->cand, st);
-  mark(s, 2, st);
-  launch_convert(s->Y, s->rs, R, V, L, a->done, a->step, a->seed, k == 0, s->Phi, s->Plo, s->best,
-                 st);
-  mark(s, 3, st);
-  if (s->impl == DS_IMPL_TENSOR) {
-    cudaError_t e = launch_selfcond_tc(s->Phi, s->Plo, static_cast<const uint16_t*>(a->E), R, V, d,
-                                       L, a->done, S, s->Opart, s->err, st);
-    if (e != cudaSuccess) return cuda_status(e);
-  } else {
-    launch_selfcond_simt(s->Phi, s->Plo, a->E, fp32, R, V, d, L, a->done, S, s->Opart, st);
+  if (!s->fused) {
+    mark(s, 1, st);
+    if (k > 0) launch_topk_chunk(s->Y, R, V, L, a->done, k, s->cand, st);
+    mark(s, 2, st);
+    launch_convert(s->Y, s->rs, R, V, L, a->done, a->step, a->seed, k == 0, s->Phi, s->Plo,
+                   s->best, st);
+    mark(s, 3, st);
+    if (s->impl != DS_IMPL_SIMT) {
+      cudaError_t e = launch_selfcond_tc(s->Phi, s->Plo, static_cast<const uint16_t*>(a->E), R,
+                                         V, d, L, a->done, S, s->Opart, s->err, st);
+      if (e != cudaSuccess) return cuda_status(e);
+    } else {
+      launch_selfcond_simt(s->Phi, s->Plo, a->E, fp32, R, V, d, L, a->done, S, s->Opart, st);
+    }
+    mark(s, 4, st);
+    launch_finalize_with_s(s->rs, s->best, s->cand, s->n_chunks, k, R, L, a->done, a->step,
+                           a->seed, a->sampled, a->conf, a->entropy, a->argmax, s->Opart, S, d,
+                           a->s, nullptr, st);
+    s->launches += (s->impl != DS_IMPL_SIMT ? 5 : 6) + (k > 0 ? 1 : 0);
   }
-  mark(s, 4, st);
-  launch_finalize_with_s(s->rs, s->best, s->cand, s->n_chunks, k, R, L, a->done, a->step,
-                         a->seed, a->sampled, a->conf, a->entropy, a->argmax, s->Opart, S, d, a->s,
-                         st);
   mark(s, 5, st);
   if (s->cfg.lock_rule == DS_LOCK_ENTROPY_BUDGET)
     launch_lock_entropy(B, L, V, s->cfg.max_steps, a->seed, s->cfg.entropy_budget,
@@ -182,7 +216,7 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
     ++s->timed_steps;
     s->timed_stream = st;
   }
-  s->launches += (s->impl == DS_IMPL_TENSOR ? 6 : 7) + (k > 0 ? 1 : 0);
+  s->launches += 1;
   return cuda_status(cudaGetLastError());
 }
 
@@ -190,7 +224,7 @@ ds_status enqueue_standin(ds_sampler* s, const void* W, const float* s_prev, con
                           const int32_t* canvas, const uint8_t* done, void* H_out, int batch,
                           cudaStream_t st) {
   const int d = s->cfg.d_model, L = s->cfg.canvas_len, R = batch * L;
-  if (s->impl == DS_IMPL_TENSOR && s->U && d % 256 == 0) {
+  if (s->impl != DS_IMPL_SIMT && s->U && d % 256 == 0) {
     launch_standin_gather(s_prev, static_cast<const uint16_t*>(E), canvas, done, R, d, L, s->U,
                           st);
     cudaError_t e = launch_standin_tc(s->U, static_cast<const uint16_t*>(W), R, d, L, done,
@@ -277,7 +311,8 @@ ds_status ds_sampler_create(const ds_sampler_config* cfg, ds_sampler** out) {
   if (c.dtype != DS_DTYPE_BF16 && c.dtype != DS_DTYPE_FP32) return DS_ERR_INVALID_ARG;
   if (c.top_k < 0 || c.top_k > kMaxTopK) return DS_ERR_INVALID_ARG;
   if (c.max_steps < 1 || c.max_steps > (1 << 28)) return DS_ERR_INVALID_ARG;
-  if (c.impl != DS_IMPL_AUTO && c.impl != DS_IMPL_TENSOR && c.impl != DS_IMPL_SIMT)
+  if (c.impl != DS_IMPL_AUTO && c.impl != DS_IMPL_TENSOR && c.impl != DS_IMPL_SIMT &&
+      c.impl != DS_IMPL_FUSED)
     return DS_ERR_INVALID_ARG;
   if (c.lock_rule != DS_LOCK_THRESHOLD && c.lock_rule != DS_LOCK_ENTROPY_BUDGET)
     return DS_ERR_INVALID_ARG;
@@ -300,7 +335,7 @@ ds_status ds_sampler_create(const ds_sampler_config* cfg, ds_sampler** out) {
     s->impl = DS_IMPL_SIMT;
   } else {
     const bool tc_ok = c.dtype == DS_DTYPE_BF16 && tc_available();
-    if (c.impl == DS_IMPL_TENSOR && !tc_ok) {
+    if ((c.impl == DS_IMPL_TENSOR || c.impl == DS_IMPL_FUSED) && !tc_ok) {
       delete s;
       return DS_ERR_UNSUPPORTED;
     }
@@ -312,20 +347,46 @@ ds_status ds_sampler_create(const ds_sampler_config* cfg, ds_sampler** out) {
 
   const size_t Rm = (size_t)c.max_batch * c.canvas_len;
   const size_t V = (size_t)c.vocab, d = (size_t)c.d_model;
-  size_t opart = 0;
-  for (int b = 1; b <= c.max_batch; ++b)
-    opart = std::max(opart, (size_t)splits_for(s, b) * b * c.canvas_len * d);
+  if (c.impl == DS_IMPL_FUSED) {
+    if (c.top_k != 0 || vocab_pass_shape((int)Rm, c.vocab, c.d_model, s->num_sms, 0).grid == 0) {
+      delete s;
+      return DS_ERR_UNSUPPORTED;
+    }
+    s->fused = true;
+    s->impl = DS_IMPL_FUSED;
+    // producer / consumer split of the fused pass (a tuning knob; 0 = in proportion to work)
+    if (const char* env = getenv("DS_VP_PRODUCERS")) s->vp_producers = atoi(env);
+  }
+  size_t opart = 0, nref = 0;
+  for (int b = 1; b <= c.max_batch; ++b) {
+    const size_t Rb = (size_t)b * c.canvas_len;
+    if (s->fused) {
+      const VocabPassShape sh = vocab_pass_shape((int)Rb, c.vocab, c.d_model, s->num_sms, 0);
+      opart = std::max(opart, (size_t)sh.n_ranges * Rb * d);
+      nref = std::max(nref, (size_t)sh.n_ranges * Rb);
+    } else {
+      opart = std::max(opart, (size_t)splits_for(s, b) * Rb * d);
+    }
+  }
   e = cudaSuccess;
-  s->Y = carve<float>(s, Rm * V, &e);
+  if (s->fused) {
+    const VocabPassShape sh = vocab_pass_shape((int)Rm, c.vocab, c.d_model, s->num_sms, 0);
+    s->seg = carve<ChunkStat>(s, Rm * (V / kVpSegment), &e);
+    s->mseg_t = carve<float>(s, Rm * (V / kVpSegment), &e);
+    s->mref = carve<float>(s, nref, &e);
+    s->vp_sync = carve<uint32_t>(s, vocab_pass_sync_words(sh), &e);
+  } else {
+    s->Y = carve<float>(s, Rm * V, &e);
+  }
   s->Phi = carve<uint16_t>(s, Rm * V, &e);
   s->Plo = carve<uint16_t>(s, Rm * V, &e);
-  s->cs = carve<ChunkStat>(s, Rm * std::max<size_t>(n_chunks, V / kTcSegment), &e);
+  if (!s->fused) s->cs = carve<ChunkStat>(s, Rm * std::max<size_t>(n_chunks, V / kTcSegment), &e);
   s->rs = carve<RowStat>(s, Rm, &e);
   s->best = carve<Best>(s, Rm * n_chunks, &e);
   if (c.top_k > 0) s->cand = carve<Cand>(s, Rm * n_chunks * c.top_k, &e);
   s->Opart = carve<float>(s, opart, &e);
   s->Teff = carve<float>(s, (size_t)c.max_batch, &e);
-  if (s->impl == DS_IMPL_TENSOR && c.d_model % 256 == 0) s->U = carve<uint16_t>(s, Rm * 2 * d, &e);
+  if (s->impl != DS_IMPL_SIMT && c.d_model % 256 == 0) s->U = carve<uint16_t>(s, Rm * 2 * d, &e);
   s->opart_floats = opart;
   s->err = carve<uint32_t>(s, 4, &e);
   s->iter = carve<int32_t>(s, 4, &e);
@@ -603,10 +664,19 @@ ds_status ds_sampler_debug_buffer(ds_sampler* s, int32_t which, const void** ptr
   const size_t R = (size_t)std::max(1, s->last_batch) * s->cfg.canvas_len;
   const size_t V = (size_t)s->cfg.vocab;
   switch (which) {
-    case 0: *ptr = s->Y; *bytes = R * V * 4; return DS_OK;
+    case 0:
+      if (!s->Y) return DS_ERR_UNSUPPORTED;
+      *ptr = s->Y;
+      *bytes = R * V * 4;
+      return DS_OK;
     case 1: *ptr = s->rs; *bytes = R * sizeof(RowStat); return DS_OK;
     case 2: *ptr = s->Phi; *bytes = R * V * 2; return DS_OK;
     case 3: *ptr = s->Plo; *bytes = R * V * 2; return DS_OK;
+    case 4:
+      if (!s->seg) return DS_ERR_UNSUPPORTED;
+      *ptr = s->seg;
+      *bytes = R * (V / kVpSegment) * sizeof(ChunkStat);
+      return DS_OK;
   }
   return DS_ERR_INVALID_ARG;
 }

@@ -30,11 +30,11 @@ struct ChunkStat {  // per (row, vocabulary chunk): the same quantities over the
   int32_t arg;
 };
 
-struct Best {  // best Gumbel-perturbed logit of a chunk
-  float v;     // y + g
-  int32_t j;   // token (lowest on ties)
-  float y;     // y at that token
-  int32_t pad;
+struct Best {   // best Gumbel-perturbed candidate of a chunk
+  float v;      // its score (larger wins; comparable within a row)
+  int32_t j;    // token (lowest on ties)
+  float y;      // y at that token, or y - m (m the row maximum) when rel is 1
+  int32_t rel;
 };
 
 struct Cand {  // a top-k candidate
@@ -89,6 +89,21 @@ DS_DEV int32_t token_from_word(uint32_t r, uint32_t V) {
 DS_DEV u32x4 gumbel_block(uint32_t jblk, uint32_t i, uint32_t b, uint32_t step, uint64_t seed) {
   return philox4x32_10(u32x4{jblk, i, b, (step << 2) | kGumbelStream}, (uint32_t)seed,
                        (uint32_t)(seed >> 32));
+}
+
+// 2^x on the special-function unit (ex2.approx.ftz: results below 2^-126 flush to zero).
+DS_DEV float exp2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// (a, b) -> bf16x2 hi = RN(a, b) and lo = RN(a - hi_a, b - hi_b), packed (a in the low half).
+DS_DEV void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(a - __low2float(h), b - __high2float(h));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 // Better (v, j) pair: larger v, then lower j.
@@ -187,6 +202,13 @@ DS_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int3
       : "memory");
 }
 
+// Prefetch a tile of a tensor map into L2 (no shared-memory destination, no completion).
+DS_DEV void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // shared -> global bulk tensor store (tracked by bulk groups of the issuing thread)
 DS_DEV void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
@@ -202,6 +224,31 @@ DS_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "me
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy (TMA).
 DS_DEV void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+DS_DEV void st_shared_u4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+// global -> shared bulk copy (16-byte aligned, size a multiple of 16), counted on an mbarrier
+DS_DEV void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+// Order this thread's generic-proxy global accesses with its async-proxy (TMA) ones.
+DS_DEV void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+DS_DEV uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+DS_DEV void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 DS_DEV void st_shared_f4(uint32_t addr, float a, float b, float c, float d) {
   asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c),
@@ -270,6 +317,21 @@ DS_DEV void tmem_ld_16cols(uint32_t taddr, uint32_t (&r)[16]) {
       : "memory");
 }
 DS_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Store 32 consecutive fp32 columns of the warp's 32 TMEM lanes (lane = row).
+DS_DEV void tmem_st_32cols(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31, %32};" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+      "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
+      "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]),
+      "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]),
+      "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+}
+DS_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand (tcgen05 format):
 // start address >> 4 in bits 0-13, leading-dimension byte offset >> 4 in 16-29, stride-dimension

@@ -12,6 +12,8 @@ namespace ds {
 
 // Vocabulary chunk handled by one CTA of the row kernels (256 threads x 32 values).
 constexpr int kChunk = 8192;
+// Most partial sums of s that the finalize kernel combines.
+constexpr int kMaxSplits = 256;
 // Largest top-k the sampler supports, and the largest candidate pool its merge takes.
 constexpr int kMaxTopK = 256;
 constexpr int kMaxTopKPool = 8192;
@@ -37,7 +39,11 @@ void launch_finalize_with_s(const RowStat* rs, const Best* best, const Cand* can
                             int k, int R, int L, const uint8_t* done, const int32_t* step,
                             uint64_t seed, int32_t* sampled, float* conf, float* entropy,
                             int32_t* argmax, const float* Opart, int S, int d, float* s,
-                            cudaStream_t st);
+                            const float* mref, cudaStream_t st);
+// Gumbel-max sample per (row, chunk) from the fused pass's probabilities (Best records).
+void launch_gumbel_seg(const uint16_t* Phi, const uint16_t* Plo, const ChunkStat* seg,
+                       const RowStat* rs, int R, int64_t V, int L, const uint8_t* done,
+                       const int32_t* step, uint64_t seed, Best* best, cudaStream_t st);
 void launch_reduce_s(const float* Opart, int S, int R, int d, int L, const uint8_t* done,
                      const RowStat* rs, float* s, cudaStream_t st);
 void launch_lock(int B, int L, int64_t V, int max_steps, uint64_t seed, const float* tau,
@@ -75,6 +81,9 @@ bool tc_make_map_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_
                       uint32_t box_rows, uint32_t box_cols);
 bool tc_make_map_f32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                      uint32_t box_rows, uint32_t box_cols);
+// The same with a 64-byte swizzle (boxes of 32 bf16 columns).
+bool tc_make_map_bf16_sw64(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                           uint32_t box_rows, uint32_t box_cols);
 void tc_prepare_logits();
 void tc_prepare_selfcond();
 // Also writes the softmax statistics of every 128-token segment of every row:
@@ -96,5 +105,31 @@ cudaError_t launch_selfcond_tc(const uint16_t* Phi, const uint16_t* Plo, const u
                                uint32_t* err, cudaStream_t st);
 // Split count of the tensor-core self-conditioning GEMM for a shape.
 int selfcond_tc_splits(int R, int64_t V, int d, int num_sms);
+
+// ---- fused vocabulary pass (ds_tc_fused.cu) ----
+// One cooperative persistent kernel: logits, segment statistics and the bf16 hi/lo
+// probabilities (producer CTAs), and the self-conditioning partials per vocabulary range with
+// their reference maxima (consumer CTAs).
+constexpr int kVpSegment = 128;  // tokens per segment of SegStat
+struct VocabPassShape {
+  int n_rt, n_vt, n_dt;  // row tiles (128), vocabulary tiles (256), d tiles (256)
+  int kvt;               // vocabulary tiles per consumer range
+  int n_ranges;          // consumer ranges
+  int producers;         // CTAs that start as producers
+  int grid;              // CTAs (one per SM)
+};
+void tc_prepare_vocab_pass();
+// Shape of the pass for R rows (0 grid when the fused pass cannot run: d % 256 != 0 or the
+// kernel does not fit one CTA per SM). `producers` <= 0 picks the default split.
+VocabPassShape vocab_pass_shape(int R, int64_t V, int d, int num_sms, int producers);
+// Words of the control block (queue counters, ready flags); zeroed before every launch.
+size_t vocab_pass_sync_words(const VocabPassShape& sh);
+cudaError_t launch_vocab_pass_tc(const VocabPassShape& sh, const uint16_t* H, const uint16_t* E,
+                                 int R, int64_t V, int d, int L, const float* T,
+                                 const uint8_t* done, const int32_t* step, uint64_t seed,
+                                 uint16_t* Phi, uint16_t* Plo, ChunkStat* seg, float* mseg_t,
+                                 float* Opart, float* mref, uint32_t* sync, uint32_t* err,
+                                 cudaStream_t st);
+
 
 }  // namespace ds

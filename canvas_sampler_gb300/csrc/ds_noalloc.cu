@@ -67,7 +67,8 @@ extern "C" ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg,
   if (c.d_model < 64 || c.d_model > 16384 || c.d_model % 64) return DS_ERR_INVALID_ARG;
   if (c.dtype != DS_DTYPE_BF16 && c.dtype != DS_DTYPE_FP32) return DS_ERR_INVALID_ARG;
   if (c.top_k < 0 || c.top_k > kMaxTopK || c.max_steps < 1) return DS_ERR_INVALID_ARG;
-  if (c.impl != DS_IMPL_AUTO && c.impl != DS_IMPL_TENSOR && c.impl != DS_IMPL_SIMT)
+  if (c.impl != DS_IMPL_AUTO && c.impl != DS_IMPL_TENSOR && c.impl != DS_IMPL_SIMT &&
+      c.impl != DS_IMPL_FUSED)
     return DS_ERR_INVALID_ARG;
   if (c.lock_rule != DS_LOCK_THRESHOLD && c.lock_rule != DS_LOCK_ENTROPY_BUDGET)
     return DS_ERR_INVALID_ARG;
@@ -84,7 +85,7 @@ extern "C" ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg,
   bool tensor = false;
   if (c.impl != DS_IMPL_SIMT) {
     const bool ok = c.dtype == DS_DTYPE_BF16 && tc_available();
-    if (c.impl == DS_IMPL_TENSOR && !ok) return DS_ERR_UNSUPPORTED;
+    if ((c.impl == DS_IMPL_TENSOR || c.impl == DS_IMPL_FUSED) && !ok) return DS_ERR_UNSUPPORTED;
     tensor = ok;
   }
   int dev = 0, sms = 1;

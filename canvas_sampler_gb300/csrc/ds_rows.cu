@@ -255,23 +255,6 @@ __global__ void __launch_bounds__(kThreads) k_row_merge(const ChunkStat* __restr
   }
 }
 
-// 2^x on the special-function unit (ex2.approx.ftz: results below 2^-126 flush to zero).
-__device__ __forceinline__ float exp2_approx(float x) {
-  float r;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-  return r;
-}
-
-// (a, b) -> bf16x2 hi = RN(a, b) and lo = RN(a - hi_a, b - hi_b), packed (a in the low half).
-__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  const __nv_bfloat162 l =
-      __floats2bfloat162_rn(a - __low2float(h), b - __high2float(h));
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
-}
-
-
 // exp(y - m) as bf16 hi + lo (the A operand of the self-conditioning GEMM) and, when `gumbel`
 // is set, the chunk's Gumbel-max winner.
 //
@@ -365,6 +348,90 @@ __global__ void __launch_bounds__(kThreads, 4) k_convert(const float* __restrict
   }
 }
 
+// Gumbel-max over the fused pass's stored probabilities, one CTA per (row, 8192-token chunk):
+// the chunk's winner of the exponential race argmin_j E_j / p_j (the form of k_convert) with
+// p_j = (P_hi + P_lo)[j] exp(m_g - m), where m_g is the maximum of token j's 128-token segment
+// and m the row maximum. A segment whose maximum is more than kGumbelReach below m cannot hold
+// the winner and is skipped without reading its probabilities. The winner's y - m is returned as
+// ln p_j (p_j carries ~17 significant bits: hi + lo is exact in fp32), with Best::rel = 1.
+__global__ void __launch_bounds__(kThreads) k_gumbel_seg(
+    const uint16_t* __restrict__ Phi, const uint16_t* __restrict__ Plo,
+    const ChunkStat* __restrict__ seg, const RowStat* __restrict__ rs, int64_t V, int L,
+    const uint8_t* __restrict__ done, const int32_t* __restrict__ step, uint64_t seed,
+    Best* __restrict__ best, int n_chunks) {
+  constexpr int kSegTok = 128, kGroups8 = kChunk / 8 / kThreads;  // 4 groups of 8 per thread
+  __shared__ float sh_scale[kChunk / kSegTok];
+  __shared__ float shv[32], shy;
+  __shared__ int32_t shj[32];
+  const int c = blockIdx.x, r = blockIdx.y;
+  const int b = r / L, i = r % L;
+  if (done && done[b]) return;
+  const float m = rs[r].m;
+  const int64_t j0 = (int64_t)c * kChunk, j1 = min(V, j0 + kChunk);
+  const int nseg = (int)((j1 - j0) / kSegTok);
+  if ((int)threadIdx.x < nseg) {
+    const float mg = seg[(size_t)r * (V / kSegTok) + j0 / kSegTok + threadIdx.x].m;
+    sh_scale[threadIdx.x] = mg >= m - kGumbelReach ? expf(mg - m) : 0.f;
+  }
+  __syncthreads();
+  const uint32_t st = (uint32_t)step[b];
+  const uint16_t* ph = Phi + (size_t)r * V;
+  const uint16_t* pl = Plo + (size_t)r * V;
+  float kbest = INFINITY, bp = 1.f;
+  int32_t bj = INT_MAX;
+  uint4 h[kGroups8], lo[kGroups8];
+  float sc[kGroups8];
+#pragma unroll
+  for (int k = 0; k < kGroups8; ++k) {  // all loads first
+    const int g = threadIdx.x + kThreads * k;
+    const int64_t j = j0 + 8 * (int64_t)g;
+    sc[k] = j < j1 ? sh_scale[g >> 4] : 0.f;
+    if (sc[k] > 0.f) {
+      h[k] = __ldcs(reinterpret_cast<const uint4*>(ph + j));
+      lo[k] = __ldcs(reinterpret_cast<const uint4*>(pl + j));
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kGroups8; ++k) {
+    if (!(sc[k] > 0.f)) continue;
+    const int64_t j = j0 + 8 * (int64_t)(threadIdx.x + kThreads * k);
+    const uint32_t hw[4] = {h[k].x, h[k].y, h[k].z, h[k].w};
+    const uint32_t lw[4] = {lo[k].x, lo[k].y, lo[k].z, lo[k].w};
+    float p[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      p[2 * e] = (__uint_as_float(hw[e] << 16) + __uint_as_float(lw[e] << 16)) * sc[k];
+      p[2 * e + 1] =
+          (__uint_as_float(hw[e] & 0xFFFF0000u) + __uint_as_float(lw[e] & 0xFFFF0000u)) * sc[k];
+    }
+#pragma unroll
+    for (int g2 = 0; g2 < 2; ++g2) {
+      const float pm = fmaxf(fmaxf(p[4 * g2], p[4 * g2 + 1]), fmaxf(p[4 * g2 + 2], p[4 * g2 + 3]));
+      if (5.9604645e-8f >= kbest * pm) continue;
+      const int64_t jb = j + 4 * g2;
+      const u32x4 w = gumbel_block((uint32_t)(jb >> 2), (uint32_t)i, (uint32_t)b, st, seed);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float pe = p[4 * g2 + e];
+        if (!(pe > 0.f)) continue;
+        const uint32_t wd = word_of(w, e);
+        // 1 - u for u = (2q + 1) / 2^24, exact in fp32
+        const float omu = __uint2float_rn(0xFFFFFFu - 2u * (wd >> 9)) * 5.9604644775390625e-8f;
+        if (omu * (1.0f - 9.5367431640625e-7f) > kbest * pe) continue;
+        const float key = -logf(word_to_uniform(wd)) / pe;
+        if (key < kbest) {
+          kbest = key;
+          bj = (int32_t)(jb + e);
+          bp = pe;
+        }
+      }
+    }
+  }
+  float v = -kbest, y = logf(bp);
+  block_best(v, bj, y, shv, shj, &shy);
+  if (threadIdx.x == 0) best[(size_t)r * n_chunks + c] = Best{v, bj, y, 1};
+}
+
 // The k largest logits of a chunk (ties toward lower tokens), written in token order.
 // Element q of thread t is token j0 + t + 256 q, so the selection's (q, thread) order is
 // token order.
@@ -404,8 +471,9 @@ __global__ void __launch_bounds__(kThreads) k_finalize(
     int n_chunks, int k, int L, const uint8_t* __restrict__ done, const int32_t* __restrict__ step,
     uint64_t seed, int32_t* __restrict__ sampled, float* __restrict__ conf,
     float* __restrict__ entropy, int32_t* __restrict__ argmax, const float* __restrict__ Opart,
-    int S, int R, int d, float* __restrict__ s_out) {
+    int S, int R, int d, float* __restrict__ s_out, const float* __restrict__ mref) {
   __shared__ float shv[32], shy, shf[32];
+  __shared__ float sh_sc[kMaxSplits];
   __shared__ int32_t shj[32];
   __shared__ int hist[256];
   __shared__ int scan_sh[32];
@@ -416,17 +484,23 @@ __global__ void __launch_bounds__(kThreads) k_finalize(
   if (done && done[b]) return;
   const RowStat st = rs[r];
   if (Opart) {
+    // partial sp is relative to exp(mref[sp] - m) (1 for the unfused splits); summed in split
+    // order
+    for (int sp = threadIdx.x; sp < S; sp += kThreads)
+      sh_sc[sp] = mref ? expf(mref[(size_t)sp * R + r] - st.m) : 1.f;
+    __syncthreads();
     const int64_t plane = (int64_t)R * d;
     const float4* src = reinterpret_cast<const float4*>(Opart + (size_t)r * d);
     float4* dst = reinterpret_cast<float4*>(s_out + (size_t)r * d);
     for (int q = threadIdx.x; q < d / 4; q += kThreads) {
-      float4 acc = src[q];
-      for (int sp = 1; sp < S; ++sp) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int sp = 0; sp < S; ++sp) {
         const float4 t = src[sp * plane / 4 + q];
-        acc.x += t.x;
-        acc.y += t.y;
-        acc.z += t.z;
-        acc.w += t.w;
+        const float c = sh_sc[sp];
+        acc.x = fmaf(t.x, c, acc.x);
+        acc.y = fmaf(t.y, c, acc.y);
+        acc.z = fmaf(t.z, c, acc.z);
+        acc.w = fmaf(t.w, c, acc.w);
       }
       dst[q] = make_float4(acc.x / st.l, acc.y / st.l, acc.z / st.l, acc.w / st.l);
     }
@@ -435,16 +509,17 @@ __global__ void __launch_bounds__(kThreads) k_finalize(
   int32_t bj = INT_MAX;
   float cval;
   if (k == 0) {
+    // Best::y is y at the winner, or y - m where Best::rel is 1
     for (int q = threadIdx.x; q < n_chunks; q += kThreads) {
       const Best t = best[(size_t)r * n_chunks + q];
       if (better(t.v, t.j, bv, bj)) {
         bv = t.v;
         bj = t.j;
-        by = t.y;
+        by = t.rel ? t.y : t.y - st.m;
       }
     }
     block_best(bv, bj, by, shv, shj, &shy);
-    cval = expf(by - st.m) / st.l;
+    cval = expf(by) / st.l;
   } else {
     // The pool holds each chunk's candidates in token order, chunks in order, so pool order
     // is token order; element q of thread t is pool entry t + 256 q.
@@ -774,16 +849,24 @@ void launch_finalize(const RowStat* rs, const Best* best, const Cand* cand, int 
                      int32_t* sampled, float* conf, float* entropy, int32_t* argmax,
                      cudaStream_t st) {
   k_finalize<<<R, kThreads, 0, st>>>(rs, best, cand, n_chunks, k, L, done, step, seed, sampled,
-                                     conf, entropy, argmax, nullptr, 0, R, 0, nullptr);
+                                     conf, entropy, argmax, nullptr, 0, R, 0, nullptr, nullptr);
 }
 
 void launch_finalize_with_s(const RowStat* rs, const Best* best, const Cand* cand, int n_chunks,
                             int k, int R, int L, const uint8_t* done, const int32_t* step,
                             uint64_t seed, int32_t* sampled, float* conf, float* entropy,
                             int32_t* argmax, const float* Opart, int S, int d, float* s,
-                            cudaStream_t st) {
+                            const float* mref, cudaStream_t st) {
   k_finalize<<<R, kThreads, 0, st>>>(rs, best, cand, n_chunks, k, L, done, step, seed, sampled,
-                                     conf, entropy, argmax, Opart, S, R, d, s);
+                                     conf, entropy, argmax, Opart, S, R, d, s, mref);
+}
+
+void launch_gumbel_seg(const uint16_t* Phi, const uint16_t* Plo, const ChunkStat* seg,
+                       const RowStat* rs, int R, int64_t V, int L, const uint8_t* done,
+                       const int32_t* step, uint64_t seed, Best* best, cudaStream_t st) {
+  const int nc = n_chunks_of(V);
+  k_gumbel_seg<<<dim3(nc, R), kThreads, 0, st>>>(Phi, Plo, seg, rs, V, L, done, step, seed, best,
+                                                 nc);
 }
 
 void launch_reduce_s(const float* Opart, int S, int R, int d, int L, const uint8_t* done,

@@ -94,5 +94,22 @@ DS_DEV void tmem_accumulate(uint32_t taddr, float (&acc)[COLS]) {
   }
 }
 
+// acc[i] += scale * TMEM column i, for COLS columns starting at taddr (this warp's 32 lanes).
+template <int COLS>
+DS_DEV void tmem_accumulate_scaled(uint32_t taddr, float (&acc)[COLS], float scale) {
+#pragma unroll
+  for (int c = 0; c < COLS / 32; ++c) {
+    uint32_t r0[16], r1[16];
+    tmem_ld_16cols(taddr + (uint32_t)(c * 32), r0);
+    tmem_ld_16cols(taddr + (uint32_t)(c * 32 + 16), r1);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      acc[c * 32 + i] = fmaf(__uint_as_float(r0[i]), scale, acc[c * 32 + i]);
+      acc[c * 32 + 16 + i] = fmaf(__uint_as_float(r1[i]), scale, acc[c * 32 + 16 + i]);
+    }
+  }
+}
+
 }  // namespace tcpipe
 }  // namespace ds

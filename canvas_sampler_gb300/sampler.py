@@ -13,7 +13,8 @@ import torch
 from . import _lib as C
 
 _DTYPES = {"bf16": (C.DS_DTYPE_BF16, torch.bfloat16), "fp32": (C.DS_DTYPE_FP32, torch.float32)}
-_IMPLS = {"auto": C.DS_IMPL_AUTO, "tensor": C.DS_IMPL_TENSOR, "simt": C.DS_IMPL_SIMT}
+_IMPLS = {"auto": C.DS_IMPL_AUTO, "tensor": C.DS_IMPL_TENSOR, "simt": C.DS_IMPL_SIMT,
+          "fused": C.DS_IMPL_FUSED}
 _LOCK_RULES = {"threshold": C.DS_LOCK_THRESHOLD, "entropy_budget": C.DS_LOCK_ENTROPY_BUDGET}
 
 
@@ -101,7 +102,7 @@ class Sampler:
     def impl(self) -> str:
         v = c_int32()
         C.check(self.lib.ds_sampler_impl(self.handle, byref(v)), "ds_sampler_impl")
-        return {C.DS_IMPL_TENSOR: "tensor", C.DS_IMPL_SIMT: "simt"}[v.value]
+        return {C.DS_IMPL_TENSOR: "tensor", C.DS_IMPL_SIMT: "simt", C.DS_IMPL_FUSED: "fused"}[v.value]
 
     @property
     def workspace_bytes(self) -> int:

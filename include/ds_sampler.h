@@ -61,8 +61,11 @@ typedef enum ds_status {
 
 enum { DS_DTYPE_BF16 = 0, DS_DTYPE_FP32 = 1 };
 /* Kernel family: TENSOR = tcgen05/TMEM/TMA tensor-core kernels (bf16 inputs, d % 64 == 0);
- * SIMT = CUDA-core fp32 kernels (any supported dtype); AUTO = TENSOR where it applies. */
-enum { DS_IMPL_AUTO = 0, DS_IMPL_TENSOR = 1, DS_IMPL_SIMT = 2 };
+ * SIMT = CUDA-core fp32 kernels (any supported dtype); FUSED = the tensor-core step with the
+ * logits and self-conditioning GEMMs in one persistent cooperative kernel that never writes the
+ * logits (bf16 inputs, top_k == 0, d % 256 == 0; else DS_ERR_UNSUPPORTED; the no-allocation
+ * step runs it as TENSOR); AUTO = TENSOR where it applies, else SIMT. */
+enum { DS_IMPL_AUTO = 0, DS_IMPL_TENSOR = 1, DS_IMPL_SIMT = 2, DS_IMPL_FUSED = 3 };
 enum { DS_H_FIXED = 0, DS_H_STANDIN = 1 };
 /* Lock rule. THRESHOLD: lock unlocked positions with c >= tau (at least one per step, sticky),
  * re-noise the rest, done when all are locked. ENTROPY_BUDGET: the pages' default sampler --
@@ -186,7 +189,8 @@ ds_status ds_sampler_destroy(ds_sampler* sampler);
 /* Bytes of device workspace the sampler holds. */
 ds_status ds_sampler_workspace_bytes(const ds_sampler* sampler, size_t* bytes);
 
-/* The kernel family the sampler runs (DS_IMPL_TENSOR or DS_IMPL_SIMT after AUTO is resolved). */
+/* The kernel family the sampler runs (DS_IMPL_TENSOR, DS_IMPL_SIMT or DS_IMPL_FUSED; AUTO is
+ * resolved at creation). */
 ds_status ds_sampler_impl(const ds_sampler* sampler, int32_t* impl);
 
 /* Enqueue one sampler step on `stream` (see ds_step_args). 1 <= batch <= max_batch. */
@@ -260,8 +264,13 @@ ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg, const ds_step_ar
 ds_status ds_sampler_selftest_wait(ds_sampler* sampler, int64_t limit_ns, void* stream);
 
 /* Read-only view of an internal buffer of the last step, for tests and profiling.
- * which: 0 = scaled logits y [B*L, V] float; 1 = row statistics [B*L] x {m, l, entropy, argmax};
- * 2 = bf16 high part of exp(y - m) [B*L, V]; 3 = bf16 low part. *ptr is [device]. */
+ * which: 0 = scaled logits y [B*L, V] float (only where the step materialises them: top_k > 0
+ * or the CUDA-core path; else DS_ERR_UNSUPPORTED); 1 = row statistics [B*L] x {m, l, entropy,
+ * argmax}; 2 = bf16 high part of the probabilities [B*L, V]; 3 = bf16 low part (exp(y - m) with
+ * m the row maximum, or, in the fused tensor-core pass, exp(y - m_g) with m_g the maximum of the
+ * token's 128-token segment); 4 = the fused pass's segment records [B*L, V/128] x {m_g,
+ * sum exp(y - m_g), sum exp(y - m_g)(y - m_g), argmax_g} (16 bytes each; DS_ERR_UNSUPPORTED on
+ * the other paths). *ptr is [device]. */
 ds_status ds_sampler_debug_buffer(ds_sampler* sampler, int32_t which, const void** ptr,
                                   size_t* bytes);
 

@@ -111,10 +111,12 @@ def test_entropy_budget_loop_teacher_forced():
     assert state.done.all().item()
 
 
-def test_entropy_budget_graph_loop_equals_plain_launches():
+@pytest.mark.parametrize("impl", ["auto", "fused"])
+def test_entropy_budget_graph_loop_equals_plain_launches(impl):
+    # the fused pass is a cooperative launch: it must capture into the loop's graph too
     results = []
     for use_graph in (True, False):
-        w, inp, sampler, dev = _setup()
+        w, inp, sampler, dev = _setup(impl=impl)
         state = CanvasState.from_numpy(inp["canvas"], inp["lock"], inp["step"], inp["done"])
         out = StepOutputs.empty(w.B, w.L, w.d)
         sampler.loop(dev["E"], dev["T"], dev["tau"], state, inp["seed"], out, H=dev["H"],

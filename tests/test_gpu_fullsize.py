@@ -36,11 +36,12 @@ def _sample_positions(g, b, n):
     return sorted(pos)
 
 
+@pytest.mark.parametrize("impl", ["auto", "fused"])
 @pytest.mark.parametrize("name,per_seq", [("step_bf16_b1_v262144_d2816", 12),
                                           ("step_bf16_b8_v262144_d2816", 3)])
-def test_full_size_step(name, per_seq):
+def test_full_size_step(name, per_seq, impl):
     w = W.WORKLOADS[name]
-    case = GpuCase(w)
+    case = GpuCase(w, impl=impl)
     state = case.state()
     pre = state_np(state)
     out = case.run_step(state)

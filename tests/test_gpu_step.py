@@ -51,9 +51,11 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("impl", ["tensor", "simt"])
+@pytest.mark.parametrize("impl", ["tensor", "simt", "fused"])
 @pytest.mark.parametrize("name,base,B,V,d", CASES, ids=[c[0] for c in CASES])
 def test_step_parity(impl, name, base, B, V, d):
+    if impl == "fused" and d % 256:
+        pytest.skip("the fused pass takes d % 256 == 0")
     w = W.scaled(base, V=V, d=d, B=B)
     case = GpuCase(w, impl=impl)
     assert case.sampler.impl == impl
@@ -72,28 +74,72 @@ def test_topk_step_parity(k):
     assert rep["excluded"] <= max(2, rep["checked"] // 100)
 
 
-def test_tensor_core_logits_match_oracle():
-    w = W.scaled(BASE_PEAKED, V=8192, d=1024, B=1)
-    case = GpuCase(w, impl="tensor")
-    case.run_step(case.state())
-    y = case.sampler.debug_tensor(0).view(torch.float32).cpu().numpy().reshape(w.B * w.L, w.V)
+def _logits_ref(case, w):
     H64 = oracle.bf16_bits_to_f64(case.inp["H"]).reshape(-1, w.d)
     ref = (H64 @ case.E64.T) / float(case.inp["T"][0])
     # fp32 accumulation of exact bf16 products over d terms: at most one fp32 ulp (2^-23) of
     # the running sum per addition, whatever the rounding direction
     bound = w.d * 2.0 ** -23 * (np.abs(H64) @ np.abs(case.E64).T) + 1e-12
+    return ref, bound
+
+
+def test_tensor_core_logits_match_oracle():
+    # top-k path: the logits are materialised
+    from dataclasses import replace
+    w = replace(W.scaled(BASE_PEAKED, V=8192, d=1024, B=1), top_k=8)
+    case = GpuCase(w, impl="tensor")
+    case.run_step(case.state())
+    y = case.sampler.debug_tensor(0).view(torch.float32).cpu().numpy().reshape(w.B * w.L, w.V)
+    ref, bound = _logits_ref(case, w)
     assert np.all(np.abs(y - ref) <= bound)
 
 
-def test_simt_and_tensor_agree():
+def test_fused_pass_segments_and_probabilities_match_oracle():
+    """Fused pass: each 128-token segment's maximum is the segment maximum of the oracle's
+    logits within the fp32 accumulation bound, and P_hi + P_lo = exp(y - m_g) within that bound,
+    the exp approximation (4e-6) and the hi/lo split (2^-17), both relative."""
+    w = W.scaled(BASE_PEAKED, V=8192, d=1024, B=1)
+    case = GpuCase(w, impl="fused")
+    case.run_step(case.state())
+    R, nseg = w.B * w.L, w.V // 128
+    seg = case.sampler.debug_tensor(4).cpu().numpy().view(np.float32).reshape(R, nseg, 4)
+    m_g = seg[:, :, 0].astype(np.float64)
+    arg = seg[:, :, 3].view(np.int32)
+    ref, bound = _logits_ref(case, w)
+    ref_s, bound_s = ref.reshape(R, nseg, 128), bound.reshape(R, nseg, 128)
+    assert np.all(np.abs(m_g - ref_s.max(axis=2)) <= bound_s.max(axis=2))
+    # the argmax is a maximum of the oracle's logits within twice the bound
+    at = np.take_along_axis(ref, arg.astype(np.int64), axis=1)
+    assert np.all(at >= ref_s.max(axis=2) - 2 * bound_s.max(axis=2))
+    hi = oracle.bf16_bits_to_f64(case.sampler.debug_tensor(2).cpu().numpy().view(np.uint16))
+    lo = oracle.bf16_bits_to_f64(case.sampler.debug_tensor(3).cpu().numpy().view(np.uint16))
+    p = (hi + lo).reshape(R, nseg, 128)
+    p_ref = np.exp(ref_s - m_g[:, :, None])
+    err = np.abs(p - p_ref)
+    tol = p_ref * (np.expm1(bound_s + bound_s.max(axis=2, keepdims=True)) + 4e-6 + 2.0 ** -17)
+    big = p_ref > 1e-13  # y - m_g > -30, where the exp approximation keeps 4e-6
+    assert np.all(err[big] <= tol[big])
+
+
+@pytest.mark.parametrize("impl", ["tensor", "fused"])
+def test_simt_and_tensor_agree(impl):
     w = W.scaled(BASE_PEAKED, V=8192, d=256, B=1)
     inp = W.make_inputs(w)
-    a = GpuCase(w, impl="tensor", inputs=inp)
+    a = GpuCase(w, impl=impl, inputs=inp)
     b = GpuCase(w, impl="simt", inputs=inp)
     oa, ob = out_np(a.run_step(a.state())), out_np(b.run_step(b.state()))
     rel = np.linalg.norm(oa["s"] - ob["s"], axis=-1) / np.linalg.norm(ob["s"], axis=-1)
     assert rel.max() < 4e-5
     assert (oa["sampled"] == ob["sampled"]).mean() > 0.99
+
+
+def test_fused_rejects_what_it_cannot_run():
+    lib = C.load_library()
+    h = ctypes.c_void_p()
+    for top_k, d in ((8, 256), (0, 320)):
+        cfg = C.ds_sampler_config(max_batch=1, canvas_len=256, d_model=d, dtype=0, vocab=8192,
+                                  top_k=top_k, max_steps=48, impl=C.DS_IMPL_FUSED)
+        assert lib.ds_sampler_create(ctypes.byref(cfg), ctypes.byref(h)) == C.DS_ERR_UNSUPPORTED
 
 
 def test_done_sequences_are_untouched():
