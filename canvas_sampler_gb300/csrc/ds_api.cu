@@ -59,7 +59,7 @@ struct ds_sampler {
   uint16_t* U = nullptr;  // stand-in operand [B*L, 2d] (tensor-core path)
   float* Teff = nullptr;  // scheduled temperatures [B]
   ChunkStat* seg = nullptr;  // fused pass: segment statistics [B*L, V/128]
-  float* mseg_t = nullptr;   // fused pass: segment maxima [V/128, B*L]
+  float* mseg_t = nullptr;   // segment maxima [V/128, B*L] (fused) / tile maxima [V/256, B*L]
   float* mref = nullptr;     // fused pass: reference maxima of the range partials [Q, B*L]
   uint32_t* vp_sync = nullptr;
   uint32_t* err = nullptr;
@@ -162,14 +162,35 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
     launch_row_merge(s->seg, (int)(V / kVpSegment), R, L, a->done, s->rs, st);
     mark(s, 1, st);
     mark(s, 2, st);
-    launch_gumbel_seg(s->Phi, s->Plo, s->seg, s->rs, R, V, L, a->done, a->step, a->seed, s->best,
-                      st);
+    launch_gumbel_seg(s->Phi, s->Plo, s->seg, s->rs, R, V, L, a->done, a->step, a->seed, false,
+                      s->best, st);
     mark(s, 3, st);
     mark(s, 4, st);
     launch_finalize_with_s(s->rs, s->best, nullptr, s->n_chunks, 0, R, L, a->done, a->step,
                            a->seed, a->sampled, a->conf, a->entropy, a->argmax, s->Opart,
                            sh.n_ranges, d, a->s, s->mref, st);
     s->launches += 4;
+  } else if (s->impl != DS_IMPL_SIMT && k == 0) {
+    // the logits leave the GEMM as segment-relative probabilities; no y, no convert pass
+    cudaError_t e = launch_logits_p_tc(static_cast<const uint16_t*>(a->H),
+                                       static_cast<const uint16_t*>(a->E), R, V, d, L, T, a->done,
+                                       s->Phi, s->Plo, s->cs, s->mseg_t, s->err, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    mark(s, 0, st);
+    launch_row_merge(s->cs, (int)(V / kTcSegment), R, L, a->done, s->rs, st);
+    mark(s, 1, st);
+    mark(s, 2, st);
+    launch_gumbel_seg(s->Phi, s->Plo, s->cs, s->rs, R, V, L, a->done, a->step, a->seed, true,
+                      s->best, st);
+    mark(s, 3, st);
+    e = launch_selfcond_tc(s->Phi, s->Plo, static_cast<const uint16_t*>(a->E), R, V, d, L,
+                           a->done, S, s->Opart, s->mseg_t, s->mref, s->err, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    mark(s, 4, st);
+    launch_finalize_with_s(s->rs, s->best, nullptr, s->n_chunks, 0, R, L, a->done, a->step,
+                           a->seed, a->sampled, a->conf, a->entropy, a->argmax, s->Opart, S, d,
+                           a->s, s->mref, st);
+    s->launches += 5;
   } else if (s->impl != DS_IMPL_SIMT) {
     cudaError_t e = launch_logits_tc(static_cast<const uint16_t*>(a->H),
                                      static_cast<const uint16_t*>(a->E), R, V, d, L, T, a->done,
@@ -183,7 +204,7 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
     launch_chunk_stats(s->Y, R, V, L, a->done, s->cs, st);
     launch_row_merge(s->cs, s->n_chunks, R, L, a->done, s->rs, st);
   }
-  if (!s->fused) {
+  if (!s->fused && (s->impl == DS_IMPL_SIMT || k > 0)) {
     mark(s, 1, st);
     if (k > 0) launch_topk_chunk(s->Y, R, V, L, a->done, k, s->cand, st);
     mark(s, 2, st);
@@ -192,7 +213,8 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
     mark(s, 3, st);
     if (s->impl != DS_IMPL_SIMT) {
       cudaError_t e = launch_selfcond_tc(s->Phi, s->Plo, static_cast<const uint16_t*>(a->E), R,
-                                         V, d, L, a->done, S, s->Opart, s->err, st);
+                                         V, d, L, a->done, S, s->Opart, nullptr, nullptr, s->err,
+                                         st);
       if (e != cudaSuccess) return cuda_status(e);
     } else {
       launch_selfcond_simt(s->Phi, s->Plo, a->E, fp32, R, V, d, L, a->done, S, s->Opart, st);
@@ -369,12 +391,18 @@ ds_status ds_sampler_create(const ds_sampler_config* cfg, ds_sampler** out) {
     }
   }
   e = cudaSuccess;
+  // the tensor-core step without top-k never materialises y (segment-relative probabilities)
+  const bool seg_path = s->impl == DS_IMPL_TENSOR && c.top_k == 0;
   if (s->fused) {
     const VocabPassShape sh = vocab_pass_shape((int)Rm, c.vocab, c.d_model, s->num_sms, 0);
     s->seg = carve<ChunkStat>(s, Rm * (V / kVpSegment), &e);
     s->mseg_t = carve<float>(s, Rm * (V / kVpSegment), &e);
     s->mref = carve<float>(s, nref, &e);
     s->vp_sync = carve<uint32_t>(s, vocab_pass_sync_words(sh), &e);
+  } else if (seg_path) {
+    s->mseg_t = carve<float>(s, Rm * (V / 256), &e);  // tile maxima [V/256, R]
+    for (int b = 1; b <= c.max_batch; ++b) nref = std::max(nref, (size_t)splits_for(s, b) * b * c.canvas_len);
+    s->mref = carve<float>(s, nref, &e);
   } else {
     s->Y = carve<float>(s, Rm * V, &e);
   }
@@ -672,11 +700,14 @@ ds_status ds_sampler_debug_buffer(ds_sampler* s, int32_t which, const void** ptr
     case 1: *ptr = s->rs; *bytes = R * sizeof(RowStat); return DS_OK;
     case 2: *ptr = s->Phi; *bytes = R * V * 2; return DS_OK;
     case 3: *ptr = s->Plo; *bytes = R * V * 2; return DS_OK;
-    case 4:
-      if (!s->seg) return DS_ERR_UNSUPPORTED;
-      *ptr = s->seg;
+    case 4: {
+      // segment records exist on the paths that keep P relative to each segment's maximum
+      const ChunkStat* seg = s->seg ? s->seg : (s->mseg_t ? s->cs : nullptr);
+      if (!seg) return DS_ERR_UNSUPPORTED;
+      *ptr = seg;
       *bytes = R * (V / kVpSegment) * sizeof(ChunkStat);
       return DS_OK;
+    }
   }
   return DS_ERR_INVALID_ARG;
 }

@@ -65,6 +65,24 @@ DS_DEV u32x4 philox4x32_10(u32x4 c, uint32_t k0, uint32_t k1) {
   return c;
 }
 
+// N independent blocks under the same key, round by round, so their multiply chains overlap.
+template <int N>
+DS_DEV void philox4x32_10_n(u32x4 (&c)[N], uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+#pragma unroll
+    for (int q = 0; q < N; ++q) {
+      const uint32_t hi0 = __umulhi(0xD2511F53u, c[q].x), lo0 = 0xD2511F53u * c[q].x;
+      const uint32_t hi1 = __umulhi(0xCD9E8D57u, c[q].z), lo1 = 0xCD9E8D57u * c[q].z;
+      c[q] = u32x4{hi1 ^ c[q].y ^ k0, lo1, hi0 ^ c[q].w ^ k1, lo0};
+    }
+  }
+}
+
 DS_DEV uint32_t word_of(const u32x4& v, int k) {
   return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
 }
@@ -104,6 +122,68 @@ DS_DEV void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
   const __nv_bfloat162 l = __floats2bfloat162_rn(a - __low2float(h), b - __high2float(h));
   hi = *reinterpret_cast<const uint32_t*>(&h);
   lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// A token more than this below the row maximum cannot win the Gumbel-max: the largest Gumbel
+// draw is -ln(-ln(1 - 2^-24)) = 16.64, the smallest -ln(-ln 2^-24) = -2.81, and
+// 19.6 > 16.64 + 2.81 leaves margin for fp32 rounding.
+constexpr float kGumbelReach = 19.6f;
+
+// The Gumbel-max exponential race over 16 consecutive tokens j .. j + 15 of position i of
+// sequence b: with E_j = -ln u_j (u_j from the Gumbel stream of Philox) and p_j = exp(y_j - m)
+// (m the row maximum), argmax_j (y_j - ln E_j) = argmin_j E_j / p_j. p_j arrives as bf16 hi + lo
+// pairs (packed two tokens per word, the lower token in the low half), in two groups of eight with
+// scales sa, sb. 1 - u_j > kbest p_j proves E_j / p_j > kbest without the logarithm
+// (-ln u >= 1 - u); a group of four is skipped without its draw when even the smallest E
+// (> 2^-24) over its largest p cannot beat kbest, decided on kbest before any of the 16 tokens (a
+// larger kbest only skips less); the four draws are computed together. Tokens arrive in
+// increasing j, so a strict comparison keeps the lowest token on ties.
+DS_DEV void gumbel_race16(const uint4& hia, const uint4& loa, float sa, const uint4& hib,
+                          const uint4& lob, float sb, int64_t j, uint32_t i, uint32_t b,
+                          uint32_t step, uint64_t seed, float& kbest, int32_t& bj, float& bp) {
+  const uint32_t hw[8] = {hia.x, hia.y, hia.z, hia.w, hib.x, hib.y, hib.z, hib.w};
+  const uint32_t lw[8] = {loa.x, loa.y, loa.z, loa.w, lob.x, lob.y, lob.z, lob.w};
+  float p[16];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float sc = e < 4 ? sa : sb;
+    p[2 * e] = (__uint_as_float(hw[e] << 16) + __uint_as_float(lw[e] << 16)) * sc;
+    p[2 * e + 1] =
+        (__uint_as_float(hw[e] & 0xFFFF0000u) + __uint_as_float(lw[e] & 0xFFFF0000u)) * sc;
+  }
+  bool need[4];
+  bool any = false;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float pm = fmaxf(fmaxf(p[4 * q], p[4 * q + 1]), fmaxf(p[4 * q + 2], p[4 * q + 3]));
+    need[q] = !(5.9604645e-8f >= kbest * pm);
+    any |= need[q];
+  }
+  if (!any) return;
+  u32x4 w[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    w[q] = u32x4{(uint32_t)((j + 4 * q) >> 2), i, b, (step << 2) | kGumbelStream};
+  philox4x32_10_n<4>(w, (uint32_t)seed, (uint32_t)(seed >> 32));
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (!need[q]) continue;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float pe = p[4 * q + e];
+      if (!(pe > 0.f)) continue;
+      const uint32_t wd = word_of(w[q], e);
+      // 1 - u for u = (2q + 1) / 2^24, exact in fp32
+      const float omu = __uint2float_rn(0xFFFFFFu - 2u * (wd >> 9)) * 5.9604644775390625e-8f;
+      if (omu * (1.0f - 9.5367431640625e-7f) > kbest * pe) continue;
+      const float key = -logf(word_to_uniform(wd)) / pe;
+      if (key < kbest) {
+        kbest = key;
+        bj = (int32_t)(j + 4 * q + e);
+        bp = pe;
+      }
+    }
+  }
 }
 
 // Better (v, j) pair: larger v, then lower j.

@@ -40,10 +40,13 @@ void launch_finalize_with_s(const RowStat* rs, const Best* best, const Cand* can
                             uint64_t seed, int32_t* sampled, float* conf, float* entropy,
                             int32_t* argmax, const float* Opart, int S, int d, float* s,
                             const float* mref, cudaStream_t st);
-// Gumbel-max sample per (row, chunk) from the fused pass's probabilities (Best records).
+// Gumbel-max sample per (row, chunk) from probabilities stored relative to each 128-token
+// segment's maximum (tile_ref = false, the fused pass) or to the maximum over each 256-token
+// tile (tile_ref = true), with the segment statistics seg [R, V/128] (Best records).
 void launch_gumbel_seg(const uint16_t* Phi, const uint16_t* Plo, const ChunkStat* seg,
                        const RowStat* rs, int R, int64_t V, int L, const uint8_t* done,
-                       const int32_t* step, uint64_t seed, Best* best, cudaStream_t st);
+                       const int32_t* step, uint64_t seed, bool tile_ref, Best* best,
+                       cudaStream_t st);
 void launch_reduce_s(const float* Opart, int S, int R, int d, int L, const uint8_t* done,
                      const RowStat* rs, float* s, cudaStream_t st);
 void launch_lock(int B, int L, int64_t V, int max_steps, uint64_t seed, const float* tau,
@@ -92,6 +95,12 @@ constexpr int kTcSegment = 128;
 cudaError_t launch_logits_tc(const uint16_t* H, const uint16_t* E, int R, int64_t V, int d, int L,
                              const float* T, const uint8_t* done, float* Y, ChunkStat* seg_stats,
                              uint32_t* err, cudaStream_t st);
+// The same GEMM writing, instead of y, P = exp(y - m_t) as bf16 hi + lo (m_t the row's maximum
+// over the token's 256-token tile) and m_t tile-major in mtile_t [V/256, R].
+cudaError_t launch_logits_p_tc(const uint16_t* H, const uint16_t* E, int R, int64_t V, int d,
+                               int L, const float* T, const uint8_t* done, uint16_t* Phi,
+                               uint16_t* Plo, ChunkStat* seg_stats, float* mtile_t, uint32_t* err,
+                               cudaStream_t st);
 // H = bf16(tanh(U . W^T)) for U [R, 2d] bf16, W [d, 2d] bf16 (d % 256 == 0).
 cudaError_t launch_standin_tc(const uint16_t* U, const uint16_t* W, int R, int d, int L,
                               const uint8_t* done, uint16_t* H_out, uint32_t* err,
@@ -100,9 +109,12 @@ cudaError_t launch_standin_tc(const uint16_t* U, const uint16_t* W, int R, int d
 void launch_standin_gather(const float* s_prev, const uint16_t* E, const int32_t* canvas,
                            const uint8_t* done, int R, int d, int L, uint16_t* U,
                            cudaStream_t st);
+// With mtile_t set, P is relative to the row's maximum over each 256-token tile (mtile_t
+// [V/256, R]) and the reference maximum of each split's partial goes to mref [S, R] (see
+// ds_tc_selfcond.cu).
 cudaError_t launch_selfcond_tc(const uint16_t* Phi, const uint16_t* Plo, const uint16_t* E, int R,
                                int64_t V, int d, int L, const uint8_t* done, int S, float* Opart,
-                               uint32_t* err, cudaStream_t st);
+                               const float* mtile_t, float* mref, uint32_t* err, cudaStream_t st);
 // Split count of the tensor-core self-conditioning GEMM for a shape.
 int selfcond_tc_splits(int R, int64_t V, int d, int num_sms);
 

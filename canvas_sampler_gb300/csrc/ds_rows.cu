@@ -20,10 +20,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kPer = kChunk / kThreads;   // 32 values per thread
 constexpr int kGroups = kPer / 4;         // float4 groups per thread
-// An element more than this below the row maximum cannot win the Gumbel-max: the largest
-// Gumbel draw is -ln(-ln(1 - 2^-24)) = 16.64, the smallest -ln(-ln 2^-24) = -2.81, and
-// 19.6 > 16.64 + 2.81 leaves margin for fp32 rounding.
-constexpr float kGumbelReach = 19.6f;
 
 __device__ float block_sum(float v, float* sh) {
   v = warp_sum(v);
@@ -348,18 +344,21 @@ __global__ void __launch_bounds__(kThreads, 4) k_convert(const float* __restrict
   }
 }
 
-// Gumbel-max over the fused pass's stored probabilities, one CTA per (row, 8192-token chunk):
-// the chunk's winner of the exponential race argmin_j E_j / p_j (the form of k_convert) with
-// p_j = (P_hi + P_lo)[j] exp(m_g - m), where m_g is the maximum of token j's 128-token segment
-// and m the row maximum. A segment whose maximum is more than kGumbelReach below m cannot hold
-// the winner and is skipped without reading its probabilities. The winner's y - m is returned as
-// ln p_j (p_j carries ~17 significant bits: hi + lo is exact in fp32), with Best::rel = 1.
+// Gumbel-max over stored probabilities, one CTA per (row, 8192-token chunk): the chunk's winner
+// of the exponential race argmin_j E_j / p_j (the form of k_convert) with
+// p_j = (P_hi + P_lo)[j] exp(m_ref - m), where m_ref is the maximum the probabilities were taken
+// against (of token j's 128-token segment, or with tile_ref of its 256-token tile, i.e. of the
+// segment pair) and m the row maximum. A segment whose maximum is more than kGumbelReach below m
+// cannot hold the winner and is skipped without reading its probabilities. The winner's y - m is
+// returned as ln p_j (p_j carries ~17 significant bits: hi + lo is exact in fp32), with
+// Best::rel = 1.
 __global__ void __launch_bounds__(kThreads) k_gumbel_seg(
     const uint16_t* __restrict__ Phi, const uint16_t* __restrict__ Plo,
     const ChunkStat* __restrict__ seg, const RowStat* __restrict__ rs, int64_t V, int L,
     const uint8_t* __restrict__ done, const int32_t* __restrict__ step, uint64_t seed,
-    Best* __restrict__ best, int n_chunks) {
-  constexpr int kSegTok = 128, kGroups8 = kChunk / 8 / kThreads;  // 4 groups of 8 per thread
+    int tile_ref, Best* __restrict__ best, int n_chunks) {
+  // each thread: kGroups8 groups of 8 tokens, in pairs of adjacent groups (16 tokens)
+  constexpr int kSegTok = 128, kGroups8 = kChunk / 8 / kThreads;
   __shared__ float sh_scale[kChunk / kSegTok];
   __shared__ float shv[32], shy;
   __shared__ int32_t shj[32];
@@ -369,11 +368,19 @@ __global__ void __launch_bounds__(kThreads) k_gumbel_seg(
   const float m = rs[r].m;
   const int64_t j0 = (int64_t)c * kChunk, j1 = min(V, j0 + kChunk);
   const int nseg = (int)((j1 - j0) / kSegTok);
+  bool reach = false;
   if ((int)threadIdx.x < nseg) {
-    const float mg = seg[(size_t)r * (V / kSegTok) + j0 / kSegTok + threadIdx.x].m;
-    sh_scale[threadIdx.x] = mg >= m - kGumbelReach ? expf(mg - m) : 0.f;
+    const ChunkStat* sg = seg + (size_t)r * (V / kSegTok) + j0 / kSegTok;
+    const float mg = sg[threadIdx.x].m;
+    // chunks and tiles start at multiples of 256 tokens, so segment pairs (2u, 2u + 1) are tiles
+    const float mref = tile_ref ? fmaxf(mg, sg[threadIdx.x ^ 1].m) : mg;
+    reach = mg >= m - kGumbelReach;
+    sh_scale[threadIdx.x] = reach ? expf(mref - m) : 0.f;
   }
-  __syncthreads();
+  if (!__syncthreads_or(reach)) {  // no token of the chunk can win
+    if (threadIdx.x == 0) best[(size_t)r * n_chunks + c] = Best{-INFINITY, INT_MAX, 0.f, 1};
+    return;
+  }
   const uint32_t st = (uint32_t)step[b];
   const uint16_t* ph = Phi + (size_t)r * V;
   const uint16_t* pl = Plo + (size_t)r * V;
@@ -381,51 +388,27 @@ __global__ void __launch_bounds__(kThreads) k_gumbel_seg(
   int32_t bj = INT_MAX;
   uint4 h[kGroups8], lo[kGroups8];
   float sc[kGroups8];
+  // group k of thread t is group 2 t + (k & 1) + 2 kThreads (k >> 1) of the chunk, so a thread's
+  // pairs are 16 consecutive tokens and a warp covers 512 consecutive tokens
 #pragma unroll
   for (int k = 0; k < kGroups8; ++k) {  // all loads first
-    const int g = threadIdx.x + kThreads * k;
+    const int g = 2 * threadIdx.x + (k & 1) + 2 * kThreads * (k >> 1);
     const int64_t j = j0 + 8 * (int64_t)g;
     sc[k] = j < j1 ? sh_scale[g >> 4] : 0.f;
     if (sc[k] > 0.f) {
       h[k] = __ldcs(reinterpret_cast<const uint4*>(ph + j));
       lo[k] = __ldcs(reinterpret_cast<const uint4*>(pl + j));
+    } else {
+      h[k] = make_uint4(0u, 0u, 0u, 0u);
+      lo[k] = h[k];
     }
   }
 #pragma unroll
-  for (int k = 0; k < kGroups8; ++k) {
-    if (!(sc[k] > 0.f)) continue;
-    const int64_t j = j0 + 8 * (int64_t)(threadIdx.x + kThreads * k);
-    const uint32_t hw[4] = {h[k].x, h[k].y, h[k].z, h[k].w};
-    const uint32_t lw[4] = {lo[k].x, lo[k].y, lo[k].z, lo[k].w};
-    float p[8];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      p[2 * e] = (__uint_as_float(hw[e] << 16) + __uint_as_float(lw[e] << 16)) * sc[k];
-      p[2 * e + 1] =
-          (__uint_as_float(hw[e] & 0xFFFF0000u) + __uint_as_float(lw[e] & 0xFFFF0000u)) * sc[k];
-    }
-#pragma unroll
-    for (int g2 = 0; g2 < 2; ++g2) {
-      const float pm = fmaxf(fmaxf(p[4 * g2], p[4 * g2 + 1]), fmaxf(p[4 * g2 + 2], p[4 * g2 + 3]));
-      if (5.9604645e-8f >= kbest * pm) continue;
-      const int64_t jb = j + 4 * g2;
-      const u32x4 w = gumbel_block((uint32_t)(jb >> 2), (uint32_t)i, (uint32_t)b, st, seed);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float pe = p[4 * g2 + e];
-        if (!(pe > 0.f)) continue;
-        const uint32_t wd = word_of(w, e);
-        // 1 - u for u = (2q + 1) / 2^24, exact in fp32
-        const float omu = __uint2float_rn(0xFFFFFFu - 2u * (wd >> 9)) * 5.9604644775390625e-8f;
-        if (omu * (1.0f - 9.5367431640625e-7f) > kbest * pe) continue;
-        const float key = -logf(word_to_uniform(wd)) / pe;
-        if (key < kbest) {
-          kbest = key;
-          bj = (int32_t)(jb + e);
-          bp = pe;
-        }
-      }
-    }
+  for (int k = 0; k < kGroups8; k += 2) {
+    if (!(sc[k] > 0.f) && !(sc[k + 1] > 0.f)) continue;
+    const int64_t j = j0 + 8 * (int64_t)(2 * threadIdx.x + 2 * kThreads * (k >> 1));
+    gumbel_race16(h[k], lo[k], sc[k], h[k + 1], lo[k + 1], sc[k + 1], j, (uint32_t)i,
+                  (uint32_t)b, st, seed, kbest, bj, bp);
   }
   float v = -kbest, y = logf(bp);
   block_best(v, bj, y, shv, shj, &shy);
@@ -863,10 +846,11 @@ void launch_finalize_with_s(const RowStat* rs, const Best* best, const Cand* can
 
 void launch_gumbel_seg(const uint16_t* Phi, const uint16_t* Plo, const ChunkStat* seg,
                        const RowStat* rs, int R, int64_t V, int L, const uint8_t* done,
-                       const int32_t* step, uint64_t seed, Best* best, cudaStream_t st) {
+                       const int32_t* step, uint64_t seed, bool tile_ref, Best* best,
+                       cudaStream_t st) {
   const int nc = n_chunks_of(V);
-  k_gumbel_seg<<<dim3(nc, R), kThreads, 0, st>>>(Phi, Plo, seg, rs, V, L, done, step, seed, best,
-                                                 nc);
+  k_gumbel_seg<<<dim3(nc, R), kThreads, 0, st>>>(Phi, Plo, seg, rs, V, L, done, step, seed,
+                                                 tile_ref ? 1 : 0, best, nc);
 }
 
 void launch_reduce_s(const float* Opart, int S, int R, int d, int L, const uint8_t* done,

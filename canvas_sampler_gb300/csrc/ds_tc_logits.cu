@@ -1,7 +1,10 @@
 // Tensor-core logits of the sampler step on sm_103a, with the softmax statistics of every
 // 128-token segment of each row fused into the epilogue:
-//   Y[r, j] = (sum_k H[r, k] E[j, k]) / T_b        bf16 x bf16 -> fp32 (H [B*L, d], E [V, d])
-//   for each row and segment: max, lowest argmax, sum exp(y - max), sum exp(y - max)(y - max)
+//   y[r, j] = (sum_k H[r, k] E[j, k]) / T_b        bf16 x bf16 -> fp32 (H [B*L, d], E [V, d])
+//   for each row and segment g: max m_g, lowest argmax, sum exp(y - m_g), sum exp(y - m_g)(y - m_g)
+// and, by output mode, either y itself (kOutY, the top-k path) or the probabilities relative to
+// the row's maximum over the 256-token tile, P = exp(y - m_t) as bf16 hi + lo, with m_t stored
+// tile-major (kOutP: y never reaches memory).
 // Definitions: DiffusionGemma Technical Report, section 6 "Sampling" (softmax over the full
 // vocabulary in full precision). Pipeline structure: ds_tc_common.cuh.
 #include <algorithm>
@@ -27,16 +30,24 @@ constexpr uint32_t LG_STG_BYTES = 32 * 32 * 4;
 constexpr size_t LG_SMEM =
     (size_t)LG_STAGES * LG_STAGE_BYTES + (size_t)kEpiWarps * LG_STG_BYTES + 1024;
 
-// STANDIN: the same GEMM with A = U [R, 2d] (bf16(s_prev) | E[canvas]), B = W [d, 2d] and the
+// kStandin: the same GEMM with A = U [R, 2d] (bf16(s_prev) | E[canvas]), B = W [d, 2d] and the
 // epilogue H = bf16(tanh(acc)) instead of y and the statistics (V plays N = d, d plays K = 2d).
-template <bool STANDIN>
+enum { kOutY = 0, kOutP = 1, kStandin = 2 };
+
+template <int MODE>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     k_logits_tc(const __grid_constant__ CUtensorMap mapH, const __grid_constant__ CUtensorMap mapE,
-                const __grid_constant__ CUtensorMap mapY, int R, int64_t V, int d, int L, const float* __restrict__ T,
-                const uint8_t* __restrict__ done, float* __restrict__ Y,
-                ChunkStat* __restrict__ seg_stats, uint16_t* __restrict__ Hout, uint32_t* err) {
+                const __grid_constant__ CUtensorMap mapY, const __grid_constant__ CUtensorMap mapPlo,
+                int R, int64_t V, int d, int L, const float* __restrict__ T,
+                const uint8_t* __restrict__ done, ChunkStat* __restrict__ seg_stats,
+                float* __restrict__ mseg_t, uint16_t* __restrict__ Hout, uint32_t* err) {
+  constexpr bool STANDIN = MODE == kStandin;
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Ctl ctl;
+  // kOutP: the two column halves' segment maxima of each row, and a barrier of all epilogue
+  // warps (bounded), passed twice an item: after the maxima are written and after they are read
+  __shared__ float xmax[2][LG_BM];
+  __shared__ uint64_t xbar;
   uint8_t* smem = align1024(dyn_smem);
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -45,11 +56,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   const int n_tiles = n_rt * n_ct;
   const int nk = d / LG_BK;
   const int n_ch = (nk + LG_CHUNK_KB - 1) / LG_CHUNK_KB;
-  if (threadIdx.x == 0) ctl_init(ctl, LG_STAGES);
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&xbar), kEpiWarps);
+    ctl_init(ctl, LG_STAGES);  // ends with the mbarrier-init fence
+  }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&mapH);
     tma_prefetch_desc(&mapE);
     if (!STANDIN) tma_prefetch_desc(&mapY);
+    if (MODE == kOutP) tma_prefetch_desc(&mapPlo);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&ctl.tmem_base), 512);
@@ -137,7 +152,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     const int q = warp & 3;              // TMEM lane quadrant this warp may access
     const int half = (warp - 2) >> 2;    // column half of the tile
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    int cc = 0;
+    int cc = 0, items = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
       const int rt = tile % n_rt, ct = tile / n_rt;
@@ -175,9 +190,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         }
         continue;
       }
-      // y = z / T (as z * (1/T)); the segment's max, argmax (lowest token), sum of exp(y - m)
-      // and sum of exp(y - m) (y - m). x * invT is monotone in x for invT > 0, so the max of
-      // the scaled values is the scaled max, at the same lowest index.
+      // y = z / T (as z * (1/T), rounded once: no fused multiply-add with the subtraction, so
+      // y - m is exactly 0 at the maximum); the segment's max, argmax (lowest token), sum of
+      // exp(y - m) and sum of exp(y - m) (y - m). x * invT is monotone in x for invT > 0, so the
+      // max of the scaled values is the scaled max, at the same lowest index.
       const float invT = 1.0f / T[b];
       const int row0 = rt * LG_BM + q * 32;
       const int64_t j0 = (int64_t)ct * LG_BN + half * LG_COLS;
@@ -190,36 +206,88 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           arg = i;
         }
       }
-      const float m = zmax * invT;
+      const float m = __fmul_rn(zmax, invT);
+      // kOutP: P is relative to the maximum of the row over the whole 256-token tile (both
+      // column halves), so that one TMEM chunk of the self-conditioning GEMM covers a tile;
+      // the statistics stay relative to the segment's own maximum m
+      float ptile = 1.f;  // exp(m - m_tile)
+      float m_tile = m;
+      if constexpr (MODE == kOutP) {
+        xmax[half][q * 32 + lane] = m;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&xbar));
+        if (!mbar_wait(smem_u32(&xbar), (uint32_t)(items & 1), abort_flag, err)) {
+          ok = false;
+          break;
+        }
+        ++items;
+        m_tile = fmaxf(m, xmax[half ^ 1][q * 32 + lane]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&xbar));
+        if (!mbar_wait(smem_u32(&xbar), (uint32_t)(items & 1), abort_flag, err)) {
+          ok = false;
+          break;
+        }
+        ++items;
+        ptile = exp2_approx((m - m_tile) * 1.4426950408889634f);
+      }
       float l = 0.f, a = 0.f;
       const uint32_t stg = sbase + LG_STAGES * LG_STAGE_BYTES + (uint32_t)(warp - 2) * LG_STG_BYTES;
 #pragma unroll
       for (int bx = 0; bx < LG_COLS / 32; ++bx) {
         if (lane == 0) bulk_wait_read_all();  // the previous store has read the staging box
         __syncwarp();
+        if constexpr (MODE == kOutY) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          float y4[4];
+          for (int c = 0; c < 8; ++c) {
+            float y4[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            y4[e] = acc[bx * 32 + c * 4 + e] * invT;
-            const float t = y4[e] - m;
-            const float x = __expf(t);
-            l += x;
-            a = fmaf(x, t, a);
+            for (int e = 0; e < 4; ++e) {
+              y4[e] = __fmul_rn(acc[bx * 32 + c * 4 + e], invT);
+              const float t = y4[e] - m;
+              const float x = __expf(t);
+              l += x;
+              a = fmaf(x, t, a);
+            }
+            // row `lane` of the box, 16-byte chunk c at its 128-byte-swizzled position
+            st_shared_f4(stg + lane * 128 + ((c ^ (lane & 7)) << 4), y4[0], y4[1], y4[2], y4[3]);
           }
-          // row `lane` of the box, 16-byte chunk c at its 128-byte-swizzled position
-          st_shared_f4(stg + lane * 128 + ((c ^ (lane & 7)) << 4), y4[0], y4[1], y4[2], y4[3]);
+        } else {
+          // exp(y - m) = 2^((y - m) log2 e) (within ~3e-6 relative for y - m > -30; 1 at the
+          // maximum); P = exp(y - m) exp(m - m_tile) as bf16 hi = RN(P) and lo = RN(P - hi);
+          // one 32 x 32 box each for hi and lo, rows of 64 bytes in the 64-byte swizzle
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float p[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float t = __fmul_rn(acc[bx * 32 + c * 8 + e], invT) - m;
+              p[e] = exp2_approx(t * 1.4426950408889634f);
+              l += p[e];
+              a = fmaf(p[e], t, a);
+              p[e] *= ptile;
+            }
+            uint32_t h[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) split_bf16x2(p[2 * e], p[2 * e + 1], h[e], lo[e]);
+            const uint32_t off = lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4);
+            st_shared_u4(stg + off, h[0], h[1], h[2], h[3]);
+            st_shared_u4(stg + 2048 + off, lo[0], lo[1], lo[2], lo[3]);
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           tma_store_2d(&mapY, stg, (int32_t)(j0 + bx * 32), row0);
+          if constexpr (MODE == kOutP) tma_store_2d(&mapPlo, stg + 2048, (int32_t)(j0 + bx * 32), row0);
           bulk_commit();
         }
       }
-      seg_stats[(size_t)(row0 + lane) * (V / LG_COLS) + (j0 / LG_COLS)] =
+      const int seg = (int)(j0 / LG_COLS);
+      seg_stats[(size_t)(row0 + lane) * (V / LG_COLS) + seg] =
           ChunkStat{m, l, a, (int32_t)(j0 + arg)};
+      if constexpr (MODE == kOutP)
+        if (half == 0) mseg_t[(size_t)ct * R + row0 + lane] = m_tile;
     }
     if (!STANDIN && lane == 0) bulk_wait_all();
   }
@@ -234,9 +302,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 }  // namespace
 
 void tc_prepare_logits() {
-  cudaFuncSetAttribute(k_logits_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaFuncSetAttribute(k_logits_tc<kOutY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)LG_SMEM);
-  cudaFuncSetAttribute(k_logits_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaFuncSetAttribute(k_logits_tc<kOutP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)LG_SMEM);
+  cudaFuncSetAttribute(k_logits_tc<kStandin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)LG_SMEM);
 }
 
@@ -251,8 +321,26 @@ cudaError_t launch_logits_tc(const uint16_t* H, const uint16_t* E, int R, int64_
     return cudaErrorInvalidValue;
   const int n_tiles = (R / LG_BM) * (int)(V / LG_BN);
   const int grid = std::max(1, std::min(n_tiles, tc_num_sms()));
-  k_logits_tc<false><<<grid, kThreadsTC, LG_SMEM, st>>>(mH, mE, mY, R, V, d, L, T, done, Y,
-                                                         seg_stats, nullptr, err);
+  k_logits_tc<kOutY><<<grid, kThreadsTC, LG_SMEM, st>>>(mH, mE, mY, mY, R, V, d, L, T, done,
+                                                         seg_stats, nullptr, nullptr, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_logits_p_tc(const uint16_t* H, const uint16_t* E, int R, int64_t V, int d,
+                               int L, const float* T, const uint8_t* done, uint16_t* Phi,
+                               uint16_t* Plo, ChunkStat* seg_stats, float* mseg_t, uint32_t* err,
+                               cudaStream_t st) {
+  if (!tc_available()) return cudaErrorNotSupported;
+  CUtensorMap mH, mE, mPh, mPl;
+  if (!tc_make_map_bf16(&mH, H, (uint64_t)R, (uint64_t)d, LG_BM, LG_BK) ||
+      !tc_make_map_bf16(&mE, E, (uint64_t)V, (uint64_t)d, LG_BN, LG_BK) ||
+      !tc_make_map_bf16_sw64(&mPh, Phi, (uint64_t)R, (uint64_t)V, 32, 32) ||
+      !tc_make_map_bf16_sw64(&mPl, Plo, (uint64_t)R, (uint64_t)V, 32, 32))
+    return cudaErrorInvalidValue;
+  const int n_tiles = (R / LG_BM) * (int)(V / LG_BN);
+  const int grid = std::max(1, std::min(n_tiles, tc_num_sms()));
+  k_logits_tc<kOutP><<<grid, kThreadsTC, LG_SMEM, st>>>(mH, mE, mPh, mPl, R, V, d, L, T, done,
+                                                         seg_stats, mseg_t, nullptr, err);
   return cudaGetLastError();
 }
 
@@ -267,9 +355,9 @@ cudaError_t launch_standin_tc(const uint16_t* U, const uint16_t* W, int R, int d
     return cudaErrorInvalidValue;
   const int n_tiles = (R / LG_BM) * (d / LG_BN);
   const int grid = std::max(1, std::min(n_tiles, tc_num_sms()));
-  k_logits_tc<true><<<grid, kThreadsTC, LG_SMEM, st>>>(mU, mW, mU, R, (int64_t)d, 2 * d, L,
-                                                        nullptr, done, nullptr, nullptr, H_out,
-                                                        err);
+  k_logits_tc<kStandin><<<grid, kThreadsTC, LG_SMEM, st>>>(mU, mW, mU, mU, R, (int64_t)d, 2 * d,
+                                                            L, nullptr, done, nullptr, nullptr,
+                                                            H_out, err);
   return cudaGetLastError();
 }
 

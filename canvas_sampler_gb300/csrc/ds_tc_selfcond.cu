@@ -3,6 +3,10 @@
 // where P_hi + P_lo = exp(y - m) split into two bf16 terms, so the product keeps ~16
 // significant bits of the probabilities (a single bf16 keeps 8); the splits over the vocabulary
 // are summed and divided by the softmax normaliser afterwards.
+// SCALED: P is relative to the row's maximum m_t over each 256-token tile t (the logits kernel's
+// kOutP output); each tile is one TMEM chunk, promoted into registers scaled by exp(m_t - M_s)
+// with M_s the running maximum of the split (the registers are rescaled when it grows), and M_s
+// is stored beside the partial, O_s = sum_t exp(m_t - M_s) sum_{j in t} P_t[r, j] E[j, n].
 // Definitions: DiffusionGemma Technical Report, section 6 "Sampling" (the self-conditioning
 // embedding matmul, in full precision). Pipeline structure: ds_tc_common.cuh.
 #include <algorithm>
@@ -23,14 +27,17 @@ constexpr uint32_t SC_BOX_BYTES = 64 * SC_BK * 2;          // 64 d-columns x 64 
 constexpr uint32_t SC_STAGE_BYTES = 2 * SC_A_BYTES + (SC_BN_MAX / 64) * SC_BOX_BYTES;
 constexpr size_t SC_SMEM = (size_t)SC_STAGES * SC_STAGE_BYTES + 1024;
 
-template <int BN>
+template <int BN, bool SCALED>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     k_selfcond_tc(const __grid_constant__ CUtensorMap mapPhi,
                   const __grid_constant__ CUtensorMap mapPlo,
                   const __grid_constant__ CUtensorMap mapE, int R, int64_t V, int d, int L,
                   int S, int kb_per_split, const uint8_t* __restrict__ done,
-                  float* __restrict__ Opart, uint32_t* err) {
+                  float* __restrict__ Opart, const float* __restrict__ mtile_t,
+                  float* __restrict__ mref, uint32_t* err) {
   constexpr int COLS = BN / 2;
+  constexpr int CHUNK_KB = SC_CHUNK_KB;  // 4 K blocks = one 256-token tile
+  static_assert(CHUNK_KB * SC_BK == 256, "a chunk is one tile of the P reference maxima");
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Ctl ctl;
   uint8_t* smem = align1024(dyn_smem);
@@ -109,7 +116,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         int split, rt, dt, kb0, kb1;
         item_coords(w, split, rt, dt, kb0, kb1);
         if (done && done[(rt * SC_BM) / L]) continue;
-        for (int c0 = kb0; c0 < kb1 && ok; c0 += SC_CHUNK_KB, ++cc) {
+        for (int c0 = kb0; c0 < kb1 && ok; c0 += CHUNK_KB, ++cc) {
           const int buf = cc & 1;
           const uint32_t par = (uint32_t)((cc >> 1) & 1);
           if (!mbar_wait(smem_u32(&ctl.tempty[buf]), par ^ 1, abort_flag, err)) {
@@ -118,7 +125,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           }
           tc_fence_after();
           const uint32_t dtm = tmem + (uint32_t)(buf * BN);
-          const int c1 = min(kb1, c0 + SC_CHUNK_KB);
+          const int c1 = min(kb1, c0 + CHUNK_KB);
           for (int kb = c0; kb < c1; ++kb) {
             if (!mbar_wait(smem_u32(&ctl.full[stage]), phase, abort_flag, err)) {
               ok = false;
@@ -163,7 +170,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       float acc[COLS];
 #pragma unroll
       for (int i = 0; i < COLS; ++i) acc[i] = 0.f;
-      for (int c0 = kb0; c0 < kb1; c0 += SC_CHUNK_KB, ++cc) {
+      const int row = rt * SC_BM + q * 32 + lane;
+      float mrun = -INFINITY, mnext = 0.f;
+      if constexpr (SCALED) mnext = mtile_t[(size_t)(kb0 / CHUNK_KB) * R + row];
+      for (int c0 = kb0; c0 < kb1; c0 += CHUNK_KB, ++cc) {
+        float beta = 1.f;
+        if constexpr (SCALED) {
+          const float mg = mnext;
+          // the next tile's maximum is loaded while this chunk is waited for
+          if (c0 + CHUNK_KB < kb1) mnext = mtile_t[(size_t)(c0 / CHUNK_KB + 1) * R + row];
+          if (mg > mrun) {
+            const float alpha = expf(mrun - mg);
+#pragma unroll
+            for (int i = 0; i < COLS; ++i) acc[i] *= alpha;
+            mrun = mg;
+          }
+          beta = expf(mg - mrun);
+        }
         const int buf = cc & 1;
         const uint32_t par = (uint32_t)((cc >> 1) & 1);
         if (!mbar_wait(smem_u32(&ctl.tfull[buf]), par, abort_flag, err)) {
@@ -171,12 +194,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           break;
         }
         tc_fence_after();
-        tmem_accumulate<COLS>(tmem + (uint32_t)(buf * BN + half * COLS) + lane_base, acc);
+        if constexpr (SCALED)
+          tmem_accumulate_scaled<COLS>(tmem + (uint32_t)(buf * BN + half * COLS) + lane_base,
+                                       acc, beta);
+        else
+          tmem_accumulate<COLS>(tmem + (uint32_t)(buf * BN + half * COLS) + lane_base, acc);
         tc_fence_before();
         mbar_arrive(smem_u32(&ctl.tempty[buf]));
       }
       if (!ok) break;
-      const int row = rt * SC_BM + q * 32 + lane;
+      if constexpr (SCALED)
+        if (dt == 0 && half == 0) mref[(size_t)split * R + row] = mrun;
       float* orow = Opart + ((size_t)split * R + row) * d + (size_t)dt * BN + half * COLS;
 #pragma unroll
       for (int v = 0; v < COLS / 4; ++v)
@@ -197,11 +225,17 @@ int selfcond_bn(int d) { return d % 256 == 0 ? 256 : (d % 128 == 0 ? 128 : 64); 
 }  // namespace
 
 void tc_prepare_selfcond() {
-  cudaFuncSetAttribute(k_selfcond_tc<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaFuncSetAttribute(k_selfcond_tc<256, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)SC_SMEM);
-  cudaFuncSetAttribute(k_selfcond_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaFuncSetAttribute(k_selfcond_tc<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)SC_SMEM);
-  cudaFuncSetAttribute(k_selfcond_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaFuncSetAttribute(k_selfcond_tc<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)SC_SMEM);
+  cudaFuncSetAttribute(k_selfcond_tc<256, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)SC_SMEM);
+  cudaFuncSetAttribute(k_selfcond_tc<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)SC_SMEM);
+  cudaFuncSetAttribute(k_selfcond_tc<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)SC_SMEM);
 }
 
@@ -228,7 +262,8 @@ int selfcond_tc_splits(int R, int64_t V, int d, int num_sms) {
 
 cudaError_t launch_selfcond_tc(const uint16_t* Phi, const uint16_t* Plo, const uint16_t* E, int R,
                                int64_t V, int d, int L, const uint8_t* done, int S, float* Opart,
-                               uint32_t* err, cudaStream_t st) {
+                               const float* mtile_t, float* mref, uint32_t* err,
+                               cudaStream_t st) {
   if (!tc_available()) return cudaErrorNotSupported;
   const int bn = selfcond_bn(d);
   CUtensorMap mPh, mPl, mE;
@@ -237,18 +272,30 @@ cudaError_t launch_selfcond_tc(const uint16_t* Phi, const uint16_t* Plo, const u
       !tc_make_map_bf16(&mE, E, (uint64_t)V, (uint64_t)d, SC_BK, 64))
     return cudaErrorInvalidValue;
   const int nkb = (int)(V / SC_BK);
-  const int per = (nkb + S - 1) / S;
+  const bool scaled = mtile_t != nullptr;
+  int per = (nkb + S - 1) / S;
+  if (scaled) per = (per + SC_CHUNK_KB - 1) / SC_CHUNK_KB * SC_CHUNK_KB;  // splits start on a tile
   const int n_items = (R / SC_BM) * (d / bn) * S;
   const int grid = std::max(1, std::min(n_items, tc_num_sms()));
-  if (bn == 256)
-    k_selfcond_tc<256><<<grid, kThreadsTC, SC_SMEM, st>>>(mPh, mPl, mE, R, V, d, L, S, per, done,
-                                                          Opart, err);
-  else if (bn == 128)
-    k_selfcond_tc<128><<<grid, kThreadsTC, SC_SMEM, st>>>(mPh, mPl, mE, R, V, d, L, S, per, done,
-                                                          Opart, err);
-  else
-    k_selfcond_tc<64><<<grid, kThreadsTC, SC_SMEM, st>>>(mPh, mPl, mE, R, V, d, L, S, per, done,
-                                                         Opart, err);
+#define DS_SELFCOND_LAUNCH(BN, SC)                                                           \
+  k_selfcond_tc<BN, SC><<<grid, kThreadsTC, SC_SMEM, st>>>(mPh, mPl, mE, R, V, d, L, S, per, \
+                                                           done, Opart, mtile_t, mref, err)
+  if (scaled) {
+    if (bn == 256)
+      DS_SELFCOND_LAUNCH(256, true);
+    else if (bn == 128)
+      DS_SELFCOND_LAUNCH(128, true);
+    else
+      DS_SELFCOND_LAUNCH(64, true);
+  } else {
+    if (bn == 256)
+      DS_SELFCOND_LAUNCH(256, false);
+    else if (bn == 128)
+      DS_SELFCOND_LAUNCH(128, false);
+    else
+      DS_SELFCOND_LAUNCH(64, false);
+  }
+#undef DS_SELFCOND_LAUNCH
   return cudaGetLastError();
 }
 

@@ -267,10 +267,10 @@ ds_status ds_sampler_selftest_wait(ds_sampler* sampler, int64_t limit_ns, void* 
  * which: 0 = scaled logits y [B*L, V] float (only where the step materialises them: top_k > 0
  * or the CUDA-core path; else DS_ERR_UNSUPPORTED); 1 = row statistics [B*L] x {m, l, entropy,
  * argmax}; 2 = bf16 high part of the probabilities [B*L, V]; 3 = bf16 low part (exp(y - m) with
- * m the row maximum, or, in the fused tensor-core pass, exp(y - m_g) with m_g the maximum of the
- * token's 128-token segment); 4 = the fused pass's segment records [B*L, V/128] x {m_g,
- * sum exp(y - m_g), sum exp(y - m_g)(y - m_g), argmax_g} (16 bytes each; DS_ERR_UNSUPPORTED on
- * the other paths). *ptr is [device]. */
+ * m the row maximum where y is materialised; on the tensor-core paths without top-k,
+ * exp(y - m_g) with m_g the maximum of the token's 128-token segment); 4 = the segment records
+ * of those paths [B*L, V/128] x {m_g, sum exp(y - m_g), sum exp(y - m_g)(y - m_g), argmax_g}
+ * (16 bytes each; DS_ERR_UNSUPPORTED on the other paths). *ptr is [device]. */
 ds_status ds_sampler_debug_buffer(ds_sampler* sampler, int32_t which, const void** ptr,
                                   size_t* bytes);
 
