@@ -53,6 +53,11 @@ class ds_loop_args(ctypes.Structure):
                 ("use_graph", c_int32), ("reserved", c_int32), ("W", c_void_p), ("H_buf", c_void_p)]
 
 
+class ds_block_args(ctypes.Structure):
+    _fields_ = [("loop", ds_loop_args), ("n_blocks", c_int32), ("first_block", c_int32),
+                ("init_canvas", c_void_p), ("out_canvas", c_void_p), ("out_steps", c_void_p)]
+
+
 # name -> (restype, argtypes): every function declared in include/ds_sampler.h
 SIGNATURES = {
     "ds_abi_version": (c_int32, []),
@@ -65,6 +70,7 @@ SIGNATURES = {
     "ds_sampler_step": (c_int32, [c_void_p, POINTER(ds_step_args), c_void_p]),
     "ds_sampler_step_host": (c_int32, [c_void_p, POINTER(ds_step_args), c_void_p]),
     "ds_denoise_loop": (c_int32, [c_void_p, POINTER(ds_loop_args), c_void_p]),
+    "ds_block_loop": (c_int32, [c_void_p, POINTER(ds_block_args), c_void_p]),
     "ds_standin_hidden": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                     c_void_p, c_int32, c_void_p]),
     "ds_sampler_device_status": (c_int32, [c_void_p, POINTER(c_int32)]),

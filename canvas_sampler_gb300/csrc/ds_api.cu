@@ -36,6 +36,12 @@ struct LoopGraph {
   cudaGraphExec_t exec = nullptr;
 };
 
+struct BlockGraph {
+  ds_block_args key;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
 }  // namespace
 
 struct ds_sampler {
@@ -70,6 +76,10 @@ struct ds_sampler {
   size_t stage_bytes = 0;
   cudaStream_t capture_stream = nullptr;
   std::vector<LoopGraph> graphs;
+  std::vector<BlockGraph> block_graphs;
+  // block-autoregressive control words: [0] block index (0 outside ds_block_loop; every random
+  // draw's counter carries it), [1..3] the driver's action, committed block and iterations
+  int32_t* blk = nullptr;
   std::vector<void*> allocations;
   // phase timing (ds_sampler_set_phase_timing)
   bool timing = false;
@@ -162,12 +172,12 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
     launch_row_merge(s->seg, (int)(V / kVpSegment), R, L, a->done, s->rs, st);
     mark(s, 1, st);
     mark(s, 2, st);
-    launch_gumbel_seg(s->Phi, s->Plo, s->seg, s->rs, R, V, L, a->done, a->step, a->seed, false,
-                      s->best, st);
+    launch_gumbel_seg(s->Phi, s->Plo, s->seg, s->rs, R, V, L, a->done, a->step, a->seed, s->blk,
+                      false, s->best, st);
     mark(s, 3, st);
     mark(s, 4, st);
     launch_finalize_with_s(s->rs, s->best, nullptr, s->n_chunks, 0, R, L, a->done, a->step,
-                           a->seed, a->sampled, a->conf, a->entropy, a->argmax, s->Opart,
+                           a->seed, s->blk, a->sampled, a->conf, a->entropy, a->argmax, s->Opart,
                            sh.n_ranges, d, a->s, s->mref, st);
     s->launches += 4;
   } else if (s->impl != DS_IMPL_SIMT && k == 0) {
@@ -180,16 +190,16 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
     launch_row_merge(s->cs, (int)(V / kTcSegment), R, L, a->done, s->rs, st);
     mark(s, 1, st);
     mark(s, 2, st);
-    launch_gumbel_seg(s->Phi, s->Plo, s->cs, s->rs, R, V, L, a->done, a->step, a->seed, true,
-                      s->best, st);
+    launch_gumbel_seg(s->Phi, s->Plo, s->cs, s->rs, R, V, L, a->done, a->step, a->seed, s->blk,
+                      true, s->best, st);
     mark(s, 3, st);
     e = launch_selfcond_tc(s->Phi, s->Plo, static_cast<const uint16_t*>(a->E), R, V, d, L,
                            a->done, S, s->Opart, s->mseg_t, s->mref, s->err, st);
     if (e != cudaSuccess) return cuda_status(e);
     mark(s, 4, st);
     launch_finalize_with_s(s->rs, s->best, nullptr, s->n_chunks, 0, R, L, a->done, a->step,
-                           a->seed, a->sampled, a->conf, a->entropy, a->argmax, s->Opart, S, d,
-                           a->s, s->mref, st);
+                           a->seed, s->blk, a->sampled, a->conf, a->entropy, a->argmax, s->Opart,
+                           S, d, a->s, s->mref, st);
     s->launches += 5;
   } else if (s->impl != DS_IMPL_SIMT) {
     cudaError_t e = launch_logits_tc(static_cast<const uint16_t*>(a->H),
@@ -208,8 +218,8 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
     mark(s, 1, st);
     if (k > 0) launch_topk_chunk(s->Y, R, V, L, a->done, k, s->cand, st);
     mark(s, 2, st);
-    launch_convert(s->Y, s->rs, R, V, L, a->done, a->step, a->seed, k == 0, s->Phi, s->Plo,
-                   s->best, st);
+    launch_convert(s->Y, s->rs, R, V, L, a->done, a->step, a->seed, s->blk, k == 0, s->Phi,
+                   s->Plo, s->best, st);
     mark(s, 3, st);
     if (s->impl != DS_IMPL_SIMT) {
       cudaError_t e = launch_selfcond_tc(s->Phi, s->Plo, static_cast<const uint16_t*>(a->E), R,
@@ -221,18 +231,18 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
     }
     mark(s, 4, st);
     launch_finalize_with_s(s->rs, s->best, s->cand, s->n_chunks, k, R, L, a->done, a->step,
-                           a->seed, a->sampled, a->conf, a->entropy, a->argmax, s->Opart, S, d,
-                           a->s, nullptr, st);
+                           a->seed, s->blk, a->sampled, a->conf, a->entropy, a->argmax, s->Opart,
+                           S, d, a->s, nullptr, st);
     s->launches += (s->impl != DS_IMPL_SIMT ? 5 : 6) + (k > 0 ? 1 : 0);
   }
   mark(s, 5, st);
   if (s->cfg.lock_rule == DS_LOCK_ENTROPY_BUDGET)
-    launch_lock_entropy(B, L, V, s->cfg.max_steps, a->seed, s->cfg.entropy_budget,
+    launch_lock_entropy(B, L, V, s->cfg.max_steps, a->seed, s->blk, s->cfg.entropy_budget,
                         s->cfg.stop_entropy, a->sampled, a->entropy, a->argmax, a->prev_argmax,
                         a->step, a->canvas, a->lock, a->done, st);
   else
-    launch_lock(B, L, V, s->cfg.max_steps, a->seed, a->tau, a->sampled, a->conf, a->step,
-                a->canvas, a->lock, a->done, st);
+    launch_lock(B, L, V, s->cfg.max_steps, a->seed, s->blk, a->tau, a->sampled, a->conf,
+                a->step, a->canvas, a->lock, a->done, st);
   mark(s, 6, st);
   if (s->timing) {
     ++s->timed_steps;
@@ -291,6 +301,11 @@ void free_all(ds_sampler* s) {
     if (g.graph) cudaGraphDestroy(g.graph);
   }
   s->graphs.clear();
+  for (auto& g : s->block_graphs) {
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+    if (g.graph) cudaGraphDestroy(g.graph);
+  }
+  s->block_graphs.clear();
   for (cudaEvent_t e : s->events) cudaEventDestroy(e);
   s->events.clear();
   for (void* p : s->allocations) cudaFree(p);
@@ -418,7 +433,9 @@ ds_status ds_sampler_create(const ds_sampler_config* cfg, ds_sampler** out) {
   s->opart_floats = opart;
   s->err = carve<uint32_t>(s, 4, &e);
   s->iter = carve<int32_t>(s, 4, &e);
+  s->blk = carve<int32_t>(s, 4, &e);
   if (e == cudaSuccess) e = cudaMemset(s->err, 0, 4 * sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMemset(s->blk, 0, 4 * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s->capture_stream, cudaStreamNonBlocking);
   if (e != cudaSuccess) {
     free_all(s);
@@ -623,6 +640,121 @@ ds_status ds_denoise_loop(ds_sampler* s, const ds_loop_args* a, void* stream) {
     }
     s->graphs.push_back(ng);
     g = &s->graphs.back();
+  }
+  return cuda_status(cudaGraphLaunch(g->exec, st));
+}
+
+ds_status ds_block_loop(ds_sampler* s, const ds_block_args* a, void* stream) {
+  if (!s || !a) return DS_ERR_INVALID_ARG;
+  const ds_loop_args& lp = a->loop;
+  if (a->n_blocks < 1 || a->first_block < 0 || (int64_t)a->first_block + a->n_blocks > 65536)
+    return DS_ERR_INVALID_ARG;
+  if (!a->init_canvas || !a->out_canvas || !a->out_steps) return DS_ERR_INVALID_ARG;
+  if (lp.max_iters < 1 || lp.max_iters > s->cfg.max_steps) return DS_ERR_INVALID_ARG;
+  if (lp.h_mode != DS_H_FIXED && lp.h_mode != DS_H_STANDIN) return DS_ERR_INVALID_ARG;
+  ds_step_args sa = lp.step;
+  if (lp.h_mode == DS_H_STANDIN) {
+    if (!lp.W || !lp.H_buf || s->cfg.dtype != DS_DTYPE_BF16) return DS_ERR_INVALID_ARG;
+    sa.H = lp.H_buf;
+  }
+  ds_status r = check_step_args(s, &sa);
+  if (r != DS_OK) return r;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int B = sa.batch, L = s->cfg.canvas_len, d = s->cfg.d_model;
+  const int total = a->n_blocks * lp.max_iters;
+  const BlockState bs{sa.canvas, sa.lock, sa.step, sa.done, sa.prev_argmax, sa.s};
+  auto body = [&](cudaStream_t cs, bool use_cond, cudaGraphConditionalHandle h) -> ds_status {
+    ds_status rr = enqueue_iteration(s, &lp, cs);
+    if (rr != DS_OK) return rr;
+    launch_block_check(s->blk, sa.done, B, a->first_block, a->n_blocks, total, use_cond, h, cs);
+    launch_block_rollover(s->blk, a->init_canvas, a->out_canvas, a->out_steps, bs, B, L, d, cs);
+    s->launches += 2;
+    return cuda_status(cudaGetLastError());
+  };
+  auto finish = [&](cudaStream_t cs) {
+    // outside a block run every draw is block 0's
+    return cuda_status(cudaMemsetAsync(s->blk, 0, sizeof(int32_t), cs));
+  };
+  if (!lp.use_graph) {
+    launch_block_start(s->blk, a->first_block, a->init_canvas, bs, B, L, d, st);
+    s->launches += 1;
+    for (int it = 0; it < total; ++it) {
+      r = body(st, false, 0);
+      if (r != DS_OK) return r;
+    }
+    return finish(st);
+  }
+  const bool was_timing = s->timing;
+  s->timing = false;
+  struct Restore {
+    ds_sampler* s;
+    bool v;
+    ~Restore() { s->timing = v; }
+  } restore{s, was_timing};
+  BlockGraph* g = nullptr;
+  for (auto& e : s->block_graphs)
+    if (std::memcmp(&e.key, a, sizeof(ds_block_args)) == 0) g = &e;
+  if (!g) {
+    BlockGraph ng;
+    std::memcpy(&ng.key, a, sizeof(ds_block_args));
+    cudaError_t e = cudaGraphCreate(&ng.graph, 0);
+    cudaGraphConditionalHandle h = 0;
+    // the loop runs at least one step: the condition starts at 1 on every launch
+    if (e == cudaSuccess)
+      e = cudaGraphConditionalHandleCreate(&h, ng.graph, 1, cudaGraphCondAssignDefault);
+    cudaStream_t cs = s->capture_stream;
+    if (e == cudaSuccess)
+      e = cudaStreamBeginCaptureToGraph(cs, ng.graph, nullptr, nullptr, 0,
+                                        cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) {
+      launch_block_start(s->blk, a->first_block, a->init_canvas, bs, B, L, d, cs);
+      s->launches += 1;
+      cudaGraph_t outg = nullptr;
+      e = cudaStreamEndCapture(cs, &outg);
+    }
+    cudaGraphNode_t start_node = nullptr;
+    size_t n_nodes = 1;
+    if (e == cudaSuccess) e = cudaGraphGetNodes(ng.graph, &start_node, &n_nodes);
+    cudaGraphNodeParams cp{};
+    cudaGraphNode_t cond_node = nullptr;
+    if (e == cudaSuccess) {
+      cp.type = cudaGraphNodeTypeConditional;
+      cp.conditional.handle = h;
+      cp.conditional.type = cudaGraphCondTypeWhile;
+      cp.conditional.size = 1;
+      e = cudaGraphAddNode(&cond_node, ng.graph, &start_node, nullptr, 1, &cp);
+    }
+    if (e == cudaSuccess) {
+      cudaGraph_t bodyg = cp.conditional.phGraph_out[0];
+      e = cudaStreamBeginCaptureToGraph(cs, bodyg, nullptr, nullptr, 0,
+                                        cudaStreamCaptureModeThreadLocal);
+      if (e == cudaSuccess) {
+        ds_status rr = body(cs, true, h);
+        cudaGraph_t outb = nullptr;
+        cudaError_t e2 = cudaStreamEndCapture(cs, &outb);
+        e = (rr != DS_OK) ? cudaErrorUnknown : e2;
+      }
+    }
+    if (e == cudaSuccess) {
+      cudaGraphNode_t reset_node = nullptr;
+      cudaMemsetParams mp{};
+      mp.dst = s->blk;
+      mp.value = 0;
+      mp.elementSize = sizeof(int32_t);
+      mp.width = 1;
+      mp.height = 1;
+      e = cudaGraphAddMemsetNode(&reset_node, ng.graph, &cond_node, 1, &mp);
+    }
+    if (e == cudaSuccess) e = cudaGraphInstantiate(&ng.exec, ng.graph, 0);
+    if (e != cudaSuccess) {
+      if (ng.exec) cudaGraphExecDestroy(ng.exec);
+      if (ng.graph) cudaGraphDestroy(ng.graph);
+      t_last_cuda_error = e;
+      cudaGetLastError();
+      return DS_ERR_CUDA;
+    }
+    s->block_graphs.push_back(ng);
+    g = &s->block_graphs.back();
   }
   return cuda_status(cudaGraphLaunch(g->exec, st));
 }

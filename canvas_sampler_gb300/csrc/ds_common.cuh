@@ -103,6 +103,12 @@ DS_DEV int32_t token_from_word(uint32_t r, uint32_t V) {
   return (int32_t)(((uint64_t)r * (uint64_t)V) >> 32);
 }
 
+// Counter word 2 of a sequence's draws: b + 2^16 block, where blk points at the block index of a
+// block-autoregressive run (nullptr or 0 for a single canvas).
+DS_DEV uint32_t stream_id(uint32_t b, const int32_t* blk) {
+  return b + ((blk ? (uint32_t)*blk : 0u) << 16);
+}
+
 // The Gumbel counter of token block j>>2 at position i of sequence b.
 DS_DEV u32x4 gumbel_block(uint32_t jblk, uint32_t i, uint32_t b, uint32_t step, uint64_t seed) {
   return philox4x32_10(u32x4{jblk, i, b, (step << 2) | kGumbelStream}, (uint32_t)seed,

@@ -25,45 +25,69 @@ void launch_chunk_stats(const float* Y, int R, int64_t V, int L, const uint8_t* 
                         ChunkStat* cs, cudaStream_t st);
 void launch_row_merge(const ChunkStat* cs, int n_chunks, int R, int L, const uint8_t* done,
                       RowStat* rs, cudaStream_t st);
+// blk: the block index of a block-autoregressive run (device int32, or nullptr for 0); every
+// launcher that draws random numbers takes it (counter word 2 = sequence + 2^16 block).
 void launch_convert(const float* Y, const RowStat* rs, int R, int64_t V, int L,
-                    const uint8_t* done, const int32_t* step, uint64_t seed, bool gumbel,
-                    uint16_t* Phi, uint16_t* Plo, Best* best, cudaStream_t st);
+                    const uint8_t* done, const int32_t* step, uint64_t seed, const int32_t* blk,
+                    bool gumbel, uint16_t* Phi, uint16_t* Plo, Best* best, cudaStream_t st);
 void launch_topk_chunk(const float* Y, int R, int64_t V, int L, const uint8_t* done, int k,
                        Cand* cand, cudaStream_t st);
 void launch_finalize(const RowStat* rs, const Best* best, const Cand* cand, int n_chunks, int k,
                      int R, int L, const uint8_t* done, const int32_t* step, uint64_t seed,
-                     int32_t* sampled, float* conf, float* entropy, int32_t* argmax,
-                     cudaStream_t st);
+                     const int32_t* blk, int32_t* sampled, float* conf, float* entropy,
+                     int32_t* argmax, cudaStream_t st);
 // launch_finalize plus the reduction of s (launch_reduce_s) in the same per-row kernel.
 void launch_finalize_with_s(const RowStat* rs, const Best* best, const Cand* cand, int n_chunks,
                             int k, int R, int L, const uint8_t* done, const int32_t* step,
-                            uint64_t seed, int32_t* sampled, float* conf, float* entropy,
-                            int32_t* argmax, const float* Opart, int S, int d, float* s,
-                            const float* mref, cudaStream_t st);
+                            uint64_t seed, const int32_t* blk, int32_t* sampled, float* conf,
+                            float* entropy, int32_t* argmax, const float* Opart, int S, int d,
+                            float* s, const float* mref, cudaStream_t st);
 // Gumbel-max sample per (row, chunk) from probabilities stored relative to each 128-token
 // segment's maximum (tile_ref = false, the fused pass) or to the maximum over each 256-token
 // tile (tile_ref = true), with the segment statistics seg [R, V/128] (Best records).
 void launch_gumbel_seg(const uint16_t* Phi, const uint16_t* Plo, const ChunkStat* seg,
                        const RowStat* rs, int R, int64_t V, int L, const uint8_t* done,
-                       const int32_t* step, uint64_t seed, bool tile_ref, Best* best,
-                       cudaStream_t st);
+                       const int32_t* step, uint64_t seed, const int32_t* blk, bool tile_ref,
+                       Best* best, cudaStream_t st);
 void launch_reduce_s(const float* Opart, int S, int R, int d, int L, const uint8_t* done,
                      const RowStat* rs, float* s, cudaStream_t st);
-void launch_lock(int B, int L, int64_t V, int max_steps, uint64_t seed, const float* tau,
-                 const int32_t* sampled, const float* conf, int32_t* step, int32_t* canvas,
-                 uint8_t* lock, uint8_t* done, cudaStream_t st);
+void launch_lock(int B, int L, int64_t V, int max_steps, uint64_t seed, const int32_t* blk,
+                 const float* tau, const int32_t* sampled, const float* conf, int32_t* step,
+                 int32_t* canvas, uint8_t* lock, uint8_t* done, cudaStream_t st);
 void launch_temperature(const int32_t* step, int B, float t_start, float t_end, int max_steps,
                         float* T, cudaStream_t st);
-void launch_lock_entropy(int B, int L, int64_t V, int max_steps, uint64_t seed, float budget,
-                         float stop_entropy, const int32_t* sampled, const float* entropy,
-                         const int32_t* argmax, int32_t* prev_argmax, int32_t* step,
-                         int32_t* canvas, uint8_t* lock, uint8_t* done, cudaStream_t st);
+void launch_lock_entropy(int B, int L, int64_t V, int max_steps, uint64_t seed,
+                         const int32_t* blk, float budget, float stop_entropy,
+                         const int32_t* sampled, const float* entropy, const int32_t* argmax,
+                         int32_t* prev_argmax, int32_t* step, int32_t* canvas, uint8_t* lock,
+                         uint8_t* done, cudaStream_t st);
 void launch_wait_selftest(uint64_t limit_ns, uint32_t* err, cudaStream_t st);
 void launch_philox(const uint32_t* ctr, uint64_t seed, uint32_t* out, int64_t n, cudaStream_t st);
 void launch_loop_begin(const uint8_t* done, int B, int32_t* iter, int max_iters,
                        cudaGraphConditionalHandle h, cudaStream_t st);
 void launch_loop_end(const uint8_t* done, int B, int32_t* iter, int max_iters,
                      cudaGraphConditionalHandle h, cudaStream_t st);
+// Block-autoregressive driver (ds_block_loop). ctl[0] = block index (the blk word of the
+// kernels above), ctl[1] = action of the last check (0 continue, 1 commit and start the next
+// block, 2 commit, all blocks finished), ctl[2] = local index of the block to commit, ctl[3] =
+// iterations. start: block first_block, state from init_canvas[0]; check (one warp): decide and,
+// when use_cond, set the loop condition; rollover: commit and reset per the decision.
+struct BlockState {
+  int32_t* canvas;
+  uint8_t* lock;
+  int32_t* step;
+  uint8_t* done;
+  int32_t* prev_argmax;  // may be nullptr
+  float* s;
+};
+void launch_block_start(int32_t* ctl, int first_block, const int32_t* init_canvas, BlockState bs,
+                        int B, int L, int d, cudaStream_t st);
+void launch_block_check(int32_t* ctl, const uint8_t* done, int B, int first_block, int n_blocks,
+                        int max_iters, bool use_cond, cudaGraphConditionalHandle h,
+                        cudaStream_t st);
+void launch_block_rollover(const int32_t* ctl, const int32_t* init_canvas, int32_t* out_canvas,
+                           int32_t* out_steps, BlockState bs, int B, int L, int d,
+                           cudaStream_t st);
 
 // ---- CUDA-core GEMMs (ds_simt.cu) ----
 void launch_logits_simt(const void* H, const void* E, bool fp32_inputs, int R, int64_t V, int d,

@@ -150,7 +150,7 @@ extern "C" ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg,
     launch_row_merge(cs, nc, R, L, a->done, rs, s);
   }
   if (k > 0) launch_topk_chunk(Y, R, V, L, a->done, k, cand, s);
-  launch_convert(Y, rs, R, V, L, a->done, a->step, a->seed, k == 0, Phi, Plo, best, s);
+  launch_convert(Y, rs, R, V, L, a->done, a->step, a->seed, nullptr, k == 0, Phi, Plo, best, s);
   if (tensor) {
     if (launch_selfcond_tc(Phi, Plo, static_cast<const uint16_t*>(a->E), R, V, d, L, a->done, S,
                            Opart, nullptr, nullptr, err, s) != cudaSuccess)
@@ -159,14 +159,14 @@ extern "C" ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg,
     launch_selfcond_simt(Phi, Plo, a->E, fp32, R, V, d, L, a->done, S, Opart, s);
   }
   launch_reduce_s(Opart, S, R, d, L, a->done, rs, a->s, s);
-  launch_finalize(rs, best, cand, nc, k, R, L, a->done, a->step, a->seed, a->sampled, a->conf,
-                  a->entropy, a->argmax, s);
+  launch_finalize(rs, best, cand, nc, k, R, L, a->done, a->step, a->seed, nullptr, a->sampled,
+                  a->conf, a->entropy, a->argmax, s);
   if (c.lock_rule == DS_LOCK_ENTROPY_BUDGET)
-    launch_lock_entropy(B, L, V, c.max_steps, a->seed, c.entropy_budget, c.stop_entropy,
+    launch_lock_entropy(B, L, V, c.max_steps, a->seed, nullptr, c.entropy_budget, c.stop_entropy,
                         a->sampled, a->entropy, a->argmax, a->prev_argmax, a->step, a->canvas,
                         a->lock, a->done, s);
   else
-    launch_lock(B, L, V, c.max_steps, a->seed, a->tau, a->sampled, a->conf, a->step, a->canvas,
-                a->lock, a->done, s);
+    launch_lock(B, L, V, c.max_steps, a->seed, nullptr, a->tau, a->sampled, a->conf, a->step,
+                a->canvas, a->lock, a->done, s);
   return cudaGetLastError() == cudaSuccess ? DS_OK : DS_ERR_CUDA;
 }

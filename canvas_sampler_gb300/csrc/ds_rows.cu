@@ -267,14 +267,15 @@ __global__ void __launch_bounds__(kThreads, 4) k_convert(const float* __restrict
                                                       const RowStat* __restrict__ rs, int64_t V,
                                                       int L, const uint8_t* __restrict__ done,
                                                       const int32_t* __restrict__ step,
-                                                      uint64_t seed, int gumbel,
-                                                      uint16_t* __restrict__ Phi,
+                                                      uint64_t seed, const int32_t* blk,
+                                                      int gumbel, uint16_t* __restrict__ Phi,
                                                       uint16_t* __restrict__ Plo,
                                                       Best* __restrict__ best, int n_chunks) {
   __shared__ float shv[32], shy;
   __shared__ int32_t shj[32];
   const int c = blockIdx.x, r = blockIdx.y;
   const int b = r / L, i = r % L;
+  const uint32_t sid = stream_id((uint32_t)b, blk);
   if (done && done[b]) return;
   const float m = rs[r].m;
   const uint32_t st = gumbel ? (uint32_t)step[b] : 0u;
@@ -320,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_convert(const float* __restrict
     const float pmax = fmaxf(fmaxf(p[0], p[1]), fmaxf(p[2], p[3]));
     const float ymax = fmaxf(fmaxf(yy[0], yy[1]), fmaxf(yy[2], yy[3]));
     if (ymax < floor_y || !(pmax > 0.f) || 5.9604645e-8f >= kbest * pmax) continue;
-    const u32x4 w = gumbel_block((uint32_t)(j >> 2), (uint32_t)i, (uint32_t)b, st, seed);
+    const u32x4 w = gumbel_block((uint32_t)(j >> 2), (uint32_t)i, sid, st, seed);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       if (!(p[e] > 0.f)) continue;
@@ -356,7 +357,7 @@ __global__ void __launch_bounds__(kThreads) k_gumbel_seg(
     const uint16_t* __restrict__ Phi, const uint16_t* __restrict__ Plo,
     const ChunkStat* __restrict__ seg, const RowStat* __restrict__ rs, int64_t V, int L,
     const uint8_t* __restrict__ done, const int32_t* __restrict__ step, uint64_t seed,
-    int tile_ref, Best* __restrict__ best, int n_chunks) {
+    const int32_t* blk, int tile_ref, Best* __restrict__ best, int n_chunks) {
   // each thread: kGroups8 groups of 8 tokens, in pairs of adjacent groups (16 tokens)
   constexpr int kSegTok = 128, kGroups8 = kChunk / 8 / kThreads;
   __shared__ float sh_scale[kChunk / kSegTok];
@@ -408,7 +409,7 @@ __global__ void __launch_bounds__(kThreads) k_gumbel_seg(
     if (!(sc[k] > 0.f) && !(sc[k + 1] > 0.f)) continue;
     const int64_t j = j0 + 8 * (int64_t)(2 * threadIdx.x + 2 * kThreads * (k >> 1));
     gumbel_race16(h[k], lo[k], sc[k], h[k + 1], lo[k + 1], sc[k + 1], j, (uint32_t)i,
-                  (uint32_t)b, st, seed, kbest, bj, bp);
+                  stream_id((uint32_t)b, blk), st, seed, kbest, bj, bp);
   }
   float v = -kbest, y = logf(bp);
   block_best(v, bj, y, shv, shj, &shy);
@@ -452,7 +453,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_chunk(const float* __restrict
 __global__ void __launch_bounds__(kThreads) k_finalize(
     const RowStat* __restrict__ rs, const Best* __restrict__ best, const Cand* __restrict__ cand,
     int n_chunks, int k, int L, const uint8_t* __restrict__ done, const int32_t* __restrict__ step,
-    uint64_t seed, int32_t* __restrict__ sampled, float* __restrict__ conf,
+    uint64_t seed, const int32_t* blk, int32_t* __restrict__ sampled, float* __restrict__ conf,
     float* __restrict__ entropy, int32_t* __restrict__ argmax, const float* __restrict__ Opart,
     int S, int R, int d, float* __restrict__ s_out, const float* __restrict__ mref) {
   __shared__ float shv[32], shy, shf[32];
@@ -534,7 +535,7 @@ __global__ void __launch_bounds__(kThreads) k_finalize(
       const int32_t j = sel_j[t];
       if (j == INT_MAX) continue;
       const float yy = sel_y[t];
-      const u32x4 w = gumbel_block((uint32_t)(j >> 2), (uint32_t)i, (uint32_t)b,
+      const u32x4 w = gumbel_block((uint32_t)(j >> 2), (uint32_t)i, stream_id((uint32_t)b, blk),
                                    (uint32_t)step[b], seed);
       const float v = yy + gumbel_from_word(word_of(w, j & 3));
       if (better(v, j, bv, bj)) {
@@ -583,7 +584,7 @@ __global__ void k_reduce_s(const float* __restrict__ Opart, int S, int R, int d,
 }
 
 // Lock / re-noise / stop for one sequence per CTA (blockDim = L).
-__global__ void k_lock(int L, uint32_t V, int max_steps, uint64_t seed,
+__global__ void k_lock(int L, uint32_t V, int max_steps, uint64_t seed, const int32_t* blk,
                        const float* __restrict__ tau, const int32_t* __restrict__ sampled,
                        const float* __restrict__ conf, int32_t* __restrict__ step,
                        int32_t* __restrict__ canvas, uint8_t* __restrict__ lock,
@@ -625,7 +626,7 @@ __global__ void k_lock(int L, uint32_t V, int max_steps, uint64_t seed,
     canvas[at] = sampled[at];
     lock[at] = 1;
   } else if (!locked) {
-    const u32x4 w = philox4x32_10(u32x4{(uint32_t)(i >> 2), 0u, (uint32_t)b,
+    const u32x4 w = philox4x32_10(u32x4{(uint32_t)(i >> 2), 0u, stream_id((uint32_t)b, blk),
                                         ((uint32_t)st << 2) | kRenoiseStream},
                                   (uint32_t)seed, (uint32_t)(seed >> 32));
     canvas[at] = token_from_word(word_of(w, i & 3), V);
@@ -687,7 +688,8 @@ __global__ void k_temperature(const int32_t* __restrict__ step, int B, float t_s
 // (rounding) count as zero. Sort: bitonic over the next power of two; the running sum is a
 // Hillis-Steele scan in a fixed order, so the result is deterministic.
 __global__ void __launch_bounds__(1024) k_lock_entropy(
-    int L, uint32_t V, int max_steps, uint64_t seed, float budget, float stop_entropy,
+    int L, uint32_t V, int max_steps, uint64_t seed, const int32_t* blk, float budget,
+    float stop_entropy,
     const int32_t* __restrict__ sampled, const float* __restrict__ entropy,
     const int32_t* __restrict__ argmax, int32_t* __restrict__ prev_argmax,
     int32_t* __restrict__ step, int32_t* __restrict__ canvas, uint8_t* __restrict__ lock,
@@ -756,7 +758,7 @@ __global__ void __launch_bounds__(1024) k_lock_entropy(
   if (accepted) {
     canvas[at] = sampled[at];
   } else {
-    const u32x4 w = philox4x32_10(u32x4{(uint32_t)(i >> 2), 0u, (uint32_t)b,
+    const u32x4 w = philox4x32_10(u32x4{(uint32_t)(i >> 2), 0u, stream_id((uint32_t)b, blk),
                                         ((uint32_t)st << 2) | kRenoiseStream},
                                   (uint32_t)seed, (uint32_t)(seed >> 32));
     canvas[at] = token_from_word(word_of(w, i & 3), V);
@@ -784,17 +786,119 @@ __global__ void k_wait_selftest(uint64_t limit_ns, uint32_t* err) {
 
 }  // namespace
 
+// ---- block-autoregressive driver (see launch_block_start / check / rollover) ----
+
+// Block first_block from init_canvas[0] with fresh state: no locks, step 0, not done, no
+// previous argmax, s = 0 (the stand-in's s_prev of the first step).
+__global__ void k_block_start(int32_t* ctl, int first_block, const int32_t* __restrict__ init0,
+                              BlockState bs, int B, int L, int d) {
+  const int64_t BL = (int64_t)B * L, n = BL * d;
+  for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < n;
+       q += (int64_t)gridDim.x * blockDim.x) {
+    if (q < BL) {
+      bs.canvas[q] = init0[q];
+      bs.lock[q] = 0;
+      if (bs.prev_argmax) bs.prev_argmax[q] = -1;
+    }
+    if (q < B) {
+      bs.step[q] = 0;
+      bs.done[q] = 0;
+    }
+    bs.s[q] = 0.f;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    ctl[0] = first_block;
+    ctl[1] = 0;
+    ctl[2] = 0;
+    ctl[3] = 0;
+  }
+}
+
+// After every step of the run (one warp): when no sequence of the current block is open, the
+// block is to be committed (ctl[2] = its local index) and, if blocks remain, the block index
+// advances so that the next step already draws for the next block; ctl[1] records the action.
+__global__ void k_block_check(int32_t* ctl, const uint8_t* __restrict__ done, int B,
+                              int first_block, int n_blocks, int max_iters, int use_cond,
+                              cudaGraphConditionalHandle h) {
+  int open = 0;
+  for (int b = threadIdx.x; b < B; b += 32) open |= (done[b] == 0);
+  open = __any_sync(0xffffffffu, open);
+  if (threadIdx.x == 0) {
+    const int blk = ctl[0];
+    int action = 0;
+    if (!open) {
+      action = blk + 1 < first_block + n_blocks ? 1 : 2;
+      ctl[2] = blk - first_block;
+      if (action == 1) ctl[0] = blk + 1;
+    }
+    ctl[1] = action;
+    const int it = ctl[3] + 1;
+    ctl[3] = it;
+    if (use_cond) cudaGraphSetConditional(h, (action != 2 && it < max_iters) ? 1u : 0u);
+  }
+}
+
+// Commit the finished block (tokens and step counts) and, for action 1, load the next block's
+// initial canvas with fresh state. Each element is read and written by one thread only.
+__global__ void k_block_rollover(const int32_t* __restrict__ ctl,
+                                 const int32_t* __restrict__ init_canvas,
+                                 int32_t* __restrict__ out_canvas, int32_t* __restrict__ out_steps,
+                                 BlockState bs, int B, int L, int d) {
+  const int action = ctl[1];
+  if (action == 0) return;
+  const int64_t k = ctl[2];
+  const int64_t BL = (int64_t)B * L, n = action == 1 ? BL * d : BL;
+  for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < n;
+       q += (int64_t)gridDim.x * blockDim.x) {
+    if (q < BL) {
+      out_canvas[k * BL + q] = bs.canvas[q];
+      if (action == 1) {
+        bs.canvas[q] = init_canvas[(k + 1) * BL + q];
+        bs.lock[q] = 0;
+        if (bs.prev_argmax) bs.prev_argmax[q] = -1;
+      }
+    }
+    if (q < B) {
+      out_steps[k * B + q] = bs.step[q];
+      if (action == 1) {
+        bs.step[q] = 0;
+        bs.done[q] = 0;
+      }
+    }
+    if (action == 1) bs.s[q] = 0.f;
+  }
+}
+
+void launch_block_start(int32_t* ctl, int first_block, const int32_t* init_canvas, BlockState bs,
+                        int B, int L, int d, cudaStream_t st) {
+  k_block_start<<<2 * 152, 256, 0, st>>>(ctl, first_block, init_canvas, bs, B, L, d);
+}
+
+void launch_block_check(int32_t* ctl, const uint8_t* done, int B, int first_block, int n_blocks,
+                        int max_iters, bool use_cond, cudaGraphConditionalHandle h,
+                        cudaStream_t st) {
+  k_block_check<<<1, 32, 0, st>>>(ctl, done, B, first_block, n_blocks, max_iters,
+                                  use_cond ? 1 : 0, h);
+}
+
+void launch_block_rollover(const int32_t* ctl, const int32_t* init_canvas, int32_t* out_canvas,
+                           int32_t* out_steps, BlockState bs, int B, int L, int d,
+                           cudaStream_t st) {
+  k_block_rollover<<<2 * 152, 256, 0, st>>>(ctl, init_canvas, out_canvas, out_steps, bs, B, L, d);
+}
+
 void launch_temperature(const int32_t* step, int B, float t_start, float t_end, int max_steps,
                         float* T, cudaStream_t st) {
   k_temperature<<<(B + 127) / 128, 128, 0, st>>>(step, B, t_start, t_end, max_steps, T);
 }
 
-void launch_lock_entropy(int B, int L, int64_t V, int max_steps, uint64_t seed, float budget,
-                         float stop_entropy, const int32_t* sampled, const float* entropy,
-                         const int32_t* argmax, int32_t* prev_argmax, int32_t* step,
-                         int32_t* canvas, uint8_t* lock, uint8_t* done, cudaStream_t st) {
-  k_lock_entropy<<<B, L, 0, st>>>(L, (uint32_t)V, max_steps, seed, budget, stop_entropy, sampled,
-                                  entropy, argmax, prev_argmax, step, canvas, lock, done);
+void launch_lock_entropy(int B, int L, int64_t V, int max_steps, uint64_t seed,
+                         const int32_t* blk, float budget, float stop_entropy,
+                         const int32_t* sampled, const float* entropy, const int32_t* argmax,
+                         int32_t* prev_argmax, int32_t* step, int32_t* canvas, uint8_t* lock,
+                         uint8_t* done, cudaStream_t st) {
+  k_lock_entropy<<<B, L, 0, st>>>(L, (uint32_t)V, max_steps, seed, blk, budget, stop_entropy,
+                                  sampled, entropy, argmax, prev_argmax, step, canvas, lock, done);
 }
 
 void launch_wait_selftest(uint64_t limit_ns, uint32_t* err, cudaStream_t st) {
@@ -813,11 +917,11 @@ void launch_row_merge(const ChunkStat* cs, int n_chunks, int R, int L, const uin
 }
 
 void launch_convert(const float* Y, const RowStat* rs, int R, int64_t V, int L,
-                    const uint8_t* done, const int32_t* step, uint64_t seed, bool gumbel,
-                    uint16_t* Phi, uint16_t* Plo, Best* best, cudaStream_t st) {
+                    const uint8_t* done, const int32_t* step, uint64_t seed, const int32_t* blk,
+                    bool gumbel, uint16_t* Phi, uint16_t* Plo, Best* best, cudaStream_t st) {
   const int nc = n_chunks_of(V);
-  k_convert<<<dim3(nc, R), kThreads, 0, st>>>(Y, rs, V, L, done, step, seed, gumbel ? 1 : 0, Phi,
-                                              Plo, best, nc);
+  k_convert<<<dim3(nc, R), kThreads, 0, st>>>(Y, rs, V, L, done, step, seed, blk, gumbel ? 1 : 0,
+                                              Phi, Plo, best, nc);
 
 }
 
@@ -829,27 +933,28 @@ void launch_topk_chunk(const float* Y, int R, int64_t V, int L, const uint8_t* d
 
 void launch_finalize(const RowStat* rs, const Best* best, const Cand* cand, int n_chunks, int k,
                      int R, int L, const uint8_t* done, const int32_t* step, uint64_t seed,
-                     int32_t* sampled, float* conf, float* entropy, int32_t* argmax,
-                     cudaStream_t st) {
-  k_finalize<<<R, kThreads, 0, st>>>(rs, best, cand, n_chunks, k, L, done, step, seed, sampled,
-                                     conf, entropy, argmax, nullptr, 0, R, 0, nullptr, nullptr);
+                     const int32_t* blk, int32_t* sampled, float* conf, float* entropy,
+                     int32_t* argmax, cudaStream_t st) {
+  k_finalize<<<R, kThreads, 0, st>>>(rs, best, cand, n_chunks, k, L, done, step, seed, blk,
+                                     sampled, conf, entropy, argmax, nullptr, 0, R, 0, nullptr,
+                                     nullptr);
 }
 
 void launch_finalize_with_s(const RowStat* rs, const Best* best, const Cand* cand, int n_chunks,
                             int k, int R, int L, const uint8_t* done, const int32_t* step,
-                            uint64_t seed, int32_t* sampled, float* conf, float* entropy,
-                            int32_t* argmax, const float* Opart, int S, int d, float* s,
-                            const float* mref, cudaStream_t st) {
-  k_finalize<<<R, kThreads, 0, st>>>(rs, best, cand, n_chunks, k, L, done, step, seed, sampled,
-                                     conf, entropy, argmax, Opart, S, R, d, s, mref);
+                            uint64_t seed, const int32_t* blk, int32_t* sampled, float* conf,
+                            float* entropy, int32_t* argmax, const float* Opart, int S, int d,
+                            float* s, const float* mref, cudaStream_t st) {
+  k_finalize<<<R, kThreads, 0, st>>>(rs, best, cand, n_chunks, k, L, done, step, seed, blk,
+                                     sampled, conf, entropy, argmax, Opart, S, R, d, s, mref);
 }
 
 void launch_gumbel_seg(const uint16_t* Phi, const uint16_t* Plo, const ChunkStat* seg,
                        const RowStat* rs, int R, int64_t V, int L, const uint8_t* done,
-                       const int32_t* step, uint64_t seed, bool tile_ref, Best* best,
-                       cudaStream_t st) {
+                       const int32_t* step, uint64_t seed, const int32_t* blk, bool tile_ref,
+                       Best* best, cudaStream_t st) {
   const int nc = n_chunks_of(V);
-  k_gumbel_seg<<<dim3(nc, R), kThreads, 0, st>>>(Phi, Plo, seg, rs, V, L, done, step, seed,
+  k_gumbel_seg<<<dim3(nc, R), kThreads, 0, st>>>(Phi, Plo, seg, rs, V, L, done, step, seed, blk,
                                                  tile_ref ? 1 : 0, best, nc);
 }
 
@@ -860,11 +965,11 @@ void launch_reduce_s(const float* Opart, int S, int R, int d, int L, const uint8
   k_reduce_s<<<blocks, 256, 0, st>>>(Opart, S, R, d, L, done, rs, s);
 }
 
-void launch_lock(int B, int L, int64_t V, int max_steps, uint64_t seed, const float* tau,
-                 const int32_t* sampled, const float* conf, int32_t* step, int32_t* canvas,
-                 uint8_t* lock, uint8_t* done, cudaStream_t st) {
-  k_lock<<<B, L, 0, st>>>(L, (uint32_t)V, max_steps, seed, tau, sampled, conf, step, canvas, lock,
-                          done);
+void launch_lock(int B, int L, int64_t V, int max_steps, uint64_t seed, const int32_t* blk,
+                 const float* tau, const int32_t* sampled, const float* conf, int32_t* step,
+                 int32_t* canvas, uint8_t* lock, uint8_t* done, cudaStream_t st) {
+  k_lock<<<B, L, 0, st>>>(L, (uint32_t)V, max_steps, seed, blk, tau, sampled, conf, step, canvas,
+                          lock, done);
 }
 
 void launch_philox(const uint32_t* ctr, uint64_t seed, uint32_t* out, int64_t n, cudaStream_t st) {

@@ -182,6 +182,42 @@ class Sampler:
                 "ds_denoise_loop")
         return out
 
+    def block_loop(self, E, temperature, tau, state: CanvasState, seed: int, out: StepOutputs,
+                   init_canvas, out_canvas, out_steps, *, first_block: int = 0, H=None, W=None,
+                   H_buf=None, max_iters: int | None = None, use_graph: bool = True,
+                   stream=None):
+        """ds_block_loop: generate init_canvas.shape[0] blocks one after another (each from its
+        initial canvas with fresh state), committing each finished canvas to out_canvas
+        [n_blocks, B, L] and its step counts to out_steps [n_blocks, B]. state and out are the
+        working buffers (their contents on entry are replaced)."""
+        standin = W is not None
+        self._check_tensors(H if not standin else H_buf, E, state, out)
+        n_blocks = int(init_canvas.shape[0])
+        B, L = state.canvas.shape
+        for t, shape in ((init_canvas, (n_blocks, B, L)), (out_canvas, (n_blocks, B, L)),
+                         (out_steps, (n_blocks, B))):
+            if tuple(t.shape) != shape or t.dtype != torch.int32 or not t.is_cuda:
+                raise ValueError(f"block buffers must be int32 CUDA tensors of shape {shape}")
+        ba = C.ds_block_args()
+        ba.loop.step = self._step_args(H if not standin else H_buf, E, temperature, tau, state, out,
+                                       seed)
+        ba.loop.h_mode = C.DS_H_STANDIN if standin else C.DS_H_FIXED
+        ba.loop.max_iters = self.max_steps if max_iters is None else int(max_iters)
+        ba.loop.use_graph = 1 if use_graph else 0
+        ba.loop.W = _ptr(W)
+        ba.loop.H_buf = _ptr(H_buf)
+        ba.n_blocks = n_blocks
+        ba.first_block = int(first_block)
+        ba.init_canvas = _ptr(init_canvas)
+        ba.out_canvas = _ptr(out_canvas)
+        ba.out_steps = _ptr(out_steps)
+        # graphs hold these pointers
+        self._keep = (E, temperature, tau, state, out, H, W, H_buf, init_canvas, out_canvas,
+                      out_steps)
+        C.check(self.lib.ds_block_loop(self.handle, byref(ba), _stream_handle(stream)),
+                "ds_block_loop")
+        return out_canvas, out_steps
+
     def standin_hidden(self, W, s_prev, E, canvas, done, H_out, stream=None):
         B = canvas.shape[0]
         C.check(self.lib.ds_standin_hidden(self.handle, _ptr(W), _ptr(s_prev), _ptr(E), _ptr(canvas),

@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define DS_SAMPLER_ABI_VERSION 2
+#define DS_SAMPLER_ABI_VERSION 3
 
 typedef enum ds_status {
   DS_OK = 0,
@@ -169,6 +169,31 @@ typedef struct ds_loop_args {
   void* H_buf;
 } ds_loop_args;
 
+/* Block-autoregressive generation ("DiffusionGemma: Google's open diffusion LLM": generation
+ * continues block by block, each new canvas starting from noise once the previous one is
+ * committed). loop describes the per-block loop: loop.step holds the working state and outputs
+ * (canvas, lock, step, done, prev_argmax, s, ...), loop.max_iters bounds each block's steps,
+ * h_mode / W / H_buf as for ds_denoise_loop (the stand-in sees only the current block: the
+ * model's attention to committed blocks is out of scope).
+ * For k = 0 .. n_blocks - 1: the state is reset (canvas = init_canvas[k], no locks, step 0,
+ * done 0, prev_argmax -1, s = 0), the block's steps run until every sequence is done, and the
+ * block is committed: out_canvas[k] = canvas, out_steps[k] = step. Block k draws its random
+ * numbers with counter word 2 = sequence + 2^16 (first_block + k); block 0 draws exactly as a
+ * single canvas does. The whole run is one graph launch when loop.use_graph is set (a while
+ * node over all blocks' steps, no host synchronisation), else plain launches of
+ * n_blocks * max_iters steps (finished blocks and sequences are skipped).
+ *   init_canvas [n_blocks, B, L] int32, out_canvas [n_blocks, B, L] int32,
+ *   out_steps [n_blocks, B] int32, all [device]; 1 <= n_blocks, first_block >= 0,
+ *   first_block + n_blocks <= 65536. */
+typedef struct ds_block_args {
+  ds_loop_args loop;
+  int32_t n_blocks;
+  int32_t first_block;
+  const int32_t* init_canvas;
+  int32_t* out_canvas;
+  int32_t* out_steps;
+} ds_block_args;
+
 /* Version of this ABI (DS_SAMPLER_ABI_VERSION). */
 int32_t ds_abi_version(void);
 
@@ -203,6 +228,9 @@ ds_status ds_sampler_step_host(ds_sampler* sampler, const ds_step_args* host_arg
 
 /* Enqueue a denoising loop on `stream` (see ds_loop_args). */
 ds_status ds_denoise_loop(ds_sampler* sampler, const ds_loop_args* args, void* stream);
+
+/* Enqueue a block-autoregressive run on `stream` (see ds_block_args). */
+ds_status ds_block_loop(ds_sampler* sampler, const ds_block_args* args, void* stream);
 
 /* Enqueue the hidden-state stand-in alone: H_out = bf16(tanh(W . [bf16(s_prev); E[canvas]]))
  * for sequences with done == 0 (done may be NULL). W [d, 2d] bf16, s_prev [B, L, d] float,

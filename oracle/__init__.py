@@ -51,4 +51,5 @@ from .sampler import (  # noqa: F401
     LOCK_ENTROPY_BUDGET,
     standin_hidden,
     denoise_loop,
+    block_loop,
 )

@@ -30,10 +30,16 @@ The pages print no sampler listing; the readings taken where they are silent:
 * the pages' own default sampler (sokufu.com, "A diffusion language model refines 256 tokens
   in 12 steps", and its Table 2) is the second lock rule, see entropy_budget_update;
 * random draws come from Philox4x32-10 keyed by the seed (low, high word), with counters
-    Gumbel  (j >> 2, i, b, 4*step + 0), word j & 3, u = (2*(r >> 9) + 1) / 2**24,
-    re-noise (i >> 2, 0, b, 4*step + 1), word i & 3, token = (r * V) >> 32.
-  u takes 2**23 values, symmetric in (0, 1) and exactly representable in fp32; the token
-  map is exactly uniform when V is a power of two.
+    Gumbel  (j >> 2, i, sid, 4*step + 0), word j & 3, u = (2*(r >> 9) + 1) / 2**24,
+    re-noise (i >> 2, 0, sid, 4*step + 1), word i & 3, token = (r * V) >> 32,
+  where sid = b + 2**16 * block: the sequence, and the block of a block-autoregressive run
+  (block 0 for a single canvas). u takes 2**23 values, symmetric in (0, 1) and exactly
+  representable in fp32; the token map is exactly uniform when V is a power of two.
+* block-autoregressive generation (the pages' "block diffusion" continuation: a finished canvas
+  is committed and the next one starts from fresh noise) is block_loop: each block is one
+  denoising loop from its own initial canvas with fresh state (no locks, step 0, s = 0) and its
+  own draws (block index in the counters); the model's conditioning on committed blocks is out
+  of scope, so the stand-in hidden state does not see them.
 """
 from __future__ import annotations
 
@@ -170,7 +176,7 @@ def _sample_row(y_row, g_row, p_row, top_k, band=1e-4):
 
 def sampler_step(H, E, T, tau, canvas, lock, step, done, seed, *, top_k=0, max_steps=48,
                  positions=None, row_chunk=64, lock_rule=LOCK_THRESHOLD, entropy_budget=0.1,
-                 stop_entropy=0.005, t_schedule=None, prev_argmax=None):
+                 stop_entropy=0.005, t_schedule=None, prev_argmax=None, block=0):
     """One sampler step over a batch, in fp64.
 
     H [B, L, d] and E [V, d] are the exact input values as float64 (bf16 or fp32 inputs
@@ -187,7 +193,8 @@ def sampler_step(H, E, T, tau, canvas, lock, step, done, seed, *, top_k=0, max_s
 
     lock_rule LOCK_ENTROPY_BUDGET replaces the threshold rule by entropy_budget_update
     (prev_argmax [B, L] carries the previous step's argmax); t_schedule = (t_start, t_end)
-    replaces T by the scheduled temperature of each sequence's step."""
+    replaces T by the scheduled temperature of each sequence's step. ``block`` selects the draws
+    of that block of a block-autoregressive run (counter word 2 = b + 2**16 block)."""
     H = np.asarray(H, dtype=np.float64)
     E = np.asarray(E, dtype=np.float64)
     B, L, d = H.shape
@@ -221,7 +228,7 @@ def sampler_step(H, E, T, tau, canvas, lock, step, done, seed, *, top_k=0, max_s
             if V > 1:
                 top2 = np.partition(y, -2, axis=1)[:, -2:]
                 out["argmax_gap"][b, rows] = top2[:, 1] - top2[:, 0]
-            u = gumbel_uniforms(seed, b, rows, int(step[b]), V)
+            u = gumbel_uniforms(seed, b + (int(block) << 16), rows, int(step[b]), V)
             g = -np.log(-np.log(u))
             for r, i in enumerate(rows):
                 x, c, margin, risk = _sample_row(y[r], g[r], p[r], top_k)
@@ -243,13 +250,13 @@ def sampler_step(H, E, T, tau, canvas, lock, step, done, seed, *, top_k=0, max_s
             if lock_rule == LOCK_ENTROPY_BUDGET:
                 cv, lk, st, dn, pa = entropy_budget_update(
                     new["canvas"][b], out["sampled"][b], out["entropy"][b], out["argmax"][b],
-                    new["prev_argmax"][b], int(step[b]), seed, b, V, max_steps, entropy_budget,
-                    stop_entropy)
+                    new["prev_argmax"][b], int(step[b]), seed, b + (int(block) << 16), V,
+                    max_steps, entropy_budget, stop_entropy)
                 new["prev_argmax"][b] = pa
             else:
                 cv, lk, st, dn = lock_update(new["canvas"][b], new["lock"][b], out["sampled"][b],
                                              out["conf"][b], float(tau[b]), int(step[b]), seed,
-                                             b, V, max_steps)
+                                             b + (int(block) << 16), V, max_steps)
             new["canvas"][b], new["lock"][b], new["step"][b], new["done"][b] = cv, lk, st, dn
     out.update(new)
     return out
@@ -334,7 +341,8 @@ def standin_hidden(W_bits, s_prev, E, canvas):
 
 def denoise_loop(E, T, tau, canvas, lock, step, done, seed, *, H=None, W_bits=None,
                  s_prev=None, top_k=0, max_steps=48, max_iters=None, lock_rule=LOCK_THRESHOLD,
-                 entropy_budget=0.1, stop_entropy=0.005, t_schedule=None, prev_argmax=None):
+                 entropy_budget=0.1, stop_entropy=0.005, t_schedule=None, prev_argmax=None,
+                 block=0):
     """Run steps until every sequence is done (or max_iters); returns the per-step records.
 
     Fixed-H mode passes H (fp64 [B, L, d]); stand-in mode passes W_bits and recomputes H
@@ -358,7 +366,7 @@ def denoise_loop(E, T, tau, canvas, lock, step, done, seed, *, H=None, W_bits=No
                            state["done"], seed, top_k=top_k, max_steps=max_steps,
                            lock_rule=lock_rule, entropy_budget=entropy_budget,
                            stop_entropy=stop_entropy, t_schedule=t_schedule,
-                           prev_argmax=state["prev_argmax"])
+                           prev_argmax=state["prev_argmax"], block=block)
         out["H"] = Hs
         active = state["done"] == 0
         s_new = state["s"].copy()
@@ -367,3 +375,24 @@ def denoise_loop(E, T, tau, canvas, lock, step, done, seed, *, H=None, W_bits=No
                  "done": out["done"], "s": s_new, "prev_argmax": out["prev_argmax"]}
         records.append(out)
     return state, records
+
+
+def block_loop(E, T, tau, init_canvas, seed, *, first_block=0, **loop_kw):
+    """Block-autoregressive generation: for k = 0 .. n_blocks - 1 run denoise_loop from
+    init_canvas[k] ([n_blocks, B, L]) with fresh state (no locks, step 0, done 0, s = 0, no
+    previous argmax) and block index first_block + k, then commit the canvas.
+
+    Returns (tokens [n_blocks, B, L], steps [n_blocks, B], per-block records)."""
+    init_canvas = np.asarray(init_canvas)
+    n_blocks, B, L = init_canvas.shape
+    tokens = np.zeros((n_blocks, B, L), np.int64)
+    steps = np.zeros((n_blocks, B), np.int64)
+    records = []
+    for k in range(n_blocks):
+        state, rec = denoise_loop(E, T, tau, init_canvas[k], np.zeros((B, L), np.uint8),
+                                  np.zeros(B, np.int64), np.zeros(B, np.uint8), seed,
+                                  block=first_block + k, **loop_kw)
+        tokens[k] = state["canvas"]
+        steps[k] = state["step"]
+        records.append(rec)
+    return tokens, steps, records

@@ -110,7 +110,7 @@ def compare_outputs(gpu: dict, ref: dict, active_rows, *, top_k=0):
 
 
 def check_lock_update(pre: dict, gpu_out: dict, gpu_post: dict, ref: dict | None, tau, seed, V,
-                      max_steps):
+                      max_steps, block=0):
     """The GPU's lock / re-noise / stop against the rule applied to the GPU's own sampled
     tokens and confidences (exact), and against the oracle where the decision is unambiguous."""
     B = pre["canvas"].shape[0]
@@ -122,7 +122,8 @@ def check_lock_update(pre: dict, gpu_out: dict, gpu_post: dict, ref: dict | None
             continue
         cv, lk, st, dn = oracle.lock_update(pre["canvas"][b], pre["lock"][b], gpu_out["sampled"][b],
                                             gpu_out["conf"][b].astype(np.float64), float(tau[b]),
-                                            int(pre["step"][b]), seed, b, V, max_steps)
+                                            int(pre["step"][b]), seed, b + (block << 16), V,
+                                            max_steps)
         assert np.array_equal(gpu_post["lock"][b], lk), f"lock rule on GPU inputs, seq {b}"
         assert np.array_equal(gpu_post["canvas"][b], cv), f"canvas rule on GPU inputs, seq {b}"
         assert gpu_post["step"][b] == st and gpu_post["done"][b] == dn

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol():
 def test_version_and_status_strings_without_gpu():
     C = _lib()
     lib = C.load_library()
-    assert lib.ds_abi_version() == 2
+    assert lib.ds_abi_version() == 3
     for code in range(7):
         assert lib.ds_status_string(code)
     assert lib.ds_status_string(99) == b"unknown status"
@@ -64,12 +64,15 @@ PROBE = r"""
 #include "ds_sampler.h"
 #define P(T, F) printf("%s.%s %zu\n", #T, #F, offsetof(T, F));
 int main(void) {
-  printf("ds_sampler_config %zu\nds_step_args %zu\nds_loop_args %zu\n",
-         sizeof(ds_sampler_config), sizeof(ds_step_args), sizeof(ds_loop_args));
+  printf("ds_sampler_config %zu\nds_step_args %zu\nds_loop_args %zu\nds_block_args %zu\n",
+         sizeof(ds_sampler_config), sizeof(ds_step_args), sizeof(ds_loop_args),
+         sizeof(ds_block_args));
   P(ds_sampler_config, vocab) P(ds_sampler_config, top_k) P(ds_sampler_config, lock_rule)
   P(ds_sampler_config, entropy_budget) P(ds_sampler_config, t_end)
   P(ds_step_args, seed) P(ds_step_args, H) P(ds_step_args, argmax) P(ds_step_args, prev_argmax)
   P(ds_loop_args, h_mode) P(ds_loop_args, W) P(ds_loop_args, H_buf)
+  P(ds_block_args, n_blocks) P(ds_block_args, first_block) P(ds_block_args, init_canvas)
+  P(ds_block_args, out_steps)
   return 0;
 }
 """
@@ -88,6 +91,7 @@ def test_struct_layouts_match_c(tmp_path):
     assert int(got["ds_sampler_config"]) == ctypes.sizeof(C.ds_sampler_config)
     assert int(got["ds_step_args"]) == ctypes.sizeof(C.ds_step_args)
     assert int(got["ds_loop_args"]) == ctypes.sizeof(C.ds_loop_args)
+    assert int(got["ds_block_args"]) == ctypes.sizeof(C.ds_block_args)
     for key, val in got.items():
         if "." in key:
             t, f = key.split(".")

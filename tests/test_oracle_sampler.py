@@ -400,3 +400,61 @@ def test_entropy_budget_loop_stops_on_a_confident_stable_canvas():
                                  lock_rule=O.LOCK_ENTROPY_BUDGET, t_schedule=(0.8, 0.4))
     assert state["done"][0] == 1 and len(recs) == 2  # step 0 cannot stop; step 1 does
     assert np.array_equal(state["canvas"][0], recs[-1]["argmax"][0])
+
+
+# ---------------------------------------------------------------- block-autoregressive runs
+
+def test_block_draws_carry_the_block_in_counter_word_2():
+    # Gumbel and re-noise draws of block k use counter word 2 = b + 2^16 k: the sample is the
+    # argmax of y + g with g from the scalar Philox at that counter, the re-noised tokens map
+    # its words; block 0 is the single-canvas draw
+    rng = np.random.default_rng(31)
+    B, L, V, d, seed, step = 2, 8, 24, 6, 0xABCDEF, 3
+    E = rng.standard_normal((V, d)) / math.sqrt(d)
+    H = rng.standard_normal((B, L, d))
+    canvas = rng.integers(0, V, (B, L))
+    lock = np.zeros((B, L), np.uint8)
+    st = np.full(B, step, np.int64)
+    done = np.zeros(B, np.uint8)
+    T, tau = [1.0, 0.9], [0.99, 0.99]
+    outs = {}
+    for blk in (0, 1, 7):
+        out = O.sampler_step(H, E, T, tau, canvas, lock, st, done, seed, max_steps=48, block=blk)
+        outs[blk] = out
+        for b in range(B):
+            sid = b + (blk << 16)
+            y = (H[b] @ E.T) / T[b]
+            for i in range(L):
+                u = np.array([(2 * (int(philox4x32_10(j >> 2, i, sid, 4 * step,
+                                                      seed_key(seed))[j & 3]) >> 9) + 1) / 2 ** 24
+                              for j in range(V)])
+                assert out["sampled"][b, i] == int(np.argmax(y[i] - np.log(-np.log(u))))
+            renoised = out["lock"][b] == 0
+            for i in np.nonzero(renoised)[0]:
+                r = int(philox4x32_10(i >> 2, 0, sid, 4 * step + 1, seed_key(seed))[i & 3])
+                assert out["canvas"][b, i] == (r * V) >> 32
+    default = O.sampler_step(H, E, T, tau, canvas, lock, st, done, seed, max_steps=48)
+    assert np.array_equal(default["sampled"], outs[0]["sampled"])
+    assert not np.array_equal(outs[1]["sampled"], outs[7]["sampled"])
+
+
+def test_block_loop_chains_fresh_denoising_loops():
+    rng = np.random.default_rng(32)
+    n_blocks, B, L, V, d = 3, 2, 16, 64, 8
+    E = rng.standard_normal((V, d)) / math.sqrt(d)
+    H = rng.standard_normal((B, L, d)) * 2
+    init = rng.integers(0, V, (n_blocks, B, L))
+    init[2] = init[1]  # same noise, different block: different draws
+    kw = dict(H=H, max_steps=12)
+    tokens, steps, recs = O.block_loop(E, [1.0, 0.8], [0.9, 0.6], init, 5, **kw)
+    z = dict(lock=np.zeros((B, L), np.uint8), step=np.zeros(B, np.int64),
+             done=np.zeros(B, np.uint8))
+    for k in range(n_blocks):
+        state, _ = O.denoise_loop(E, [1.0, 0.8], [0.9, 0.6], init[k], seed=5, block=k, **kw, **z)
+        assert np.array_equal(tokens[k], state["canvas"])
+        assert np.array_equal(steps[k], state["step"])
+        assert np.all(steps[k] <= 12) and state["done"].all()
+    assert not np.array_equal(tokens[1], tokens[2])
+    # first_block shifts the block indices: blocks 1..2 alone reproduce the last two blocks
+    t2, s2, _ = O.block_loop(E, [1.0, 0.8], [0.9, 0.6], init[1:], 5, first_block=1, **kw)
+    assert np.array_equal(t2, tokens[1:]) and np.array_equal(s2, steps[1:])
