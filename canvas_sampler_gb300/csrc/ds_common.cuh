@@ -178,11 +178,13 @@ DS_DEV void gumbel_race16(const uint4& hia, const uint4& loa, float sa, const ui
     for (int e = 0; e < 4; ++e) {
       const float pe = p[4 * q + e];
       if (!(pe > 0.f)) continue;
-      const uint32_t wd = word_of(w[q], e);
-      // 1 - u for u = (2q + 1) / 2^24, exact in fp32
-      const float omu = __uint2float_rn(0xFFFFFFu - 2u * (wd >> 9)) * 5.9604644775390625e-8f;
+      // f = 1 + (r >> 9) 2^-23 from the mantissa bits; u = (2 (r >> 9) + 1) / 2^24 = (f - 1) +
+      // 2^-24 and 1 - u = (2 - f) - 2^-24, both exact in fp32 (24 significant bits), without an
+      // integer-to-float conversion
+      const float f = __uint_as_float(0x3F800000u | (word_of(w[q], e) >> 9));
+      const float omu = (2.0f - f) - 5.9604644775390625e-8f;
       if (omu * (1.0f - 9.5367431640625e-7f) > kbest * pe) continue;
-      const float key = -logf(word_to_uniform(wd)) / pe;
+      const float key = -logf((f - 1.0f) + 5.9604644775390625e-8f) / pe;
       if (key < kbest) {
         kbest = key;
         bj = (int32_t)(j + 4 * q + e);
