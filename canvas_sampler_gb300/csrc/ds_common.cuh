@@ -135,34 +135,70 @@ DS_DEV void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
 // 19.6 > 16.64 + 2.81 leaves margin for fp32 rounding.
 constexpr float kGumbelReach = 19.6f;
 
+// One token's entry in the exponential race: p_j > 0 its probability (relative to the row
+// maximum), r the Philox word of its Gumbel draw. f = 1 + (r >> 9) 2^-23 from the mantissa bits;
+// u = (2 (r >> 9) + 1) / 2^24 = (f - 1) + 2^-24 and 1 - u = (2 - f) - 2^-24, both exact in fp32
+// (24 significant bits), without an integer-to-float conversion. 1 - u > kc p_j proves
+// E_j / p_j > kc without the logarithm (-ln u >= 1 - u; the factor 1 - 2^-20 covers the rounding
+// of the computed key), so the token cannot beat a key kc that is already known.
+DS_DEV void gumbel_token(float pe, uint32_t r, int32_t j, float kc, float& kbest, int32_t& bj,
+                         float& bp) {
+  const float f = __uint_as_float(0x3F800000u | (r >> 9));
+  const float omu = (2.0f - f) - 5.9604644775390625e-8f;
+  if (omu * (1.0f - 9.5367431640625e-7f) > kc * pe) return;
+  const float key = -logf((f - 1.0f) + 5.9604644775390625e-8f) / pe;
+  if (key < kbest) {
+    kbest = key;
+    bj = j;
+    bp = pe;
+  }
+}
+
+// p of the 8 tokens of a bf16 hi / lo group (two tokens per word, the lower token in the low
+// half), times the group's scale.
+DS_DEV void unpack_p8(const uint4& hi, const uint4& lo, float sc, float (&p)[8]) {
+  const uint32_t hw[4] = {hi.x, hi.y, hi.z, hi.w};
+  const uint32_t lw[4] = {lo.x, lo.y, lo.z, lo.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    p[2 * e] = (__uint_as_float(hw[e] << 16) + __uint_as_float(lw[e] << 16)) * sc;
+    p[2 * e + 1] = (__uint_as_float(hw[e] & 0xFFFF0000u) + __uint_as_float(lw[e] & 0xFFFF0000u)) * sc;
+  }
+}
+
 // The Gumbel-max exponential race over 16 consecutive tokens j .. j + 15 of position i of
 // sequence b: with E_j = -ln u_j (u_j from the Gumbel stream of Philox) and p_j = exp(y_j - m)
 // (m the row maximum), argmax_j (y_j - ln E_j) = argmin_j E_j / p_j. p_j arrives as bf16 hi + lo
-// pairs (packed two tokens per word, the lower token in the low half), in two groups of eight with
-// scales sa, sb. 1 - u_j > kbest p_j proves E_j / p_j > kbest without the logarithm
-// (-ln u >= 1 - u); a group of four is skipped without its draw when even the smallest E
-// (> 2^-24) over its largest p cannot beat kbest, decided on kbest before any of the 16 tokens (a
-// larger kbest only skips less); the four draws are computed together. Tokens arrive in
-// increasing j, so a strict comparison keeps the lowest token on ties.
+// in two groups of eight with scales sa, sb. Tokens are tested against kc = min(kbest, cut),
+// cut being a key some token has already reached (the warp's best so far): a group of four is
+// skipped without its draw when even the smallest E (> 2^-24) over its largest p cannot beat kc,
+// and a token without its logarithm when 1 - u_j proves it cannot; both skips need a strict
+// inequality, so a token tying the best is never skipped. The four draws are computed together.
+// Tokens arrive in increasing j, so a strict comparison keeps the lowest token on ties. With
+// SKIP4 the first four tokens are left out (already raced by gumbel_seed4).
+template <bool SKIP4 = false>
 DS_DEV void gumbel_race16(const uint4& hia, const uint4& loa, float sa, const uint4& hib,
                           const uint4& lob, float sb, int64_t j, uint32_t i, uint32_t b,
-                          uint32_t step, uint64_t seed, float& kbest, int32_t& bj, float& bp) {
-  const uint32_t hw[8] = {hia.x, hia.y, hia.z, hia.w, hib.x, hib.y, hib.z, hib.w};
-  const uint32_t lw[8] = {loa.x, loa.y, loa.z, loa.w, lob.x, lob.y, lob.z, lob.w};
+                          uint32_t step, uint64_t seed, float cut, float& kbest, int32_t& bj,
+                          float& bp) {
   float p[16];
+  {
+    float pa[8], pb[8];
+    unpack_p8(hia, loa, sa, pa);
+    unpack_p8(hib, lob, sb, pb);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const float sc = e < 4 ? sa : sb;
-    p[2 * e] = (__uint_as_float(hw[e] << 16) + __uint_as_float(lw[e] << 16)) * sc;
-    p[2 * e + 1] =
-        (__uint_as_float(hw[e] & 0xFFFF0000u) + __uint_as_float(lw[e] & 0xFFFF0000u)) * sc;
+    for (int e = 0; e < 8; ++e) {
+      p[e] = pa[e];
+      p[8 + e] = pb[e];
+    }
   }
   bool need[4];
   bool any = false;
+  const float kc0 = fminf(kbest, cut);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const float pm = fmaxf(fmaxf(p[4 * q], p[4 * q + 1]), fmaxf(p[4 * q + 2], p[4 * q + 3]));
-    need[q] = !(5.9604645e-8f >= kbest * pm);
+    need[q] = !(SKIP4 && q == 0) && !(5.9604645e-8f >= kc0 * pm);
     any |= need[q];
   }
   if (!any) return;
@@ -178,20 +214,25 @@ DS_DEV void gumbel_race16(const uint4& hia, const uint4& loa, float sa, const ui
     for (int e = 0; e < 4; ++e) {
       const float pe = p[4 * q + e];
       if (!(pe > 0.f)) continue;
-      // f = 1 + (r >> 9) 2^-23 from the mantissa bits; u = (2 (r >> 9) + 1) / 2^24 = (f - 1) +
-      // 2^-24 and 1 - u = (2 - f) - 2^-24, both exact in fp32 (24 significant bits), without an
-      // integer-to-float conversion
-      const float f = __uint_as_float(0x3F800000u | (word_of(w[q], e) >> 9));
-      const float omu = (2.0f - f) - 5.9604644775390625e-8f;
-      if (omu * (1.0f - 9.5367431640625e-7f) > kbest * pe) continue;
-      const float key = -logf((f - 1.0f) + 5.9604644775390625e-8f) / pe;
-      if (key < kbest) {
-        kbest = key;
-        bj = (int32_t)(j + 4 * q + e);
-        bp = pe;
-      }
+      gumbel_token(pe, word_of(w[q], e), (int32_t)(j + 4 * q + e), fminf(kbest, cut), kbest, bj,
+                   bp);
     }
   }
+}
+
+// The race over the first four tokens j .. j + 3 of a group (words hi.x, hi.y) without any
+// cutoff, for every lane of a warp at once: its result seeds the warp's cutoff before the lanes
+// race their other tokens, so that the logarithm is taken on few tokens (and few lanes).
+DS_DEV void gumbel_seed4(const uint4& hi, const uint4& lo, float sc, int64_t j, uint32_t i,
+                         uint32_t b, uint32_t step, uint64_t seed, float& kbest, int32_t& bj,
+                         float& bp) {
+  float p[8];
+  unpack_p8(hi, lo, sc, p);
+  u32x4 w[1] = {u32x4{(uint32_t)(j >> 2), i, b, (step << 2) | kGumbelStream}};
+  philox4x32_10_n<1>(w, (uint32_t)seed, (uint32_t)(seed >> 32));
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    if (p[e] > 0.f) gumbel_token(p[e], word_of(w[0], e), (int32_t)(j + e), INFINITY, kbest, bj, bp);
 }
 
 // Better (v, j) pair: larger v, then lower j.
@@ -243,16 +284,32 @@ DS_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+DS_DEV bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Wait for the phase of `parity` to complete. Gives up (and returns false) when the CTA's
 // abort flag is raised by another role or when kWaitLimitNs pass; on a time-out it raises the
 // abort flag and sets the device error word.
+// kCluster: acquire at cluster scope (arrivals from the peer CTA of a pair).
+template <bool kCluster = false>
 DS_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t* err) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto test = [&]() {
+    if constexpr (kCluster) return mbar_try_wait_cluster(bar, parity);
+    else return mbar_try_wait(bar, parity);
+  };
+  if (test()) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (test()) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       *abort_flag = 1;
@@ -307,6 +364,9 @@ DS_DEV void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_
 DS_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every committed bulk store of this thread has finished reading shared memory.
 DS_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until all but the most recent committed bulk group of this thread have finished reading
+// shared memory.
+DS_DEV void bulk_wait_read_le1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // Wait until every committed bulk store of this thread has completed.
 DS_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy (TMA).
@@ -379,6 +439,74 @@ DS_DEV void umma_commit(uint32_t bar) {
                : "memory");
 }
 
+// ---- CTA pairs (a cluster of two CTAs on the two SMs of a TPC) ----
+// One MMA of M = 256 spans both CTAs: each CTA holds its 128 rows of A and half of the N rows of
+// B in shared memory at the same offsets, and its 128 rows of D in its own TMEM (all N columns).
+// The even CTA issues the MMAs; TMEM is allocated by one warp of each CTA collectively.
+DS_DEV uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address in the shared::cluster window of the variable at `addr` (shared::cta) in CTA `rank`.
+DS_DEV uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// All threads of both CTAs (release / acquire at cluster scope).
+DS_DEV void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// Arrive on an mbarrier given by its shared::cluster address (this CTA's or the peer's), with
+// the default (CTA-scope) release: used where the order that matters is that of tcgen05
+// operations, which tcgen05.fence::before_thread_sync establishes, so no cluster-scope fence
+// is spent on it.
+DS_DEV void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Tile load into this CTA's shared memory whose completion is counted on an mbarrier of either
+// CTA of the pair (bar: shared::cluster address).
+DS_DEV void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x,
+                             int32_t y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(map), "r"(bar), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+DS_DEV void tmem_alloc_pair(uint32_t dst_slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_slot),
+               "r"(ncols)
+               : "memory");
+}
+DS_DEV void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+DS_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// D (+)= A . B^T over the CTA pair (M = 256), bf16 inputs, fp32 accumulators.
+DS_DEV void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                           uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on the mbarrier at offset `bar` in every CTA of `cta_mask` once the pair MMAs issued
+// so far by this thread have completed.
+DS_DEV void umma_commit_pair(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
 // 32 consecutive fp32 columns of the warp's 32 TMEM lanes (lane = row, register = column).
 DS_DEV void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
@@ -446,6 +574,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
 // ----------------------------------------------------------------------------------------
 // block reductions (blockDim.x == 256)
 // ----------------------------------------------------------------------------------------
+DS_DEV float warp_min(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
 DS_DEV float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

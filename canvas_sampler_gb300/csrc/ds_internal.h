@@ -119,6 +119,9 @@ constexpr int kTcSegment = 128;
 cudaError_t launch_logits_tc(const uint16_t* H, const uint16_t* E, int R, int64_t V, int d, int L,
                              const float* T, const uint8_t* done, float* Y, ChunkStat* seg_stats,
                              uint32_t* err, cudaStream_t st);
+// Whether the logits GEMMs run as CTA pairs (M = 256 tiles over two SMs) for R rows: R % 256 ==
+// 0 and not switched off by DS_LOGITS_PAIR=0 in the environment.
+bool logits_pair_enabled(int R);
 // The same GEMM writing, instead of y, P = exp(y - m_t) as bf16 hi + lo (m_t the row's maximum
 // over the token's 256-token tile) and m_t tile-major in mtile_t [V/256, R].
 cudaError_t launch_logits_p_tc(const uint16_t* H, const uint16_t* E, int R, int64_t V, int d,

@@ -404,12 +404,25 @@ __global__ void __launch_bounds__(kThreads, 3) k_gumbel_seg(
       lo[k] = h[k];
     }
   }
+  const uint32_t sid = stream_id((uint32_t)b, blk);
+  // every lane races its first four tokens in full; the warp's best key so far then cuts the
+  // rest (refreshed after each 16 tokens), so few lanes reach the logarithm
+  if (sc[0] > 0.f)
+    gumbel_seed4(h[0], lo[0], sc[0], j0 + 16 * (int64_t)threadIdx.x, (uint32_t)i, sid, st, seed,
+                 kbest, bj, bp);
+  float cut = warp_min(kbest);
 #pragma unroll
   for (int k = 0; k < kGroups8; k += 2) {
-    if (!(sc[k] > 0.f) && !(sc[k + 1] > 0.f)) continue;
-    const int64_t j = j0 + 8 * (int64_t)(2 * threadIdx.x + 2 * kThreads * (k >> 1));
-    gumbel_race16(h[k], lo[k], sc[k], h[k + 1], lo[k + 1], sc[k + 1], j, (uint32_t)i,
-                  stream_id((uint32_t)b, blk), st, seed, kbest, bj, bp);
+    if (sc[k] > 0.f || sc[k + 1] > 0.f) {
+      const int64_t j = j0 + 8 * (int64_t)(2 * threadIdx.x + 2 * kThreads * (k >> 1));
+      if (k == 0)
+        gumbel_race16<true>(h[k], lo[k], sc[k], h[k + 1], lo[k + 1], sc[k + 1], j, (uint32_t)i,
+                            sid, st, seed, cut, kbest, bj, bp);
+      else
+        gumbel_race16(h[k], lo[k], sc[k], h[k + 1], lo[k + 1], sc[k + 1], j, (uint32_t)i, sid,
+                      st, seed, cut, kbest, bj, bp);
+    }
+    cut = warp_min(fminf(cut, kbest));
   }
   float v = -kbest, y = logf(bp);
   block_best(v, bj, y, shv, shj, &shy);

@@ -29,9 +29,11 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;
 constexpr int kEpiWarps = 8;
 constexpr int kThreadsTC = 64 + 32 * kEpiWarps;
 
+constexpr int kMaxStages = 6;
+
 struct Ctl {
-  uint64_t full[4];
-  uint64_t empty[4];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t mma_done;
@@ -52,14 +54,15 @@ DS_DEV bool mbar_wait_quiet(uint32_t bar, uint32_t parity) {
   return true;
 }
 
-DS_DEV void ctl_init(Ctl& c, int stages) {
+// tempty_count: arrivals that release a TMEM buffer (every epilogue thread by default).
+DS_DEV void ctl_init(Ctl& c, int stages, uint32_t tempty_count = 32 * kEpiWarps) {
   for (int s = 0; s < stages; ++s) {
     mbar_init(smem_u32(&c.full[s]), 1);
     mbar_init(smem_u32(&c.empty[s]), 1);
   }
   for (int b = 0; b < 2; ++b) {
     mbar_init(smem_u32(&c.tfull[b]), 1);
-    mbar_init(smem_u32(&c.tempty[b]), 32 * kEpiWarps);
+    mbar_init(smem_u32(&c.tempty[b]), tempty_count);
   }
   mbar_init(smem_u32(&c.mma_done), 1);
   c.abort = 0;

@@ -8,6 +8,7 @@
 // Definitions: DiffusionGemma Technical Report, section 6 "Sampling" (softmax over the full
 // vocabulary in full precision). Pipeline structure: ds_tc_common.cuh.
 #include <algorithm>
+#include <cstdlib>
 
 #include "ds_tc_common.cuh"
 
@@ -19,22 +20,50 @@ using namespace tcpipe;
 // ------------------------------------------------------------------------------------------
 // logits (+ softmax statistics of each 128-token segment of a row)
 // ------------------------------------------------------------------------------------------
-constexpr int LG_BM = 128, LG_BN = 256, LG_BK = 64, LG_STAGES = 4, LG_CHUNK_KB = 2;
+// LG_CHUNK_KB: k-blocks (of 4 MMAs) accumulated into one TMEM chunk before the epilogue adds it
+// to its fp32 registers. Longer chains carry more of the accumulator's round-toward-zero error
+// but leave the epilogue's round trip (drain, release, next issue) and the output of each tile
+// more time to hide behind the MMAs. Measured against the fp64 oracle at V = 262144, d = 2816
+// (49 positions) and V = 32768, d = 1024 (256 positions), largest relative errors of s /
+// entropy: 2 k-blocks 2.4e-6 / 1.9e-6, 4: 3.6e-6 / 3.2e-6, 6: 3.6e-6 / 4.3e-6, 8: 5.5e-6 /
+// 7.2e-6, with the logits kernel at 0.393, 0.350, 0.335 and 0.327 ms.
+constexpr int LG_BM = 128, LG_BN = 256, LG_BK = 64, LG_STAGES = 4, LG_CHUNK_KB = 6;
 constexpr int LG_COLS = LG_BN / 2;
 constexpr uint32_t LG_A_BYTES = LG_BM * LG_BK * 2;
 constexpr uint32_t LG_B_BYTES = LG_BN * LG_BK * 2;
 constexpr uint32_t LG_STAGE_BYTES = LG_A_BYTES + LG_B_BYTES;
-// y leaves through one 32 x 32 fp32 staging box per epilogue warp (128-byte swizzle, written
-// by the warp, stored by one TMA bulk store), so the global stores are full lines.
+// The output leaves through 4 KB staging boxes, written by one epilogue warp and stored by TMA
+// (full lines in global memory): one 32 x 32 fp32 box of y, or a 32 x 32 bf16 box each of the
+// hi and lo parts of P.
 constexpr uint32_t LG_STG_BYTES = 32 * 32 * 4;
+// CTA pair: each CTA stages its 128 rows of H and 128 of the tile's 256 rows of E (32 KB a
+// stage), so an SM takes in 2/3 of the bytes per MAC of a one-CTA tile; the smaller stages
+// leave room for two staging boxes per warp, used in turn, so a warp writes the next box while
+// the TMA store of the previous one is still reading shared memory.
+constexpr int LG2_STAGES = 5, LG2_STG_BOXES = 2;
+constexpr uint32_t LG2_STAGE_BYTES = LG_A_BYTES + LG_B_BYTES / 2;
+static_assert(LG2_STAGES <= tcpipe::kMaxStages && LG_STAGES <= tcpipe::kMaxStages, "stages");
 constexpr size_t LG_SMEM =
     (size_t)LG_STAGES * LG_STAGE_BYTES + (size_t)kEpiWarps * LG_STG_BYTES + 1024;
+constexpr size_t LG2_SMEM = (size_t)LG2_STAGES * LG2_STAGE_BYTES +
+                            (size_t)kEpiWarps * LG2_STG_BOXES * LG_STG_BYTES + 1024;
 
 // kStandin: the same GEMM with A = U [R, 2d] (bf16(s_prev) | E[canvas]), B = W [d, 2d] and the
 // epilogue H = bf16(tanh(acc)) instead of y and the statistics (V plays N = d, d plays K = 2d).
 enum { kOutY = 0, kOutP = 1, kStandin = 2 };
 
-template <int MODE>
+// True when every sequence with a row in [r0, r0 + n) is finished.
+DS_DEV bool rows_done(const uint8_t* done, int r0, int n, int L) {
+  if (!done) return false;
+  for (int b = r0 / L; b <= (r0 + n - 1) / L; ++b)
+    if (!done[b]) return false;
+  return true;
+}
+
+// PAIR: launched in clusters of two CTAs; a work item is a 256-row x 256-token tile computed by
+// M = 256 MMAs that the even CTA issues for both, each CTA holding the accumulator of its own
+// 128 rows (its epilogue is the one-CTA epilogue of that 128 x 256 tile). Needs R % 256 == 0.
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(kThreadsTC, 1)
     k_logits_tc(const __grid_constant__ CUtensorMap mapH, const __grid_constant__ CUtensorMap mapE,
                 const __grid_constant__ CUtensorMap mapY, const __grid_constant__ CUtensorMap mapPlo,
@@ -42,23 +71,32 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 const uint8_t* __restrict__ done, ChunkStat* __restrict__ seg_stats,
                 float* __restrict__ mseg_t, uint16_t* __restrict__ Hout, uint32_t* err) {
   constexpr bool STANDIN = MODE == kStandin;
+  constexpr int STAGES = PAIR ? LG2_STAGES : LG_STAGES;
+  constexpr uint32_t STAGE_BYTES = PAIR ? LG2_STAGE_BYTES : LG_STAGE_BYTES;
+  constexpr int ROWS = PAIR ? 2 * LG_BM : LG_BM;  // rows of a work item
+  constexpr int NSTG = PAIR ? LG2_STG_BOXES : 1;  // staging boxes per epilogue warp
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Ctl ctl;
-  // kOutP: the two column halves' segment maxima of each row, and a barrier of all epilogue
-  // warps (bounded), passed twice an item: after the maxima are written and after they are read
+  // kOutP: the two column halves' segment maxima of each row, and per TMEM lane quadrant a
+  // barrier of its two epilogue warps (bounded), passed twice an item: after the maxima are
+  // written and after they are read
   __shared__ float xmax[2][LG_BM];
-  __shared__ uint64_t xbar;
+  __shared__ uint64_t xbar[4];
   uint8_t* smem = align1024(dyn_smem);
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_rt = R / LG_BM;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int n_units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int n_it = R / ROWS;  // row items
   const int n_ct = (int)(V / LG_BN);
-  const int n_tiles = n_rt * n_ct;
+  const int n_tiles = n_it * n_ct;
   const int nk = d / LG_BK;
   const int n_ch = (nk + LG_CHUNK_KB - 1) / LG_CHUNK_KB;
   if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&xbar), kEpiWarps);
-    ctl_init(ctl, LG_STAGES);  // ends with the mbarrier-init fence
+    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&xbar[i]), 2);
+    // pair: one arrival per epilogue warp of both CTAs releases a TMEM buffer of the pair
+    ctl_init(ctl, STAGES, PAIR ? 2 * kEpiWarps : 32 * kEpiWarps);  // ends with the init fence
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&mapH);
@@ -67,11 +105,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     if (MODE == kOutP) tma_prefetch_desc(&mapPlo);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ctl.tmem_base), 512);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(&ctl.tmem_base), 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&ctl.tmem_base), 512);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // both CTAs' barriers initialised before any remote use
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
   volatile int* abort_flag = &ctl.abort;
@@ -82,37 +126,49 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        const int rt = tile % n_rt, ct = tile / n_rt;
-        if (done && done[(rt * LG_BM) / L]) continue;
+      for (int tile = unit; tile < n_tiles && ok; tile += n_units) {
+        const int it = tile % n_it, ct = tile / n_it;
+        if (rows_done(done, it * ROWS, ROWS, L)) continue;
+        const int rt = PAIR ? 2 * it + (int)rank : it;
         for (int kc = 0; kc < nk; ++kc) {
           if (!mbar_wait(smem_u32(&ctl.empty[stage]), phase ^ 1, abort_flag, err)) {
             ok = false;
             break;
           }
-          const uint32_t sa = sbase + stage * LG_STAGE_BYTES, sb = sa + LG_A_BYTES;
+          const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + LG_A_BYTES;
           const uint32_t fb = smem_u32(&ctl.full[stage]);
-          mbar_arrive_expect_tx(fb, LG_STAGE_BYTES);
-          tma_load_2d(sa, &mapH, fb, kc * LG_BK, rt * LG_BM, pol_H);
-          tma_load_2d(sb, &mapE, fb, kc * LG_BK, ct * LG_BN, pol_E);
+          if constexpr (PAIR) {
+            // both CTAs' copies complete on the even CTA's barrier, which expects all of them
+            if (rank == 0) mbar_arrive_expect_tx(fb, 2 * STAGE_BYTES);
+            const uint32_t fb0 = mapa_shared(fb, 0);
+            tma_load_2d_pair(sa, &mapH, fb0, kc * LG_BK, rt * LG_BM, pol_H);
+            tma_load_2d_pair(sb, &mapE, fb0, kc * LG_BK, ct * LG_BN + (int)rank * (LG_BN / 2),
+                             pol_E);
+          } else {
+            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            tma_load_2d(sa, &mapH, fb, kc * LG_BK, rt * LG_BM, pol_H);
+            tma_load_2d(sb, &mapE, fb, kc * LG_BK, ct * LG_BN, pol_E);
+          }
           ++issued;
-          if (++stage == LG_STAGES) {
+          if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
-      if (!ok) producer_drain(ctl, issued, LG_STAGES);
+      // (pair: the odd CTA's copies complete on the even CTA's barriers, which its own
+      // producer drains)
+      if (!ok && rank == 0) producer_drain(ctl, issued, STAGES);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(LG_BM, LG_BN, false, false);
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(ROWS, LG_BN, false, false);
       int stage = 0, cc = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        const int rt = tile % n_rt;
-        if (done && done[(rt * LG_BM) / L]) continue;
+      for (int tile = unit; tile < n_tiles && ok; tile += n_units) {
+        const int it = tile % n_it;
+        if (rows_done(done, it * ROWS, ROWS, L)) continue;
         for (int ch = 0; ch < n_ch && ok; ++ch, ++cc) {
           const int buf = cc & 1;
           const uint32_t par = (uint32_t)((cc >> 1) & 1);
@@ -130,34 +186,45 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             }
             tc_fence_after();
             *(volatile int*)&ctl.consumed = ctl.consumed + 1;
-            const uint32_t sa = sbase + stage * LG_STAGE_BYTES, sb = sa + LG_A_BYTES;
+            const uint32_t sa = sbase + stage * STAGE_BYTES, sb = sa + LG_A_BYTES;
 #pragma unroll
-            for (int k = 0; k < LG_BK / 16; ++k)
-              umma_bf16(dt, sdesc_sw128(sa + 32 * k, 16, 1024),
-                        sdesc_sw128(sb + 32 * k, 16, 1024), idesc, (kc != kc0 || k) ? 1u : 0u);
-            umma_commit(smem_u32(&ctl.empty[stage]));
-            if (++stage == LG_STAGES) {
+            for (int k = 0; k < LG_BK / 16; ++k) {
+              const uint64_t ad = sdesc_sw128(sa + 32 * k, 16, 1024);
+              const uint64_t bd = sdesc_sw128(sb + 32 * k, 16, 1024);
+              const uint32_t acc_in = (kc != kc0 || k) ? 1u : 0u;
+              if constexpr (PAIR) umma_bf16_pair(dt, ad, bd, idesc, acc_in);
+              else umma_bf16(dt, ad, bd, idesc, acc_in);
+            }
+            if constexpr (PAIR) umma_commit_pair(smem_u32(&ctl.empty[stage]), 0x3);
+            else umma_commit(smem_u32(&ctl.empty[stage]));
+            if (++stage == STAGES) {
               stage = 0;
               phase ^= 1;
             }
           }
           if (!ok) break;
-          umma_commit(smem_u32(&ctl.tfull[buf]));
+          if constexpr (PAIR) umma_commit_pair(smem_u32(&ctl.tfull[buf]), 0x3);
+          else umma_commit(smem_u32(&ctl.tfull[buf]));
         }
       }
-      umma_commit(smem_u32(&ctl.mma_done));
+      if constexpr (PAIR) umma_commit_pair(smem_u32(&ctl.mma_done), 0x1);
+      else umma_commit(smem_u32(&ctl.mma_done));
       mbar_wait_quiet(smem_u32(&ctl.mma_done), 0);
     }
   } else {
     const int q = warp & 3;              // TMEM lane quadrant this warp may access
     const int half = (warp - 2) >> 2;    // column half of the tile
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    // pair: the TMEM buffers are released on the even CTA's barriers, once per warp
+    const uint32_t tempty0 = PAIR ? mapa_shared(smem_u32(&ctl.tempty[0]), 0) : 0u;
+    const uint32_t tempty1 = PAIR ? mapa_shared(smem_u32(&ctl.tempty[1]), 0) : 0u;
     int cc = 0, items = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-      const int rt = tile % n_rt, ct = tile / n_rt;
+    for (int tile = unit; tile < n_tiles && ok; tile += n_units) {
+      const int it = tile % n_it, ct = tile / n_it;
+      if (rows_done(done, it * ROWS, ROWS, L)) continue;
+      const int rt = PAIR ? 2 * it + (int)rank : it;
       const int b = (rt * LG_BM) / L;
-      if (done && done[b]) continue;
       float acc[LG_COLS];
 #pragma unroll
       for (int i = 0; i < LG_COLS; ++i) acc[i] = 0.f;
@@ -171,7 +238,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         tc_fence_after();
         tmem_accumulate<LG_COLS>(tmem + (uint32_t)(buf * LG_BN + half * LG_COLS) + lane_base, acc);
         tc_fence_before();
-        mbar_arrive(smem_u32(&ctl.tempty[buf]));
+        if constexpr (PAIR) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(buf ? tempty1 : tempty0);
+        } else {
+          mbar_arrive(smem_u32(&ctl.tempty[buf]));
+        }
       }
       if (!ok) break;
       if constexpr (STANDIN) {
@@ -215,16 +287,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       if constexpr (MODE == kOutP) {
         xmax[half][q * 32 + lane] = m;
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&xbar));
-        if (!mbar_wait(smem_u32(&xbar), (uint32_t)(items & 1), abort_flag, err)) {
+        if (lane == 0) mbar_arrive(smem_u32(&xbar[q]));
+        if (!mbar_wait(smem_u32(&xbar[q]), (uint32_t)(items & 1), abort_flag, err)) {
           ok = false;
           break;
         }
         ++items;
         m_tile = fmaxf(m, xmax[half ^ 1][q * 32 + lane]);
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&xbar));
-        if (!mbar_wait(smem_u32(&xbar), (uint32_t)(items & 1), abort_flag, err)) {
+        if (lane == 0) mbar_arrive(smem_u32(&xbar[q]));
+        if (!mbar_wait(smem_u32(&xbar[q]), (uint32_t)(items & 1), abort_flag, err)) {
           ok = false;
           break;
         }
@@ -232,10 +304,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         ptile = exp2_approx((m - m_tile) * 1.4426950408889634f);
       }
       float l = 0.f, a = 0.f;
-      const uint32_t stg = sbase + LG_STAGES * LG_STAGE_BYTES + (uint32_t)(warp - 2) * LG_STG_BYTES;
+      const uint32_t stg0 =
+          sbase + STAGES * STAGE_BYTES + (uint32_t)((warp - 2) * NSTG) * LG_STG_BYTES;
 #pragma unroll
       for (int bx = 0; bx < LG_COLS / 32; ++bx) {
-        if (lane == 0) bulk_wait_read_all();  // the previous store has read the staging box
+        const uint32_t stg = stg0 + (uint32_t)(bx % NSTG) * LG_STG_BYTES;
+        // the store issued from this box NSTG boxes ago has read it
+        if (lane == 0) {
+          if constexpr (NSTG == 2) bulk_wait_read_le1();
+          else bulk_wait_read_all();
+        }
         __syncwarp();
         if constexpr (MODE == kOutY) {
 #pragma unroll
@@ -293,37 +371,112 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // pair: neither CTA frees its TMEM or exits while the other may still use its barriers,
+  // shared memory or TMEM
+  if constexpr (PAIR) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem, 512);
+    else tmem_dealloc(tmem, 512);
   }
 }
 
 }  // namespace
 
+// Clusters of the pair kernel that can be resident at once (a TPC with an SM unavailable holds
+// none), so that no pair starts its items after the others have finished theirs.
+static int g_pairs_resident = 1;
+
 void tc_prepare_logits() {
-  cudaFuncSetAttribute(k_logits_tc<kOutY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)LG_SMEM);
-  cudaFuncSetAttribute(k_logits_tc<kOutP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)LG_SMEM);
-  cudaFuncSetAttribute(k_logits_tc<kStandin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)LG_SMEM);
+  const int smem = (int)LG_SMEM;
+  cudaFuncSetAttribute(k_logits_tc<kOutY, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaFuncSetAttribute(k_logits_tc<kOutP, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaFuncSetAttribute(k_logits_tc<kStandin, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       smem);
+  cudaFuncSetAttribute(k_logits_tc<kOutY, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)LG2_SMEM);
+  cudaFuncSetAttribute(k_logits_tc<kOutP, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)LG2_SMEM);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::max(2, sms - sms % 2));
+  cfg.blockDim = dim3(kThreadsTC);
+  cfg.dynamicSmemBytes = LG2_SMEM;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_logits_tc<kOutP, true>, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = std::max(1, sms / 2);
+  }
+  g_pairs_resident = n;
 }
+
+bool logits_pair_enabled(int R) {
+  static const bool on = [] {
+    const char* e = getenv("DS_LOGITS_PAIR");
+    return !(e && e[0] == '0');
+  }();
+  return on && R % (2 * LG_BM) == 0 && tc_num_sms() >= 2;
+}
+
+namespace {
+
+// One launch of the logits GEMM in mode MODE: one CTA per SM, or (pair) one cluster of two CTAs
+// per two SMs.
+template <int MODE>
+cudaError_t launch_logits_mode(const CUtensorMap& mH, const CUtensorMap& mE1,
+                               const CUtensorMap& mE2, const CUtensorMap& mOut,
+                               const CUtensorMap& mOut2, int R, int64_t V, int d, int L,
+                               const float* T, const uint8_t* done, ChunkStat* seg_stats,
+                               float* mseg_t, uint32_t* err, cudaStream_t st) {
+  const int n_ct = (int)(V / LG_BN);
+  if (logits_pair_enabled(R)) {
+    const int n_items = (R / (2 * LG_BM)) * n_ct;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreadsTC);
+    cfg.dynamicSmemBytes = LG2_SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int pairs = std::max(1, std::min(n_items, g_pairs_resident));
+    cfg.gridDim = dim3((unsigned)(2 * pairs));
+    return cudaLaunchKernelEx(&cfg, k_logits_tc<MODE, true>, mH, mE2, mOut, mOut2, R, V, d, L, T,
+                              done, seg_stats, mseg_t, (uint16_t*)nullptr, err);
+  }
+  const int n_tiles = (R / LG_BM) * n_ct;
+  const int grid = std::max(1, std::min(n_tiles, tc_num_sms()));
+  k_logits_tc<MODE, false><<<grid, kThreadsTC, LG_SMEM, st>>>(
+      mH, mE1, mOut, mOut2, R, V, d, L, T, done, seg_stats, mseg_t, nullptr, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
 
 cudaError_t launch_logits_tc(const uint16_t* H, const uint16_t* E, int R, int64_t V, int d, int L,
                              const float* T, const uint8_t* done, float* Y, ChunkStat* seg_stats,
                              uint32_t* err, cudaStream_t st) {
   if (!tc_available()) return cudaErrorNotSupported;
-  CUtensorMap mH, mE, mY;
+  CUtensorMap mH, mE, mE2, mY;
   if (!tc_make_map_bf16(&mH, H, (uint64_t)R, (uint64_t)d, LG_BM, LG_BK) ||
       !tc_make_map_bf16(&mE, E, (uint64_t)V, (uint64_t)d, LG_BN, LG_BK) ||
+      !tc_make_map_bf16(&mE2, E, (uint64_t)V, (uint64_t)d, LG_BN / 2, LG_BK) ||
       !tc_make_map_f32(&mY, Y, (uint64_t)R, (uint64_t)V, 32, 32))
     return cudaErrorInvalidValue;
-  const int n_tiles = (R / LG_BM) * (int)(V / LG_BN);
-  const int grid = std::max(1, std::min(n_tiles, tc_num_sms()));
-  k_logits_tc<kOutY><<<grid, kThreadsTC, LG_SMEM, st>>>(mH, mE, mY, mY, R, V, d, L, T, done,
-                                                         seg_stats, nullptr, nullptr, err);
-  return cudaGetLastError();
+  return launch_logits_mode<kOutY>(mH, mE, mE2, mY, mY, R, V, d, L, T, done, seg_stats, nullptr,
+                                   err, st);
 }
 
 cudaError_t launch_logits_p_tc(const uint16_t* H, const uint16_t* E, int R, int64_t V, int d,
@@ -331,17 +484,15 @@ cudaError_t launch_logits_p_tc(const uint16_t* H, const uint16_t* E, int R, int6
                                uint16_t* Plo, ChunkStat* seg_stats, float* mseg_t, uint32_t* err,
                                cudaStream_t st) {
   if (!tc_available()) return cudaErrorNotSupported;
-  CUtensorMap mH, mE, mPh, mPl;
+  CUtensorMap mH, mE, mE2, mPh, mPl;
   if (!tc_make_map_bf16(&mH, H, (uint64_t)R, (uint64_t)d, LG_BM, LG_BK) ||
       !tc_make_map_bf16(&mE, E, (uint64_t)V, (uint64_t)d, LG_BN, LG_BK) ||
+      !tc_make_map_bf16(&mE2, E, (uint64_t)V, (uint64_t)d, LG_BN / 2, LG_BK) ||
       !tc_make_map_bf16_sw64(&mPh, Phi, (uint64_t)R, (uint64_t)V, 32, 32) ||
       !tc_make_map_bf16_sw64(&mPl, Plo, (uint64_t)R, (uint64_t)V, 32, 32))
     return cudaErrorInvalidValue;
-  const int n_tiles = (R / LG_BM) * (int)(V / LG_BN);
-  const int grid = std::max(1, std::min(n_tiles, tc_num_sms()));
-  k_logits_tc<kOutP><<<grid, kThreadsTC, LG_SMEM, st>>>(mH, mE, mPh, mPl, R, V, d, L, T, done,
-                                                         seg_stats, mseg_t, nullptr, err);
-  return cudaGetLastError();
+  return launch_logits_mode<kOutP>(mH, mE, mE2, mPh, mPl, R, V, d, L, T, done, seg_stats, mseg_t,
+                                   err, st);
 }
 
 cudaError_t launch_standin_tc(const uint16_t* U, const uint16_t* W, int R, int d, int L,
@@ -355,7 +506,7 @@ cudaError_t launch_standin_tc(const uint16_t* U, const uint16_t* W, int R, int d
     return cudaErrorInvalidValue;
   const int n_tiles = (R / LG_BM) * (d / LG_BN);
   const int grid = std::max(1, std::min(n_tiles, tc_num_sms()));
-  k_logits_tc<kStandin><<<grid, kThreadsTC, LG_SMEM, st>>>(mU, mW, mU, mU, R, (int64_t)d, 2 * d,
+  k_logits_tc<kStandin, false><<<grid, kThreadsTC, LG_SMEM, st>>>(mU, mW, mU, mU, R, (int64_t)d, 2 * d,
                                                             L, nullptr, done, nullptr, nullptr,
                                                             H_out, err);
   return cudaGetLastError();

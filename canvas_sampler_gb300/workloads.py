@@ -75,12 +75,14 @@ BENCH_WORKLOAD = "step_bf16_b1_v262144_d2816"
 
 
 def scaled(w: Workload, *, V: int | None = None, d: int | None = None, B: int | None = None,
-           name: str | None = None) -> Workload:
+           L: int | None = None, name: str | None = None) -> Workload:
     """The same recipe at other sizes (for parity cases the oracle finishes quickly)."""
     V = w.V if V is None else V
     d = w.d if d is None else d
     B = w.B if B is None else B
-    return replace(w, V=V, d=d, B=B, name=name or f"{w.name}@B{B}_V{V}_d{d}")
+    L = w.L if L is None else L
+    tag = "" if L == w.L else f"_L{L}"
+    return replace(w, V=V, d=d, B=B, L=L, name=name or f"{w.name}@B{B}_V{V}_d{d}{tag}")
 
 
 # --------------------------------------------------------------------------------------

@@ -44,19 +44,22 @@ def test_tiny_fp32_workload_full_parity():
 
 
 CASES = [
-    # (name, base recipe, B, V, d): several tiles, several 8192-token chunks, ragged tails
-    ("peaked_v16384_d512", BASE_PEAKED, 1, 16384, 512),
-    ("peaked_ragged_v8960_d320", BASE_PEAKED, 1, 8960, 320),
-    ("batched_b3_v8192_d256", BASE_BATCH, 3, 8192, 256),
+    # (name, base recipe, B, V, d, L): several tiles, several 8192-token chunks, ragged tails;
+    # B * L % 256 == 0 runs the logits GEMM as CTA pairs (256-row tiles), else one CTA per tile
+    ("peaked_v16384_d512", BASE_PEAKED, 1, 16384, 512, 256),
+    ("peaked_ragged_v8960_d320", BASE_PEAKED, 1, 8960, 320, 256),
+    ("batched_b3_v8192_d256", BASE_BATCH, 3, 8192, 256, 256),
+    ("canvas128_b3_v8192_d512", BASE_BATCH, 3, 8192, 512, 128),
+    ("canvas128_b2_v8960_d256", BASE_BATCH, 2, 8960, 256, 128),
 ]
 
 
 @pytest.mark.parametrize("impl", ["tensor", "simt", "fused"])
-@pytest.mark.parametrize("name,base,B,V,d", CASES, ids=[c[0] for c in CASES])
-def test_step_parity(impl, name, base, B, V, d):
+@pytest.mark.parametrize("name,base,B,V,d,L", CASES, ids=[c[0] for c in CASES])
+def test_step_parity(impl, name, base, B, V, d, L):
     if impl == "fused" and d % 256:
         pytest.skip("the fused pass takes d % 256 == 0")
-    w = W.scaled(base, V=V, d=d, B=B)
+    w = W.scaled(base, V=V, d=d, B=B, L=L)
     case = GpuCase(w, impl=impl)
     assert case.sampler.impl == impl
     _, _, rep = full_step_check(case, case.state())
@@ -170,6 +173,31 @@ def test_done_sequences_are_untouched():
     assert np.all(g["sampled"][0] >= 0) and np.all(g["sampled"][2] >= 0)
     ref = oracle_step(case, pre)
     compare_outputs(g, ref, [(b, i) for b in (0, 2) for i in range(w.L)])
+
+
+@pytest.mark.parametrize("done", [(1, 0), (0, 1)])
+def test_done_sequence_inside_a_pair_tile(done):
+    # 128-token canvases: one 256-row tile of the paired logits GEMM holds both sequences, one
+    # of them finished; the live one must match the oracle and the finished one stay untouched
+    w = W.scaled(BASE_BATCH, V=8192, d=256, B=2, L=128)
+    inp = W.make_inputs(w)
+    inp["done"] = np.array(done, np.uint8)
+    case = GpuCase(w, inputs=inp)
+    state = case.state()
+    out = StepOutputs.empty(2, w.L, w.d)
+    out.s.fill_(-7.0)
+    out.sampled.fill_(-7)
+    pre = state_np(state)
+    case.sampler.step(case.H, case.E, case.T, case.tau, state, inp["seed"], out=out)
+    torch.cuda.synchronize()
+    post = state_np(state)
+    dead, live = (0, 1) if done[0] else (1, 0)
+    for k in pre:
+        assert np.array_equal(post[k][dead], pre[k][dead])
+    g = out_np(out)
+    assert np.all(g["s"][dead] == -7.0) and np.all(g["sampled"][dead] == -7)
+    ref = oracle_step(case, pre)
+    compare_outputs(g, ref, [(live, i) for i in range(w.L)])
 
 
 def test_deterministic_bits():
