@@ -218,18 +218,30 @@ __global__ void __launch_bounds__(kThreads) k_row_merge(const ChunkStat* __restr
       }
   }
   block_best(m, arg, dummy_y, shv, shj, &shy);
-  double l = 0.0, a = 0.0;
+  // l = sum_g l_g e^{m_g - m} and a = sum_g (a_g + l_g (m_g - m)) e^{m_g - m}: every term has one
+  // sign (l_g > 0, a_g <= 0, m_g <= m), so there is no cancellation; each thread sums its terms
+  // in fp32 with a compensation term (Kahan), the warps by a shuffle tree and the block's eight
+  // warp sums in fp64, a relative error of a few fp32 units
+  float l = 0.f, a = 0.f, cl = 0.f, ca = 0.f;
+  auto kahan = [](float& sum, float& comp, float x) {
+    const float y = x - comp;
+    const float t = sum + y;
+    comp = (t - sum) - y;
+    sum = t;
+  };
   for (int base = 0; base < n_chunks; base += kThreads * kPer) {
     if (base > 0 || n_chunks > kThreads * kPer) load_batch(base, mine);
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       if (mine[k].arg == INT_MAX) continue;
       const float dm = mine[k].m - m;
-      const double sc = (double)expf(dm);
-      l += (double)mine[k].l * sc;
-      a += ((double)mine[k].a + (double)mine[k].l * (double)dm) * sc;
+      const float sc = expf(dm);
+      kahan(l, cl, mine[k].l * sc);
+      kahan(a, ca, fmaf(mine[k].l, dm, mine[k].a) * sc);
     }
   }
+  l -= cl;
+  a -= ca;
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
     l += __shfl_xor_sync(0xffffffffu, l, o);
@@ -237,8 +249,8 @@ __global__ void __launch_bounds__(kThreads) k_row_merge(const ChunkStat* __restr
   }
   const int w = threadIdx.x >> 5, ln = threadIdx.x & 31;
   if (ln == 0) {
-    shd[0][w] = l;
-    shd[1][w] = a;
+    shd[0][w] = (double)l;
+    shd[1][w] = (double)a;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
