@@ -74,6 +74,7 @@ struct ds_sampler {
   // device staging for ds_sampler_step_host (allocated on first use)
   void* stage = nullptr;
   size_t stage_bytes = 0;
+  void* hstage = nullptr;  // pinned host mirror of the small per-step buffers
   cudaStream_t capture_stream = nullptr;
   std::vector<LoopGraph> graphs;
   std::vector<BlockGraph> block_graphs;
@@ -312,6 +313,8 @@ void free_all(ds_sampler* s) {
   s->allocations.clear();
   if (s->stage) cudaFree(s->stage);
   s->stage = nullptr;
+  if (s->hstage) cudaFreeHost(s->hstage);
+  s->hstage = nullptr;
   if (s->capture_stream) cudaStreamDestroy(s->capture_stream);
   s->capture_stream = nullptr;
 }
@@ -483,12 +486,29 @@ ds_status ds_sampler_step_host(ds_sampler* s, const ds_step_args* h, void* strea
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t B = (size_t)h->batch, L = (size_t)s->cfg.canvas_len, d = (size_t)s->cfg.d_model;
   const size_t Bm = (size_t)s->cfg.max_batch;
+  const size_t es = esize(s->cfg.dtype);
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
-  // staging layout for max_batch: H | s | T | tau | step | canvas | lock | done | sampled | conf
-  // | entropy | argmax | prev_argmax
-  const size_t nH = up(Bm * L * d * esize(s->cfg.dtype)), nS = up(Bm * L * d * 4);
-  const size_t nB4 = up(Bm * 4), nBL4 = up(Bm * L * 4), nBL1 = up(Bm * L), nB1 = up(Bm);
-  const size_t total = nH + nS + 3 * nB4 + nBL4 + nBL1 + nB1 + 5 * nBL4;
+  auto up16 = [](size_t x) { return (x + 15) & ~size_t(15); };
+  // The small per-step buffers travel as one block, mirrored in pinned host memory: [T | tau |
+  // step | canvas | lock | done | prev_argmax | sampled | conf | entropy | argmax] laid out for
+  // this batch. The inputs go in with one copy (T .. prev_argmax), the updated state and the
+  // outputs come back with one (step .. argmax); H and s move directly between the caller's
+  // buffers and the device. Four copies a step instead of one per buffer.
+  size_t o = 0;
+  auto seg = [&](size_t n) {
+    const size_t at = o;
+    o += up16(n);
+    return at;
+  };
+  const size_t oT = seg(B * 4), otau = seg(B * 4), ostep = seg(B * 4), ocanvas = seg(B * L * 4),
+               olock = seg(B * L), odone = seg(B), oprev = seg(h->prev_argmax ? B * L * 4 : 0),
+               osampled = seg(B * L * 4), oconf = seg(B * L * 4), oent = seg(B * L * 4),
+               oarg = seg(B * L * 4);
+  const size_t oend = o;
+  // block size at max_batch (the largest any call needs)
+  const size_t nblock = up(9 * up16(Bm * L * 4) + 4 * up16(Bm * 4) + up16(Bm * L) + up16(Bm));
+  const size_t nH = up(Bm * L * d * es), nS = up(Bm * L * d * 4);
+  const size_t total = nH + nS + nblock;
   if (!s->stage) {
     cudaError_t e = cudaMalloc(&s->stage, total);
     if (e != cudaSuccess) {
@@ -497,57 +517,63 @@ ds_status ds_sampler_step_host(ds_sampler* s, const ds_step_args* h, void* strea
     }
     s->stage_bytes = total;
   }
-  uint8_t* p = static_cast<uint8_t*>(s->stage);
+  if (!s->hstage) {
+    cudaError_t e = cudaMallocHost(&s->hstage, nblock);
+    if (e != cudaSuccess) {
+      s->hstage = nullptr;
+      return cuda_status(e);
+    }
+  }
+  uint8_t* dev = static_cast<uint8_t*>(s->stage);
+  uint8_t* blk_d = dev + nH + nS;
+  uint8_t* blk_h = static_cast<uint8_t*>(s->hstage);
+  std::memcpy(blk_h + oT, h->temperature, B * 4);
+  std::memcpy(blk_h + otau, h->tau, B * 4);
+  std::memcpy(blk_h + ostep, h->step, B * 4);
+  std::memcpy(blk_h + ocanvas, h->canvas, B * L * 4);
+  std::memcpy(blk_h + olock, h->lock, B * L);
+  std::memcpy(blk_h + odone, h->done, B);
+  if (h->prev_argmax) std::memcpy(blk_h + oprev, h->prev_argmax, B * L * 4);
   ds_step_args a{};
   a.batch = h->batch;
   a.seed = h->seed;
   a.E = h->E;
-  a.H = p; p += nH;
-  a.s = reinterpret_cast<float*>(p); p += nS;
-  a.temperature = reinterpret_cast<const float*>(p); p += nB4;
-  a.tau = reinterpret_cast<const float*>(p); p += nB4;
-  a.step = reinterpret_cast<int32_t*>(p); p += nB4;
-  a.canvas = reinterpret_cast<int32_t*>(p); p += nBL4;
-  a.lock = p; p += nBL1;
-  a.done = p; p += nB1;
-  a.sampled = reinterpret_cast<int32_t*>(p); p += nBL4;
-  a.conf = reinterpret_cast<float*>(p); p += nBL4;
-  a.entropy = reinterpret_cast<float*>(p); p += nBL4;
-  a.argmax = reinterpret_cast<int32_t*>(p); p += nBL4;
-  a.prev_argmax = h->prev_argmax ? reinterpret_cast<int32_t*>(p) : nullptr; p += nBL4;
-  cudaError_t e = cudaSuccess;
-  auto h2d = [&](const void* dst, const void* src, size_t n) {
-    if (e == cudaSuccess)
-      e = cudaMemcpyAsync(const_cast<void*>(dst), src, n, cudaMemcpyHostToDevice, st);
-  };
-  auto d2h = [&](void* dst, const void* src, size_t n) {
-    if (e == cudaSuccess) e = cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToHost, st);
-  };
-  h2d(a.H, h->H, B * L * d * esize(s->cfg.dtype));
-  h2d(a.temperature, h->temperature, B * 4);
-  h2d(a.tau, h->tau, B * 4);
-  h2d(a.step, h->step, B * 4);
-  h2d(a.canvas, h->canvas, B * L * 4);
-  h2d(a.lock, h->lock, B * L);
-  h2d(a.done, h->done, B);
-  if (a.prev_argmax) h2d(a.prev_argmax, h->prev_argmax, B * L * 4);
+  a.H = dev;
+  a.s = reinterpret_cast<float*>(dev + nH);
+  a.temperature = reinterpret_cast<const float*>(blk_d + oT);
+  a.tau = reinterpret_cast<const float*>(blk_d + otau);
+  a.step = reinterpret_cast<int32_t*>(blk_d + ostep);
+  a.canvas = reinterpret_cast<int32_t*>(blk_d + ocanvas);
+  a.lock = blk_d + olock;
+  a.done = blk_d + odone;
+  a.prev_argmax = h->prev_argmax ? reinterpret_cast<int32_t*>(blk_d + oprev) : nullptr;
+  a.sampled = reinterpret_cast<int32_t*>(blk_d + osampled);
+  a.conf = reinterpret_cast<float*>(blk_d + oconf);
+  a.entropy = reinterpret_cast<float*>(blk_d + oent);
+  a.argmax = reinterpret_cast<int32_t*>(blk_d + oarg);
+  cudaError_t e = cudaMemcpyAsync(dev, h->H, B * L * d * es, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(blk_d, blk_h, osampled, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return cuda_status(e);
   ds_status r = check_step_args(s, &a);
   if (r != DS_OK) return r;
   r = enqueue_step(s, &a, st);
   if (r != DS_OK) return r;
-  d2h(h->s, a.s, B * L * d * 4);
-  d2h(h->sampled, a.sampled, B * L * 4);
-  d2h(h->conf, a.conf, B * L * 4);
-  d2h(h->entropy, a.entropy, B * L * 4);
-  d2h(h->argmax, a.argmax, B * L * 4);
-  d2h(h->step, a.step, B * 4);
-  d2h(h->canvas, a.canvas, B * L * 4);
-  d2h(h->lock, a.lock, B * L);
-  d2h(h->done, a.done, B);
-  if (a.prev_argmax) d2h(h->prev_argmax, a.prev_argmax, B * L * 4);
+  e = cudaMemcpyAsync(h->s, a.s, B * L * d * 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(blk_h + ostep, blk_d + ostep, oend - ostep, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-  return cuda_status(e);
+  if (e != cudaSuccess) return cuda_status(e);
+  std::memcpy(h->step, blk_h + ostep, B * 4);
+  std::memcpy(h->canvas, blk_h + ocanvas, B * L * 4);
+  std::memcpy(h->lock, blk_h + olock, B * L);
+  std::memcpy(h->done, blk_h + odone, B);
+  if (h->prev_argmax) std::memcpy(h->prev_argmax, blk_h + oprev, B * L * 4);
+  std::memcpy(h->sampled, blk_h + osampled, B * L * 4);
+  std::memcpy(h->conf, blk_h + oconf, B * L * 4);
+  std::memcpy(h->entropy, blk_h + oent, B * L * 4);
+  std::memcpy(h->argmax, blk_h + oarg, B * L * 4);
+  return DS_OK;
 }
 
 ds_status ds_standin_hidden(ds_sampler* s, const void* W, const float* s_prev, const void* E,
