@@ -12,6 +12,7 @@
 #include <climits>
 
 #include "ds_internal.h"
+#include "ds_sample.cuh"
 
 namespace ds {
 
