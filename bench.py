@@ -372,6 +372,16 @@ def run_ours(args):
         roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": ach / peak_tf, "traffic": traffic,
                 "peak_source": f"{peak_key} ({peak_src})"}
+    # the vocabulary pass (both GEMMs with the epilogues fused into them: the logits and
+    # self-conditioning phases, or the fused kernel) against the tensor roofline of its
+    # 4 B L V d algorithmic FLOP; the bf16 hi/lo split makes its tensor work 6 B L V d, so no
+    # schedule exceeds 2/3 of it
+    vp_ms = (phases.get("logits", 0.0) + phases.get("selfcond", 0.0)) / max(1, nsteps)
+    vp = None
+    if vp_ms > 0:
+        vp_ach = 4.0 * w.B * w.L * w.V * w.d / (vp_ms / 1e3) / 1e12
+        vp = {"bound": "tensor", "ms": vp_ms, "achieved": vp_ach, "peak": peak_tf,
+              "unit": "TFLOP/s", "frac": vp_ach / peak_tf, "frac_cap": 2.0 / 3.0}
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
@@ -387,6 +397,7 @@ def run_ours(args):
                           "note": "4 B L V d algorithmic FLOP per step over the whole step, "
                                   f"against {peak_key}"},
         "roofline": roof,
+        "vocab_pass_roofline": vp,
         "phase_ms_per_step": {k: v / max(1, nsteps) for k, v in phases.items()},
         "gpu_launches": launches,
         "e2e": {"value": world * args.e2e_steps / e2e_s, "unit": "steps/s",
