@@ -366,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_convert(const float* __restrict
 // cannot hold the winner and is skipped without reading its probabilities. The winner's y - m is
 // returned as ln p_j (p_j carries ~17 significant bits: hi + lo is exact in fp32), with
 // Best::rel = 1.
-__global__ void __launch_bounds__(kThreads, 3) k_gumbel_seg(
+__global__ void __launch_bounds__(kThreads, 4) k_gumbel_seg(
     const uint16_t* __restrict__ Phi, const uint16_t* __restrict__ Plo,
     const ChunkStat* __restrict__ seg, const RowStat* __restrict__ rs, int64_t V, int L,
     const uint8_t* __restrict__ done, const int32_t* __restrict__ step, uint64_t seed,
