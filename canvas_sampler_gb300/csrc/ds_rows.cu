@@ -365,7 +365,8 @@ __global__ void __launch_bounds__(kThreads, 4) k_convert(const float* __restrict
 // segment pair) and m the row maximum. A segment whose maximum is more than kGumbelReach below m
 // cannot hold the winner and is skipped without reading its probabilities. The winner's y - m is
 // returned as ln p_j (p_j carries ~17 significant bits: hi + lo is exact in fp32), with
-// Best::rel = 1.
+// Best::rel = 1. Latency-bound (fixed-latency dependences of the Philox rounds): four CTAs per SM
+// (64 registers) measured faster than three (80) or five (48).
 __global__ void __launch_bounds__(kThreads, 4) k_gumbel_seg(
     const uint16_t* __restrict__ Phi, const uint16_t* __restrict__ Plo,
     const ChunkStat* __restrict__ seg, const RowStat* __restrict__ rs, int64_t V, int L,
