@@ -559,7 +559,23 @@ ds_status ds_sampler_step_host(ds_sampler* s, const ds_step_args* h, void* strea
   if (r != DS_OK) return r;
   r = enqueue_step(s, &a, st);
   if (r != DS_OK) return r;
-  e = cudaMemcpyAsync(h->s, a.s, B * L * d * 4, cudaMemcpyDeviceToHost, st);
+  // Like the device entry point, the outputs of sequences that were done before the step are
+  // left as the caller had them: s comes back for each run of consecutive live sequences (one
+  // copy when all are live), the small outputs row by row from the staging mirror.
+  const uint8_t* done_in = blk_h + odone;  // the flags as they were before the step
+  for (size_t b0 = 0; b0 < B && e == cudaSuccess;) {
+    if (done_in[b0]) {
+      ++b0;
+      continue;
+    }
+    size_t b1 = b0;
+    while (b1 < B && !done_in[b1]) ++b1;
+    e = cudaMemcpyAsync(h->s + b0 * L * d, a.s + b0 * L * d, (b1 - b0) * L * d * 4,
+                        cudaMemcpyDeviceToHost, st);
+    b0 = b1;
+  }
+  std::vector<uint8_t> live(B);
+  for (size_t b = 0; b < B; ++b) live[b] = !done_in[b];
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(blk_h + ostep, blk_d + ostep, oend - ostep, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
@@ -569,10 +585,13 @@ ds_status ds_sampler_step_host(ds_sampler* s, const ds_step_args* h, void* strea
   std::memcpy(h->lock, blk_h + olock, B * L);
   std::memcpy(h->done, blk_h + odone, B);
   if (h->prev_argmax) std::memcpy(h->prev_argmax, blk_h + oprev, B * L * 4);
-  std::memcpy(h->sampled, blk_h + osampled, B * L * 4);
-  std::memcpy(h->conf, blk_h + oconf, B * L * 4);
-  std::memcpy(h->entropy, blk_h + oent, B * L * 4);
-  std::memcpy(h->argmax, blk_h + oarg, B * L * 4);
+  for (size_t b = 0; b < B; ++b) {
+    if (!live[b]) continue;
+    std::memcpy(h->sampled + b * L, blk_h + osampled + b * L * 4, L * 4);
+    std::memcpy(h->conf + b * L, blk_h + oconf + b * L * 4, L * 4);
+    std::memcpy(h->entropy + b * L, blk_h + oent + b * L * 4, L * 4);
+    std::memcpy(h->argmax + b * L, blk_h + oarg + b * L * 4, L * 4);
+  }
   return DS_OK;
 }
 

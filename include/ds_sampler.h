@@ -223,7 +223,11 @@ ds_status ds_sampler_step(ds_sampler* sampler, const ds_step_args* args, void* s
 
 /* The same step with every per-step buffer in [host] memory (page-locked memory gives
  * asynchronous copies) and only E on the device: copies the inputs in, runs the step, copies
- * the outputs and the updated state back, and synchronises `stream` before returning. */
+ * the outputs and the updated state back, and synchronises `stream` before returning. As with
+ * ds_sampler_step, the outputs (s, sampled, conf, entropy, argmax) of sequences with done == 1
+ * on entry are left as the caller had them. Uses a device staging area and a page-locked host
+ * staging block of the sampler (allocated on the first call), so calls on one sampler must not
+ * overlap. */
 ds_status ds_sampler_step_host(ds_sampler* sampler, const ds_step_args* host_args, void* stream);
 
 /* Enqueue a denoising loop on `stream` (see ds_loop_args). */
