@@ -306,7 +306,10 @@ def run_ours(args):
     clocks.start()
     time.sleep(0.3)
     launches0 = sampler.launch_count
-    sampler.set_phase_timing(True)
+    # coarse phase events inside the timed region (ends of the logits, up-to-self-conditioning,
+    # self-conditioning and final phases): enough for both GEMMs' live durations, with fewer
+    # events between the step's kernels
+    sampler.set_phase_timing(True, coarse=True)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     ev0.record(stream)
@@ -321,6 +324,12 @@ def run_ours(args):
     sampler.set_phase_timing(False)
     launches = sampler.launch_count - launches0
     clk = clocks.stop()
+    # every phase, on a short untimed pass after the timed region (informational breakdown)
+    sampler.set_phase_timing(True)
+    for _ in range(min(args.steps, 20)):
+        one_step()
+    breakdown, nbd = sampler.phase_times()
+    sampler.set_phase_timing(False)
     ms = reduce_max(ms, dist if world > 1 else None, dev)
     status = sampler.device_status()
 
@@ -353,7 +362,7 @@ def run_ours(args):
     # algorithmic FLOP per launch; the phase named "logits" spans it, the convert and selfcond
     # phases are empty), or on the unfused path the self-conditioning GEMM (2 B L V d). The bf16
     # hi/lo doubling of the self-conditioning tensor work is not algorithmic.
-    fused = nsteps > 0 and phases.get("selfcond", 0.0) == 0.0 and phases.get("convert", 0.0) == 0.0
+    fused = sampler.impl == "fused"
     dom = max(phases, key=phases.get) if nsteps else "selfcond"
     dom_ms = phases.get(dom, 0.0) / max(1, nsteps)
     if fused and dom == "logits":
@@ -399,6 +408,7 @@ def run_ours(args):
         "roofline": roof,
         "vocab_pass_roofline": vp,
         "phase_ms_per_step": {k: v / max(1, nsteps) for k, v in phases.items()},
+        "phase_breakdown_ms_per_step": {k: v / max(1, nbd) for k, v in breakdown.items()},
         "gpu_launches": launches,
         "e2e": {"value": world * args.e2e_steps / e2e_s, "unit": "steps/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},

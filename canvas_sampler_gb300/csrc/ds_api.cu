@@ -83,7 +83,7 @@ struct ds_sampler {
   int32_t* blk = nullptr;
   std::vector<void*> allocations;
   // phase timing (ds_sampler_set_phase_timing)
-  bool timing = false;
+  int timing = 0;  // 0 off, 1 every phase, 2 the coarse boundaries only (coarse_phase)
   std::vector<cudaEvent_t> events;  // kPhaseEvents per timed step
   int timed_steps = 0;
   cudaStream_t timed_stream = nullptr;
@@ -97,13 +97,20 @@ constexpr int kPhaseEvents = kPhases + 1;
 
 // Event marking the end of `phase` (or the start of the step for phase -1) in the current
 // timed step; nullptr when timing is off.
+// Phases whose end is marked in coarse timing: the logits GEMM, everything up to the
+// self-conditioning GEMM, the GEMM itself, and everything after it (fewer events between the
+// kernels of a step: an event between two kernels costs more than its own record, since the
+// second kernel can no longer be launched as the first retires).
+bool coarse_phase(int phase) { return phase == 0 || phase == 3 || phase == 4 || phase == 6; }
+
 void mark(ds_sampler* s, int phase, cudaStream_t st) {
   if (!s->timing) return;
+  if (s->timing == 2 && phase >= 0 && !coarse_phase(phase)) return;
   const size_t need = (size_t)(s->timed_steps + 1) * kPhaseEvents;
   while (s->events.size() < need) {
     cudaEvent_t e;
     if (cudaEventCreate(&e) != cudaSuccess) {
-      s->timing = false;
+      s->timing = 0;
       return;
     }
     s->events.push_back(e);
@@ -624,11 +631,11 @@ ds_status ds_denoise_loop(ds_sampler* s, const ds_loop_args* a, void* stream) {
     }
     return DS_OK;
   }
-  const bool was_timing = s->timing;
-  s->timing = false;
+  const int was_timing = s->timing;
+  s->timing = 0;
   struct Restore {
     ds_sampler* s;
-    bool v;
+    int v;
     ~Restore() { s->timing = v; }
   } restore{s, was_timing};
   LoopGraph* g = nullptr;
@@ -729,11 +736,11 @@ ds_status ds_block_loop(ds_sampler* s, const ds_block_args* a, void* stream) {
     }
     return finish(st);
   }
-  const bool was_timing = s->timing;
-  s->timing = false;
+  const int was_timing = s->timing;
+  s->timing = 0;
   struct Restore {
     ds_sampler* s;
-    bool v;
+    int v;
     ~Restore() { s->timing = v; }
   } restore{s, was_timing};
   BlockGraph* g = nullptr;
@@ -826,7 +833,8 @@ ds_status ds_philox4x32_10(const uint32_t* ctr, uint64_t seed, uint32_t* out, in
 
 ds_status ds_sampler_set_phase_timing(ds_sampler* s, int32_t enable) {
   if (!s) return DS_ERR_INVALID_ARG;
-  s->timing = enable != 0;
+  if (enable < 0 || enable > 2) return DS_ERR_INVALID_ARG;
+  s->timing = enable;
   s->timed_steps = 0;
   return DS_OK;
 }
@@ -837,13 +845,18 @@ ds_status ds_sampler_phase_times(ds_sampler* s, float* ms, int32_t n, int32_t* s
   if (s->timed_steps > 0) {
     cudaError_t e = cudaStreamSynchronize(s->timed_stream);
     if (e != cudaSuccess) return DS_ERR_CUDA;
-    for (int t = 0; t < s->timed_steps; ++t)
+    for (int t = 0; t < s->timed_steps; ++t) {
+      // each recorded phase end, from the previous recorded event (the step's start first)
+      const size_t base = (size_t)t * kPhaseEvents;
+      size_t prev = base;
       for (int p = 0; p < kPhases; ++p) {
+        if (s->timing == 2 && !coarse_phase(p)) continue;
         float x = 0.f;
-        const size_t base = (size_t)t * kPhaseEvents;
-        if (cudaEventElapsedTime(&x, s->events[base + p], s->events[base + p + 1]) == cudaSuccess)
+        if (cudaEventElapsedTime(&x, s->events[prev], s->events[base + p + 1]) == cudaSuccess)
           acc[p] += x;
+        prev = base + p + 1;
       }
+    }
   }
   for (int p = 0; p < n && p < kPhases; ++p) ms[p] = (float)acc[p];
   if (steps) *steps = s->timed_steps;

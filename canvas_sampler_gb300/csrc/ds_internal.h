@@ -20,6 +20,28 @@ constexpr int kMaxTopKPool = 8192;
 
 inline int n_chunks_of(int64_t V) { return (int)((V + kChunk - 1) / kChunk); }
 
+// Whether kernels of a step are launched with programmatic stream serialisation (each may start
+// while its predecessor finishes; it waits in-kernel before using the predecessor's results).
+// On unless DS_PDL=0 in the environment.
+bool pdl_enabled();
+
+// Launch `kernel` on `st`, with programmatic stream serialisation when pdl_enabled().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---- row kernels (ds_rows.cu) ----
 void launch_chunk_stats(const float* Y, int R, int64_t V, int L, const uint8_t* done,
                         ChunkStat* cs, cudaStream_t st);

@@ -196,6 +196,7 @@ __global__ void __launch_bounds__(kThreads) k_row_merge(const ChunkStat* __restr
   __shared__ float shv[32], shy;
   __shared__ int32_t shj[32];
   __shared__ double shd[2][32];
+  pdl_wait();
   const int r = blockIdx.x;
   if (done && done[r / L]) return;
   const ChunkStat* c = cs + (size_t)r * n_chunks;
@@ -377,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_gumbel_seg(
   __shared__ float sh_scale[kChunk / kSegTok];
   __shared__ float shv[32], shy;
   __shared__ int32_t shj[32];
+  pdl_wait();
   const int c = blockIdx.x, r = blockIdx.y;
   const int b = r / L, i = r % L;
   if (done && done[b]) return;
@@ -490,6 +492,7 @@ __global__ void __launch_bounds__(kThreads) k_finalize(
   __shared__ int scan_sh[32];
   __shared__ float sel_y[kMaxTopK];
   __shared__ int32_t sel_j[kMaxTopK];
+  pdl_wait();
   const int r = blockIdx.x;
   const int b = r / L, i = r % L;
   if (done && done[b]) return;
@@ -618,6 +621,7 @@ __global__ void k_lock(int L, uint32_t V, int max_steps, uint64_t seed, const in
                        uint8_t* __restrict__ done) {
   __shared__ float shv[32];
   __shared__ int32_t shj[32];
+  pdl_wait();
   const int b = blockIdx.x, i = threadIdx.x;
   if (done[b]) return;
   const int st = step[b];
@@ -940,7 +944,7 @@ void launch_chunk_stats(const float* Y, int R, int64_t V, int L, const uint8_t* 
 
 void launch_row_merge(const ChunkStat* cs, int n_chunks, int R, int L, const uint8_t* done,
                       RowStat* rs, cudaStream_t st) {
-  k_row_merge<<<R, kThreads, 0, st>>>(cs, n_chunks, L, done, rs);
+  launch_k(k_row_merge, dim3(R), dim3(kThreads), 0, st, cs, n_chunks, L, done, rs);
 }
 
 void launch_convert(const float* Y, const RowStat* rs, int R, int64_t V, int L,
@@ -962,9 +966,8 @@ void launch_finalize(const RowStat* rs, const Best* best, const Cand* cand, int 
                      int R, int L, const uint8_t* done, const int32_t* step, uint64_t seed,
                      const int32_t* blk, int32_t* sampled, float* conf, float* entropy,
                      int32_t* argmax, cudaStream_t st) {
-  k_finalize<<<R, kThreads, 0, st>>>(rs, best, cand, n_chunks, k, L, done, step, seed, blk,
-                                     sampled, conf, entropy, argmax, nullptr, 0, R, 0, nullptr,
-                                     nullptr);
+  launch_k(k_finalize, dim3(R), dim3(kThreads), 0, st, rs, best, cand, n_chunks, k, L, done, step,
+           seed, blk, sampled, conf, entropy, argmax, nullptr, 0, R, 0, nullptr, nullptr);
 }
 
 void launch_finalize_with_s(const RowStat* rs, const Best* best, const Cand* cand, int n_chunks,
@@ -972,8 +975,8 @@ void launch_finalize_with_s(const RowStat* rs, const Best* best, const Cand* can
                             uint64_t seed, const int32_t* blk, int32_t* sampled, float* conf,
                             float* entropy, int32_t* argmax, const float* Opart, int S, int d,
                             float* s, const float* mref, cudaStream_t st) {
-  k_finalize<<<R, kThreads, 0, st>>>(rs, best, cand, n_chunks, k, L, done, step, seed, blk,
-                                     sampled, conf, entropy, argmax, Opart, S, R, d, s, mref);
+  launch_k(k_finalize, dim3(R), dim3(kThreads), 0, st, rs, best, cand, n_chunks, k, L, done, step,
+           seed, blk, sampled, conf, entropy, argmax, Opart, S, R, d, s, mref);
 }
 
 void launch_gumbel_seg(const uint16_t* Phi, const uint16_t* Plo, const ChunkStat* seg,
@@ -981,8 +984,8 @@ void launch_gumbel_seg(const uint16_t* Phi, const uint16_t* Plo, const ChunkStat
                        const int32_t* step, uint64_t seed, const int32_t* blk, bool tile_ref,
                        Best* best, cudaStream_t st) {
   const int nc = n_chunks_of(V);
-  k_gumbel_seg<<<dim3(nc, R), kThreads, 0, st>>>(Phi, Plo, seg, rs, V, L, done, step, seed, blk,
-                                                 tile_ref ? 1 : 0, best, nc);
+  launch_k(k_gumbel_seg, dim3(nc, R), dim3(kThreads), 0, st, Phi, Plo, seg, rs, V, L, done, step,
+           seed, blk, tile_ref ? 1 : 0, best, nc);
 }
 
 void launch_reduce_s(const float* Opart, int S, int R, int d, int L, const uint8_t* done,
@@ -995,8 +998,8 @@ void launch_reduce_s(const float* Opart, int S, int R, int d, int L, const uint8
 void launch_lock(int B, int L, int64_t V, int max_steps, uint64_t seed, const int32_t* blk,
                  const float* tau, const int32_t* sampled, const float* conf, int32_t* step,
                  int32_t* canvas, uint8_t* lock, uint8_t* done, cudaStream_t st) {
-  k_lock<<<B, L, 0, st>>>(L, (uint32_t)V, max_steps, seed, blk, tau, sampled, conf, step, canvas,
-                          lock, done);
+  launch_k(k_lock, dim3(B), dim3(L), 0, st, L, (uint32_t)V, max_steps, seed, blk, tau, sampled,
+           conf, step, canvas, lock, done);
 }
 
 void launch_philox(const uint32_t* ctr, uint64_t seed, uint32_t* out, int64_t n, cudaStream_t st) {

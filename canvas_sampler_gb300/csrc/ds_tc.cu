@@ -2,6 +2,7 @@
 // count, and 2-D tensor maps over row-major arrays.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "ds_internal.h"
@@ -42,6 +43,14 @@ bool encode(CUtensorMap* map, CUtensorMapDataType type, uint32_t esize, const vo
 }
 
 }  // namespace
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("DS_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
 
 bool tc_available() {
   std::call_once(g_once, resolve);

@@ -119,6 +119,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
   volatile int* abort_flag = &ctl.abort;
+  // the setup above is local; H, T and done may still be being written by the kernel before
+  pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -444,13 +446,15 @@ cudaError_t launch_logits_mode(const CUtensorMap& mH, const CUtensorMap& mE1,
     cfg.blockDim = dim3(kThreadsTC);
     cfg.dynamicSmemBytes = LG2_SMEM;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
     const int pairs = std::max(1, std::min(n_items, g_pairs_resident));
     cfg.gridDim = dim3((unsigned)(2 * pairs));
     return cudaLaunchKernelEx(&cfg, k_logits_tc<MODE, true>, mH, mE2, mOut, mOut2, R, V, d, L, T,
@@ -458,9 +462,8 @@ cudaError_t launch_logits_mode(const CUtensorMap& mH, const CUtensorMap& mE1,
   }
   const int n_tiles = (R / LG_BM) * n_ct;
   const int grid = std::max(1, std::min(n_tiles, tc_num_sms()));
-  k_logits_tc<MODE, false><<<grid, kThreadsTC, LG_SMEM, st>>>(
-      mH, mE1, mOut, mOut2, R, V, d, L, T, done, seg_stats, mseg_t, nullptr, err);
-  return cudaGetLastError();
+  return launch_k(k_logits_tc<MODE, false>, dim3(grid), dim3(kThreadsTC), LG_SMEM, st, mH, mE1,
+                  mOut, mOut2, R, V, d, L, T, done, seg_stats, mseg_t, (uint16_t*)nullptr, err);
 }
 
 }  // namespace

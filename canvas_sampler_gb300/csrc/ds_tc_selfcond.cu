@@ -63,6 +63,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
   volatile int* abort_flag = &ctl.abort;
+  // the setup above is local; P, the tile maxima and done come from the kernels before
+  pdl_wait();
 
   auto item_coords = [&](int w, int& split, int& rt, int& dt, int& kb0, int& kb1) {
     split = w / n_tiles;
@@ -277,9 +279,10 @@ cudaError_t launch_selfcond_tc(const uint16_t* Phi, const uint16_t* Plo, const u
   if (scaled) per = (per + SC_CHUNK_KB - 1) / SC_CHUNK_KB * SC_CHUNK_KB;  // splits start on a tile
   const int n_items = (R / SC_BM) * (d / bn) * S;
   const int grid = std::max(1, std::min(n_items, tc_num_sms()));
-#define DS_SELFCOND_LAUNCH(BN, SC)                                                           \
-  k_selfcond_tc<BN, SC><<<grid, kThreadsTC, SC_SMEM, st>>>(mPh, mPl, mE, R, V, d, L, S, per, \
-                                                           done, Opart, mtile_t, mref, err)
+  cudaError_t e = cudaSuccess;
+#define DS_SELFCOND_LAUNCH(BN, SC)                                                             \
+  e = launch_k(k_selfcond_tc<BN, SC>, dim3(grid), dim3(kThreadsTC), SC_SMEM, st, mPh, mPl, mE, \
+               R, V, d, L, S, per, done, Opart, mtile_t, mref, err)
   if (scaled) {
     if (bn == 256)
       DS_SELFCOND_LAUNCH(256, true);
@@ -296,7 +299,7 @@ cudaError_t launch_selfcond_tc(const uint16_t* Phi, const uint16_t* Plo, const u
       DS_SELFCOND_LAUNCH(64, false);
   }
 #undef DS_SELFCOND_LAUNCH
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace ds

@@ -225,9 +225,11 @@ class Sampler:
                 "ds_standin_hidden")
         return H_out
 
-    def set_phase_timing(self, enable: bool) -> None:
-        C.check(self.lib.ds_sampler_set_phase_timing(self.handle, 1 if enable else 0),
-                "set_phase_timing")
+    def set_phase_timing(self, enable: bool, coarse: bool = False) -> None:
+        """Per-phase CUDA-event timing of each step (coarse: only the ends of the logits,
+        up-to-self-conditioning, self-conditioning and final phases are marked)."""
+        level = 0 if not enable else (2 if coarse else 1)
+        C.check(self.lib.ds_sampler_set_phase_timing(self.handle, level), "set_phase_timing")
 
     def phase_times(self) -> tuple[dict, int]:
         """Accumulated milliseconds per phase since timing was enabled, and the step count."""

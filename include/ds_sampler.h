@@ -252,13 +252,16 @@ ds_status ds_sampler_device_status(ds_sampler* sampler, ds_status* out);
 ds_status ds_philox4x32_10(const uint32_t* ctr, uint64_t seed, uint32_t* out, int64_t n,
                            void* stream);
 
-/* Per-phase device timing of ds_sampler_step, for profiling. While enabled, every step records
+/* Per-phase device timing of ds_sampler_step, for profiling. enable = 1: every step records
  * CUDA events on its stream around each phase and accumulates the elapsed times:
  *   0 logits GEMM, 1 softmax statistics, 2 top-k candidates, 3 exp(y - m) split + Gumbel-max,
  *   4 self-conditioning GEMM, 5 reduction of s + finalize, 6 lock / re-noise / stop.
- * ds_sampler_phase_times synchronises the stream of the last timed step, writes up to n
- * accumulated milliseconds (per phase, summed over *steps steps) and resets the totals.
- * Not for use inside stream capture. */
+ * enable = 2 (coarse): only the ends of phases 0, 3, 4 and 6 are marked, so phases 1-3 are
+ * accumulated under 3 and phases 5-6 under 6 (fewer events between the kernels, which then
+ * run closer to their untimed schedule). enable = 0 switches timing off; other values are
+ * DS_ERR_INVALID_ARG. ds_sampler_phase_times synchronises the stream of the last timed step,
+ * writes up to n accumulated milliseconds (per phase, summed over *steps steps) and resets the
+ * totals. Not for use inside stream capture. */
 ds_status ds_sampler_set_phase_timing(ds_sampler* sampler, int32_t enable);
 ds_status ds_sampler_phase_times(ds_sampler* sampler, float* ms, int32_t n, int32_t* steps);
 

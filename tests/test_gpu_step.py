@@ -295,3 +295,28 @@ def test_standin_hidden_matches_oracle():
     got = Hout.view(torch.int16).cpu().numpy().view(np.uint16)
     frac = standin_close(got, inp["W"], s_prev.astype(np.float64), case.E64, inp["canvas"])
     assert frac < 1e-2
+
+
+def test_phase_timing_levels():
+    # every phase (1) and the coarse boundaries (2) account for the same step time; the coarse
+    # mode folds statistics / top-k into "convert" and finalize into "lock"
+    w = W.scaled(BASE_BATCH, V=8192, d=512, B=2)
+    case = GpuCase(w)
+    sampler = case.sampler
+    totals = {}
+    for level, coarse in ((1, False), (2, True)):
+        sampler.set_phase_timing(True, coarse=coarse)
+        for _ in range(20):
+            case.run_step(case.state())
+        ph, n = sampler.phase_times()
+        sampler.set_phase_timing(False)
+        assert n == 20
+        assert ph["logits"] > 0 and ph["selfcond"] > 0 and ph["convert"] > 0 and ph["lock"] > 0
+        if coarse:
+            assert ph["stats"] == 0 and ph["topk"] == 0 and ph["finalize"] == 0
+        else:
+            assert ph["stats"] > 0 and ph["finalize"] > 0
+        totals[level] = sum(ph.values()) / n
+    assert abs(totals[1] - totals[2]) <= 0.25 * totals[1]
+    lib = C.load_library()
+    assert lib.ds_sampler_set_phase_timing(sampler.handle, 3) == C.DS_ERR_INVALID_ARG
