@@ -53,8 +53,8 @@ def parse_args():
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling runs)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-positions", type=int, default=32,
-                    help="canvas positions in the oracle's timed sample")
+    ap.add_argument("--cpu-positions", type=int, default=256,
+                    help="canvas positions in the oracle's timed sample (256: one full step)")
     return ap.parse_args()
 
 
@@ -424,8 +424,9 @@ def run_ours(args):
         sec_step = sec * (w.L / n) * w.B
         line["cpu_baseline"] = {
             "value": 1.0 / sec_step, "unit": "steps/s", "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"fp64 oracle over {n} of {w.L} canvas positions (full vocabulary), "
-                      f"{sec:.1f} s, scaled by {w.L / n * w.B:g} to one step"}
+            "sample": (f"fp64 oracle over {n} of {w.L} canvas positions (full vocabulary), "
+                       f"{sec:.1f} s" + (": one whole step" if w.L / n * w.B == 1 else
+                                         f", scaled by {w.L / n * w.B:g} to one step"))}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
