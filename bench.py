@@ -53,6 +53,9 @@ def parse_args():
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling runs)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--loop", action="store_true",
+                    help="time the whole denoising loop (ds_denoise_loop) of the workload, as a "
+                         "CUDA graph and as plain launches, instead of one step")
     ap.add_argument("--cpu-positions", type=int, default=256,
                     help="canvas positions in the oracle's timed sample (256: one full step)")
     return ap.parse_args()
@@ -434,10 +437,78 @@ def run_ours(args):
     return 0
 
 
+def run_loop(args):
+    """The workload's whole denoising loop through ds_denoise_loop (fixed H, or the stand-in
+    hidden states for stand-in workloads): device time per loop and per iteration, as one CUDA
+    graph with a device-side stop condition and as plain launches. One JSON line."""
+    import torch
+
+    from canvas_sampler_gb300.sampler import CanvasState, Sampler, StepOutputs
+
+    dev = torch.device("cuda", 0)
+    w = workload_of(args)
+    inp = W.make_inputs(w)
+
+    def upload(a):
+        if w.dtype == "fp32":
+            return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    E = upload(inp["E"])
+    T = torch.from_numpy(inp["T"]).to(dev)
+    tau = torch.from_numpy(inp["tau"]).to(dev)
+    standin = w.h_mode == "standin"
+    H = None if standin else upload(inp["H"])
+    Wt = upload(inp["W"]) if standin else None
+    sampler = Sampler(w.V, w.d, canvas_len=w.L, max_batch=w.B, dtype=w.dtype, top_k=w.top_k,
+                      max_steps=w.max_steps, impl=args.kernel_impl)
+    B, L = w.B, w.L
+    state = CanvasState.from_numpy(inp["canvas"], inp["lock"], inp["step"], inp["done"],
+                                   device=dev)
+    init = CanvasState.from_numpy(inp["canvas"], inp["lock"], inp["step"], inp["done"],
+                                  device=dev)
+    out = StepOutputs.empty(B, L, w.d, device=dev)
+    H_buf = torch.zeros(B, L, w.d, dtype=torch.bfloat16, device=dev) if standin else None
+
+    def one_loop(use_graph):
+        for k in ("canvas", "lock", "step", "done"):
+            getattr(state, k).copy_(getattr(init, k))
+        out.s.zero_()  # the stand-in starts from s_prev = 0
+        sampler.loop(E, T, tau, state, inp["seed"], out, H=H, W=Wt, H_buf=H_buf,
+                     max_iters=w.max_steps, use_graph=use_graph)
+
+    res = {}
+    for use_graph in (True, False):
+        for _ in range(max(1, args.warmup)):
+            one_loop(use_graph)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record()
+        for _ in range(args.steps):
+            one_loop(use_graph)
+        ev1.record()
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1) / args.steps
+        iters = int(state.step.max().item())  # the loop runs until its last sequence is done
+        res["graph" if use_graph else "plain"] = {
+            "ms_per_loop": ms, "iterations": iters, "ms_per_iteration": ms / max(1, iters),
+            "steps_per_s": iters / (ms / 1e3)}
+    assert sampler.device_status() == 0
+    line = {"mode": "loop", "workload": w.name, "B": B, "L": L, "V": w.V, "d": w.d,
+            "top_k": w.top_k, "h_mode": w.h_mode, "max_steps": w.max_steps,
+            "loops": args.steps, "warmup": args.warmup, "impl": sampler.impl,
+            "note": "device time of one whole loop (state reset by device copies inside the "
+                    "timed region), CUDA events on the launching stream", **res}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.loop:
+        return run_loop(args)
     return run_ours(args)
 
 
