@@ -508,6 +508,8 @@ __global__ void __launch_bounds__(kThreads) k_finalize(
     float4* dst = reinterpret_cast<float4*>(s_out + (size_t)r * d);
     for (int q = threadIdx.x; q < d / 4; q += kThreads) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      // unrolled so that a thread's loads of the split partials are in flight together
+#pragma unroll 13
       for (int sp = 0; sp < S; ++sp) {
         const float4 t = src[sp * plane / 4 + q];
         const float c = sh_sc[sp];
