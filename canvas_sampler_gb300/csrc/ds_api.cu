@@ -188,8 +188,10 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
                            a->seed, s->blk, a->sampled, a->conf, a->entropy, a->argmax, s->Opart,
                            sh.n_ranges, d, a->s, s->mref, st);
     s->launches += 4;
-  } else if (s->impl != DS_IMPL_SIMT && k == 0) {
-    // the logits leave the GEMM as segment-relative probabilities; no y, no convert pass
+  } else if (s->impl != DS_IMPL_SIMT) {
+    // the logits leave the GEMM as tile-relative probabilities; no y, no convert pass. Without
+    // top-k the Gumbel race runs over all of them; with top-k each chunk's k most probable
+    // tokens become the candidates that finalize draws among.
     cudaError_t e = launch_logits_p_tc(static_cast<const uint16_t*>(a->H),
                                        static_cast<const uint16_t*>(a->E), R, V, d, L, T, a->done,
                                        s->Phi, s->Plo, s->cs, s->mseg_t, s->err, st);
@@ -197,51 +199,42 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
     mark(s, 0, st);
     launch_row_merge(s->cs, (int)(V / kTcSegment), R, L, a->done, s->rs, st);
     mark(s, 1, st);
+    if (k > 0)
+      launch_topk_row(s->Phi, s->Plo, s->cs, s->mseg_t, s->rs, R, V, L, a->done, k, s->cand, st);
     mark(s, 2, st);
-    launch_gumbel_seg(s->Phi, s->Plo, s->cs, s->rs, R, V, L, a->done, a->step, a->seed, s->blk,
-                      true, s->best, st);
+    if (k == 0)
+      launch_gumbel_seg(s->Phi, s->Plo, s->cs, s->rs, R, V, L, a->done, a->step, a->seed, s->blk,
+                        true, s->best, st);
     mark(s, 3, st);
     e = launch_selfcond_tc(s->Phi, s->Plo, static_cast<const uint16_t*>(a->E), R, V, d, L,
                            a->done, S, s->Opart, s->mseg_t, s->mref, s->err, st);
     if (e != cudaSuccess) return cuda_status(e);
     mark(s, 4, st);
-    launch_finalize_with_s(s->rs, s->best, nullptr, s->n_chunks, 0, R, L, a->done, a->step,
-                           a->seed, s->blk, a->sampled, a->conf, a->entropy, a->argmax, s->Opart,
-                           S, d, a->s, s->mref, st);
+    // with top-k the candidate pool of a row is its k candidates (one "chunk")
+    launch_finalize_with_s(s->rs, s->best, k > 0 ? s->cand : nullptr, k > 0 ? 1 : s->n_chunks, k,
+                           R, L, a->done, a->step, a->seed, s->blk, a->sampled, a->conf,
+                           a->entropy, a->argmax, s->Opart, S, d, a->s, s->mref, st);
     s->launches += 5;
-  } else if (s->impl != DS_IMPL_SIMT) {
-    cudaError_t e = launch_logits_tc(static_cast<const uint16_t*>(a->H),
-                                     static_cast<const uint16_t*>(a->E), R, V, d, L, T, a->done,
-                                     s->Y, s->cs, s->err, st);
-    if (e != cudaSuccess) return cuda_status(e);
-    mark(s, 0, st);
-    launch_row_merge(s->cs, (int)(V / kTcSegment), R, L, a->done, s->rs, st);
   } else {
     launch_logits_simt(a->H, a->E, fp32, R, V, d, L, T, a->done, s->Y, st);
     mark(s, 0, st);
     launch_chunk_stats(s->Y, R, V, L, a->done, s->cs, st);
     launch_row_merge(s->cs, s->n_chunks, R, L, a->done, s->rs, st);
   }
-  if (!s->fused && (s->impl == DS_IMPL_SIMT || k > 0)) {
+  if (!s->fused && s->impl == DS_IMPL_SIMT) {
+    // CUDA-core path: y materialised, split into hi / lo by the convert pass
     mark(s, 1, st);
     if (k > 0) launch_topk_chunk(s->Y, R, V, L, a->done, k, s->cand, st);
     mark(s, 2, st);
     launch_convert(s->Y, s->rs, R, V, L, a->done, a->step, a->seed, s->blk, k == 0, s->Phi,
                    s->Plo, s->best, st);
     mark(s, 3, st);
-    if (s->impl != DS_IMPL_SIMT) {
-      cudaError_t e = launch_selfcond_tc(s->Phi, s->Plo, static_cast<const uint16_t*>(a->E), R,
-                                         V, d, L, a->done, S, s->Opart, nullptr, nullptr, s->err,
-                                         st);
-      if (e != cudaSuccess) return cuda_status(e);
-    } else {
-      launch_selfcond_simt(s->Phi, s->Plo, a->E, fp32, R, V, d, L, a->done, S, s->Opart, st);
-    }
+    launch_selfcond_simt(s->Phi, s->Plo, a->E, fp32, R, V, d, L, a->done, S, s->Opart, st);
     mark(s, 4, st);
     launch_finalize_with_s(s->rs, s->best, s->cand, s->n_chunks, k, R, L, a->done, a->step,
                            a->seed, s->blk, a->sampled, a->conf, a->entropy, a->argmax, s->Opart,
                            S, d, a->s, nullptr, st);
-    s->launches += (s->impl != DS_IMPL_SIMT ? 5 : 6) + (k > 0 ? 1 : 0);
+    s->launches += 6 + (k > 0 ? 1 : 0);
   }
   mark(s, 5, st);
   if (s->cfg.lock_rule == DS_LOCK_ENTROPY_BUDGET)
@@ -416,8 +409,8 @@ ds_status ds_sampler_create(const ds_sampler_config* cfg, ds_sampler** out) {
     }
   }
   e = cudaSuccess;
-  // the tensor-core step without top-k never materialises y (segment-relative probabilities)
-  const bool seg_path = s->impl == DS_IMPL_TENSOR && c.top_k == 0;
+  // the tensor-core step never materialises y (tile-relative probabilities)
+  const bool seg_path = s->impl == DS_IMPL_TENSOR;
   if (s->fused) {
     const VocabPassShape sh = vocab_pass_shape((int)Rm, c.vocab, c.d_model, s->num_sms, 0);
     s->seg = carve<ChunkStat>(s, Rm * (V / kVpSegment), &e);

@@ -476,6 +476,212 @@ __global__ void __launch_bounds__(kThreads) k_topk_chunk(const float* __restrict
   });
 }
 
+// The same selection from the stored probabilities instead of y: P = (hi + lo)[j], relative to
+// the row's maximum over token j's 256-token tile (mtile_t [V/256, R]), is brought to the row
+// maximum m, p_j = P e^{m_t - m}, which orders the tokens as y does (up to the ~17 significant
+// bits of hi + lo); the k largest are written with y = m + ln p_j. Element q of thread t is token
+// j0 + t + 256 q, so the selection's (q, thread) order is token order, and all tokens of element
+// q lie in one tile.
+__global__ void __launch_bounds__(kThreads) k_topk_chunk_p(const uint16_t* __restrict__ Phi,
+                                                           const uint16_t* __restrict__ Plo,
+                                                           const float* __restrict__ mtile_t,
+                                                           const RowStat* __restrict__ rs,
+                                                           int R, int64_t V, int L,
+                                                           const uint8_t* __restrict__ done,
+                                                           int k, Cand* __restrict__ cand,
+                                                           int n_chunks) {
+  __shared__ int hist[256];
+  __shared__ int scan_sh[32];
+  __shared__ float sh_scale[kPer];
+  pdl_wait();
+  const int c = blockIdx.x, r = blockIdx.y;
+  if (done && done[r / L]) return;
+  const float m = rs[r].m;
+  const int64_t j0 = (int64_t)c * kChunk, j1 = min(V, j0 + kChunk);
+  if (threadIdx.x < kPer) {
+    const int64_t jt = j0 + 256 * (int64_t)threadIdx.x;
+    sh_scale[threadIdx.x] = jt < j1 ? expf(mtile_t[(size_t)(jt / 256) * R + r] - m) : 0.f;
+  }
+  __syncthreads();
+  const uint16_t* ph = Phi + (size_t)r * V;
+  const uint16_t* pl = Plo + (size_t)r * V;
+  uint32_t key[kPer];
+  bool valid[kPer];
+  float pv[kPer];
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const int64_t j = j0 + threadIdx.x + (int64_t)kThreads * q;
+    valid[q] = j < j1;
+    float p = 0.f;
+    if (valid[q])
+      p = (__uint_as_float((uint32_t)ph[j] << 16) + __uint_as_float((uint32_t)pl[j] << 16)) *
+          sh_scale[q];
+    pv[q] = p;
+    key[q] = float_key(p);
+  }
+  Cand* out = cand + ((size_t)r * n_chunks + c) * k;
+  for (int t = threadIdx.x; t < k; t += kThreads) out[t] = Cand{-INFINITY, INT_MAX};
+  __syncthreads();
+  block_select_topk<kPer>(key, valid, k, hist, scan_sh, [&](int q, int slot) {
+    out[slot] = Cand{pv[q] > 0.f ? m + logf(pv[q]) : -INFINITY,
+                     (int32_t)(j0 + threadIdx.x + (int64_t)kThreads * q)};
+  });
+}
+
+// Top-k of a row from the stored probabilities, one CTA (8 warps) per row. The k largest
+// segment maxima are k distinct tokens, so the row's k-th largest logit is at least the k-th
+// largest segment maximum theta, and only segments whose maximum reaches theta can hold a top-k
+// token (about k of them: every segment when the logits are all equal). The selection is a
+// radix select (8-bit digits from the top) over float keys, first of the segment maxima, then
+// of p_j = P e^{m_t - m} (the same order as y, up to the ~17 significant bits of hi + lo) over
+// the tokens of those segments, re-read from P on each pass; histogram updates are aggregated per
+// warp (lanes with the same digit add once). The k selected are written with y = m + ln p in a
+// fixed order (warp by warp, each warp's segments in order, tokens in order): finalize does not
+// depend on the order of its candidates, only on their set.
+namespace {
+
+constexpr int kTkWarps = kThreads / 32;
+
+// Warp-aggregated histogram increment of digit `bin` for the lanes with `mine`; called by all
+// lanes of the warp together.
+DS_DEV void tk_hist_add(int* hist, bool mine, uint32_t bin) {
+  const unsigned act = __ballot_sync(0xffffffffu, mine);
+  if (mine) {
+    const unsigned peers = __match_any_sync(act, bin);
+    if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+  }
+}
+
+// One radix select over the keys a functor enumerates: each_key(f) calls f(valid, key) for
+// every key of this thread, in the same order on every call and with all lanes of a warp
+// together. Returns the k-th largest key and, in *need, how many keys equal to it are taken.
+template <class EachKey>
+DS_DEV uint32_t tk_select(EachKey each_key, int k, int* hist, int* sel, int* need_out) {
+  uint32_t prefix = 0, mask = 0;
+  int need = k;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int t = threadIdx.x; t < 256; t += blockDim.x) hist[t] = 0;
+    __syncthreads();
+    each_key([&](bool valid, uint32_t key) {
+      tk_hist_add(hist, valid && (key & mask) == prefix, (key >> shift) & 255u);
+    });
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int cum = 0, bin = 255;
+      for (; bin >= 0; --bin) {
+        if (cum + hist[bin] >= need) break;
+        cum += hist[bin];
+      }
+      if (bin < 0) bin = 0;  // fewer valid keys than k: all of them are taken
+      sel[0] = bin;
+      sel[1] = need - cum;
+    }
+    __syncthreads();
+    prefix |= (uint32_t)sel[0] << shift;
+    mask |= 255u << shift;
+    need = sel[1];
+    __syncthreads();
+  }
+  *need_out = need;
+  return prefix;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads) k_topk_row(const uint16_t* __restrict__ Phi,
+                                                       const uint16_t* __restrict__ Plo,
+                                                       const ChunkStat* __restrict__ seg,
+                                                       const float* __restrict__ mtile_t,
+                                                       const RowStat* __restrict__ rs, int R,
+                                                       int64_t V, int L,
+                                                       const uint8_t* __restrict__ done, int k,
+                                                       Cand* __restrict__ cand) {
+  __shared__ int hist[256];
+  __shared__ int sel[2];
+  __shared__ int sh_cnt[2][kTkWarps];
+  pdl_wait();
+  const int r = blockIdx.x;
+  if (done && done[r / L]) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float m = rs[r].m;
+  const int nseg = (int)(V / 128);
+  const ChunkStat* sg = seg + (size_t)r * nseg;
+  const uint16_t* ph = Phi + (size_t)r * V;
+  const uint16_t* pl = Plo + (size_t)r * V;
+  Cand* out = cand + (size_t)r * k;
+  for (int t = threadIdx.x; t < k; t += kThreads) out[t] = Cand{-INFINITY, INT_MAX};
+
+  // theta: the min(k, nseg)-th largest segment maximum
+  int dummy = 0;
+  const int n_it = (nseg + kThreads - 1) / kThreads;
+  const uint32_t theta = tk_select(
+      [&](auto f) {
+        for (int it = 0; it < n_it; ++it) {
+          const int g = threadIdx.x + kThreads * it;
+          f(g < nseg, g < nseg ? float_key(sg[g].m) : 0u);
+        }
+      },
+      min(k, nseg), hist, sel, &dummy);
+
+  // the tokens of the segments whose maximum reaches theta, warp w taking segments w, w + 8, ...;
+  // lane l takes tokens 4 l .. 4 l + 3 of a segment
+  auto each_token = [&](auto f) {
+    for (int g = warp; g < nseg; g += kTkWarps) {
+      if (float_key(sg[g].m) < theta) continue;  // the whole warp skips the segment
+      const float scale = expf(mtile_t[(size_t)(g >> 1) * R + r] - m);
+      const int64_t j = (int64_t)g * 128 + 4 * lane;
+      const uint2 h = *reinterpret_cast<const uint2*>(ph + j);
+      const uint2 lo = *reinterpret_cast<const uint2*>(pl + j);
+      const uint32_t hw[2] = {h.x, h.y}, lw[2] = {lo.x, lo.y};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t hb = (e & 1) ? (hw[e >> 1] & 0xFFFF0000u) : (hw[e >> 1] << 16);
+        const uint32_t lb = (e & 1) ? (lw[e >> 1] & 0xFFFF0000u) : (lw[e >> 1] << 16);
+        const float p = (__uint_as_float(hb) + __uint_as_float(lb)) * scale;
+        f(j + e, p, float_key(p));
+      }
+    }
+  };
+  int need = 0;
+  const uint32_t kth = tk_select(
+      [&](auto f) { each_token([&](int64_t, float, uint32_t key) { f(true, key); }); }, k, hist,
+      sel, &need);
+
+  // per warp: keys above the k-th, and keys equal to it (of which the first `need`, in warp
+  // order, are taken)
+  int gt = 0, eq = 0;
+  each_token([&](int64_t, float, uint32_t key) {
+    gt += __popc(__ballot_sync(0xffffffffu, key > kth));
+    eq += __popc(__ballot_sync(0xffffffffu, key == kth));
+  });
+  if (lane == 0) {
+    sh_cnt[0][warp] = gt;
+    sh_cnt[1][warp] = eq;
+  }
+  __syncthreads();
+  int eq_before = 0, take_before = 0;
+  for (int w = 0; w < warp; ++w) {
+    const int eq_w = sh_cnt[1][w];
+    const int take_eq = max(0, min(eq_w, need - eq_before));
+    take_before += sh_cnt[0][w] + take_eq;
+    eq_before += eq_w;
+  }
+  int taken = 0, eq_seen = 0;
+  const unsigned below = (1u << lane) - 1u;
+  each_token([&](int64_t j, float p, uint32_t key) {
+    const bool is_eq = key == kth;
+    const unsigned eq_b = __ballot_sync(0xffffffffu, is_eq);
+    const bool take = key > kth || (is_eq && eq_before + eq_seen + __popc(eq_b & below) < need);
+    const unsigned tk_b = __ballot_sync(0xffffffffu, take);
+    if (take) {
+      const int slot = take_before + taken + __popc(tk_b & below);
+      if (slot < k) out[slot] = Cand{p > 0.f ? m + logf(p) : -INFINITY, (int32_t)j};
+    }
+    taken += __popc(tk_b);
+    eq_seen += __popc(eq_b);
+  });
+}
+
 // Per row: the sampled token, its confidence, the entropy and the argmax.
 // With Opart set, it also writes s for the row: the sum of the vocabulary-split partials in
 // split order, divided by the softmax normaliser.
@@ -536,6 +742,26 @@ __global__ void __launch_bounds__(kThreads) k_finalize(
     }
     block_best(bv, bj, by, shv, shj, &shy);
     cval = expf(by) / st.l;
+  } else if (n_chunks == 1) {
+    // the pool is the row's k candidates already (one per slot, unused slots with token
+    // INT_MAX): Gumbel-max over them and the truncated normaliser, no selection
+    float e_sum = 0.f;
+    for (int t = threadIdx.x; t < k; t += kThreads) {
+      const Cand c = cand[(size_t)r * k + t];
+      if (c.j == INT_MAX) continue;
+      const u32x4 w = gumbel_block((uint32_t)(c.j >> 2), (uint32_t)i, stream_id((uint32_t)b, blk),
+                                   (uint32_t)step[b], seed);
+      const float v = c.y + gumbel_from_word(word_of(w, c.j & 3));
+      if (better(v, c.j, bv, bj)) {
+        bv = v;
+        bj = c.j;
+        by = c.y;
+      }
+      e_sum += expf(c.y - st.m);
+    }
+    e_sum = block_sum(e_sum, shf);
+    block_best(bv, bj, by, shv, shj, &shy);
+    cval = expf(by - st.m) / e_sum;
   } else {
     // The pool holds each chunk's candidates in token order, chunks in order, so pool order
     // is token order; element q of thread t is pool entry t + 256 q.
@@ -962,6 +1188,21 @@ void launch_topk_chunk(const float* Y, int R, int64_t V, int L, const uint8_t* d
                        Cand* cand, cudaStream_t st) {
   const int nc = n_chunks_of(V);
   k_topk_chunk<<<dim3(nc, R), kThreads, 0, st>>>(Y, V, L, done, k, cand, nc);
+}
+
+void launch_topk_chunk_p(const uint16_t* Phi, const uint16_t* Plo, const float* mtile_t,
+                         const RowStat* rs, int R, int64_t V, int L, const uint8_t* done, int k,
+                         Cand* cand, cudaStream_t st) {
+  const int nc = n_chunks_of(V);
+  launch_k(k_topk_chunk_p, dim3(nc, R), dim3(kThreads), 0, st, Phi, Plo, mtile_t, rs, R, V, L,
+           done, k, cand, nc);
+}
+
+void launch_topk_row(const uint16_t* Phi, const uint16_t* Plo, const ChunkStat* seg,
+                     const float* mtile_t, const RowStat* rs, int R, int64_t V, int L,
+                     const uint8_t* done, int k, Cand* cand, cudaStream_t st) {
+  launch_k(k_topk_row, dim3(R), dim3(kThreads), 0, st, Phi, Plo, seg, mtile_t, rs, R, V, L, done,
+           k, cand);
 }
 
 void launch_finalize(const RowStat* rs, const Best* best, const Cand* cand, int n_chunks, int k,

@@ -16,6 +16,8 @@ from canvas_sampler_gb300 import _lib as C
 from canvas_sampler_gb300 import workloads as W
 from canvas_sampler_gb300.sampler import CanvasState, Sampler, StepOutputs
 
+from _helpers import GpuCase, compare_outputs, out_np, oracle_step, state_np
+
 pytestmark = pytest.mark.gpu
 
 REL_TOL = 2e-5
@@ -78,3 +80,31 @@ def test_no_alloc_step_rejects_what_does_not_fit():
     assert rc == C.DS_ERR_UNSUPPORTED
     torch.cuda.synchronize()
     assert torch.all(out.sampled == -3)  # nothing was enqueued
+
+
+def test_no_alloc_topk_step_matches_oracle():
+    # the no-allocation top-k path materialises y (the tensor-core logits in fp32), selects each
+    # chunk's top k from it and splits exp(y - m) for the self-conditioning GEMM; the sampler's
+    # own top-k path selects from the stored probabilities instead: both against the oracle
+    from dataclasses import replace
+    lib = C.load_library()
+    w = replace(W.scaled(W.WORKLOADS["loop8_bf16_b1_v32768_d1024"], V=8192, d=512, B=2), top_k=8)
+    case = GpuCase(w, impl="tensor")
+    pre = state_np(case.state())
+    cfg = case.sampler._cfg
+    st = case.state()
+    out = StepOutputs.empty(w.B, w.L, w.d)
+    a = _args(case.sampler, case.H, case.E, case.T, case.tau, st, out, case.inp["seed"])
+    rc = lib.ds_sampler_step_noalloc(ctypes.byref(cfg), ctypes.byref(a),
+                                     torch.cuda.current_stream().cuda_stream)
+    assert rc == C.DS_OK, C.status_string(rc)
+    torch.cuda.synchronize()
+    ref = oracle_step(case, pre)
+    rows = [(b, i) for b in range(w.B) for i in range(w.L)]
+    rep = compare_outputs(out_np(out), ref, rows, top_k=w.top_k)
+    assert rep["checked"] == len(rows)
+    assert rep["excluded"] <= max(2, len(rows) // 100)
+    # the sampler's step on the same inputs
+    out2 = case.run_step(case.state())
+    rep2 = compare_outputs(out_np(out2), ref, rows, top_k=w.top_k)
+    assert rep2["excluded"] <= max(2, len(rows) // 100)
