@@ -60,11 +60,6 @@ void launch_topk_chunk(const float* Y, int R, int64_t V, int L, const uint8_t* d
 void launch_topk_row(const uint16_t* Phi, const uint16_t* Plo, const ChunkStat* seg,
                      const float* mtile_t, const RowStat* rs, int R, int64_t V, int L,
                      const uint8_t* done, int k, Cand* cand, cudaStream_t st);
-// Per chunk from the stored probabilities (bf16 hi + lo relative to the tile maxima mtile_t
-// [V/256, R]) and the row maxima in rs: candidates carry y = m + ln p.
-void launch_topk_chunk_p(const uint16_t* Phi, const uint16_t* Plo, const float* mtile_t,
-                         const RowStat* rs, int R, int64_t V, int L, const uint8_t* done, int k,
-                         Cand* cand, cudaStream_t st);
 void launch_finalize(const RowStat* rs, const Best* best, const Cand* cand, int n_chunks, int k,
                      int R, int L, const uint8_t* done, const int32_t* step, uint64_t seed,
                      const int32_t* blk, int32_t* sampled, float* conf, float* entropy,

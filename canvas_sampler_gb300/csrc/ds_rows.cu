@@ -476,58 +476,6 @@ __global__ void __launch_bounds__(kThreads) k_topk_chunk(const float* __restrict
   });
 }
 
-// The same selection from the stored probabilities instead of y: P = (hi + lo)[j], relative to
-// the row's maximum over token j's 256-token tile (mtile_t [V/256, R]), is brought to the row
-// maximum m, p_j = P e^{m_t - m}, which orders the tokens as y does (up to the ~17 significant
-// bits of hi + lo); the k largest are written with y = m + ln p_j. Element q of thread t is token
-// j0 + t + 256 q, so the selection's (q, thread) order is token order, and all tokens of element
-// q lie in one tile.
-__global__ void __launch_bounds__(kThreads) k_topk_chunk_p(const uint16_t* __restrict__ Phi,
-                                                           const uint16_t* __restrict__ Plo,
-                                                           const float* __restrict__ mtile_t,
-                                                           const RowStat* __restrict__ rs,
-                                                           int R, int64_t V, int L,
-                                                           const uint8_t* __restrict__ done,
-                                                           int k, Cand* __restrict__ cand,
-                                                           int n_chunks) {
-  __shared__ int hist[256];
-  __shared__ int scan_sh[32];
-  __shared__ float sh_scale[kPer];
-  pdl_wait();
-  const int c = blockIdx.x, r = blockIdx.y;
-  if (done && done[r / L]) return;
-  const float m = rs[r].m;
-  const int64_t j0 = (int64_t)c * kChunk, j1 = min(V, j0 + kChunk);
-  if (threadIdx.x < kPer) {
-    const int64_t jt = j0 + 256 * (int64_t)threadIdx.x;
-    sh_scale[threadIdx.x] = jt < j1 ? expf(mtile_t[(size_t)(jt / 256) * R + r] - m) : 0.f;
-  }
-  __syncthreads();
-  const uint16_t* ph = Phi + (size_t)r * V;
-  const uint16_t* pl = Plo + (size_t)r * V;
-  uint32_t key[kPer];
-  bool valid[kPer];
-  float pv[kPer];
-#pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    const int64_t j = j0 + threadIdx.x + (int64_t)kThreads * q;
-    valid[q] = j < j1;
-    float p = 0.f;
-    if (valid[q])
-      p = (__uint_as_float((uint32_t)ph[j] << 16) + __uint_as_float((uint32_t)pl[j] << 16)) *
-          sh_scale[q];
-    pv[q] = p;
-    key[q] = float_key(p);
-  }
-  Cand* out = cand + ((size_t)r * n_chunks + c) * k;
-  for (int t = threadIdx.x; t < k; t += kThreads) out[t] = Cand{-INFINITY, INT_MAX};
-  __syncthreads();
-  block_select_topk<kPer>(key, valid, k, hist, scan_sh, [&](int q, int slot) {
-    out[slot] = Cand{pv[q] > 0.f ? m + logf(pv[q]) : -INFINITY,
-                     (int32_t)(j0 + threadIdx.x + (int64_t)kThreads * q)};
-  });
-}
-
 // Top-k of a row from the stored probabilities, one CTA (8 warps) per row. The k largest
 // segment maxima are k distinct tokens, so the row's k-th largest logit is at least the k-th
 // largest segment maximum theta, and only segments whose maximum reaches theta can hold a top-k
@@ -1188,14 +1136,6 @@ void launch_topk_chunk(const float* Y, int R, int64_t V, int L, const uint8_t* d
                        Cand* cand, cudaStream_t st) {
   const int nc = n_chunks_of(V);
   k_topk_chunk<<<dim3(nc, R), kThreads, 0, st>>>(Y, V, L, done, k, cand, nc);
-}
-
-void launch_topk_chunk_p(const uint16_t* Phi, const uint16_t* Plo, const float* mtile_t,
-                         const RowStat* rs, int R, int64_t V, int L, const uint8_t* done, int k,
-                         Cand* cand, cudaStream_t st) {
-  const int nc = n_chunks_of(V);
-  launch_k(k_topk_chunk_p, dim3(nc, R), dim3(kThreads), 0, st, Phi, Plo, mtile_t, rs, R, V, L,
-           done, k, cand, nc);
 }
 
 void launch_topk_row(const uint16_t* Phi, const uint16_t* Plo, const ChunkStat* seg,
