@@ -489,6 +489,9 @@ __global__ void __launch_bounds__(kThreads) k_topk_chunk(const float* __restrict
 namespace {
 
 constexpr int kTkWarps = kThreads / 32;
+// Candidate segments listed in shared memory (more, e.g. when every logit is equal, are found by
+// scanning the segment maxima on every pass instead).
+constexpr int kTkListCap = 2048;
 
 // Warp-aggregated histogram increment of digit `bin` for the lanes with `mine`; called by all
 // lanes of the warp together.
@@ -547,6 +550,8 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(const uint16_t* __restric
   __shared__ int hist[256];
   __shared__ int sel[2];
   __shared__ int sh_cnt[2][kTkWarps];
+  __shared__ int scan_sh[32];
+  __shared__ int sh_list[kTkListCap];
   pdl_wait();
   const int r = blockIdx.x;
   if (done && done[r / L]) return;
@@ -571,11 +576,33 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(const uint16_t* __restric
       },
       min(k, nseg), hist, sel, &dummy);
 
-  // the tokens of the segments whose maximum reaches theta, warp w taking segments w, w + 8, ...;
-  // lane l takes tokens 4 l .. 4 l + 3 of a segment
+  // the segments whose maximum reaches theta, listed once (thread t's segments t, t + 256, ...
+  // in turn, threads in order)
+  int n_cand = 0;
+  {
+    int mine = 0;
+    for (int it = 0; it < n_it; ++it) {
+      const int g = threadIdx.x + kThreads * it;
+      mine += (g < nseg && float_key(sg[g].m) >= theta) ? 1 : 0;
+    }
+    const int base = block_exclusive_scan(mine, scan_sh, &n_cand);
+    if (n_cand <= kTkListCap) {
+      int o = base;
+      for (int it = 0; it < n_it; ++it) {
+        const int g = threadIdx.x + kThreads * it;
+        if (g < nseg && float_key(sg[g].m) >= theta) sh_list[o++] = g;
+      }
+    }
+    __syncthreads();
+  }
+  const bool listed = n_cand <= kTkListCap;
+  // the tokens of those segments, warp w taking the w-th, (w + 8)-th, ... of them; lane l takes
+  // tokens 4 l .. 4 l + 3 of a segment
   auto each_token = [&](auto f) {
-    for (int g = warp; g < nseg; g += kTkWarps) {
-      if (float_key(sg[g].m) < theta) continue;  // the whole warp skips the segment
+    const int n_walk = listed ? n_cand : nseg;
+    for (int e = warp; e < n_walk; e += kTkWarps) {
+      const int g = listed ? sh_list[e] : e;
+      if (!listed && float_key(sg[g].m) < theta) continue;  // the whole warp skips it
       const float scale = expf(mtile_t[(size_t)(g >> 1) * R + r] - m);
       const int64_t j = (int64_t)g * 128 + 4 * lane;
       const uint2 h = *reinterpret_cast<const uint2*>(ph + j);
