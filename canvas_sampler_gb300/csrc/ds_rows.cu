@@ -483,9 +483,10 @@ __global__ void __launch_bounds__(kThreads) k_topk_chunk(const float* __restrict
 // radix select (8-bit digits from the top) over float keys, first of the segment maxima, then
 // of p_j = P e^{m_t - m} (the same order as y, up to the ~17 significant bits of hi + lo) over
 // the tokens of those segments, re-read from P on each pass; histogram updates are aggregated per
-// warp (lanes with the same digit add once). The k selected are written with y = m + ln p in a
-// fixed order (warp by warp, each warp's segments in order, tokens in order): finalize does not
-// depend on the order of its candidates, only on their set.
+// warp (lanes with the same digit add once). Of the tokens whose key equals the k-th, the lowest
+// are taken (a second select over their indices when not all of them fit). The k selected are
+// written with y = m + ln p in a fixed order (warp by warp, each warp's segments in list order):
+// finalize does not depend on the order of its candidates, only on their set.
 namespace {
 
 constexpr int kTkWarps = kThreads / 32;
@@ -622,8 +623,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(const uint16_t* __restric
       [&](auto f) { each_token([&](int64_t, float, uint32_t key) { f(true, key); }); }, k, hist,
       sel, &need);
 
-  // per warp: keys above the k-th, and keys equal to it (of which the first `need`, in warp
-  // order, are taken)
+  // per warp: keys above the k-th, and keys equal to it
   int gt = 0, eq = 0;
   each_token([&](int64_t, float, uint32_t key) {
     gt += __popc(__ballot_sync(0xffffffffu, key > kth));
@@ -634,26 +634,45 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(const uint16_t* __restric
     sh_cnt[1][warp] = eq;
   }
   __syncthreads();
-  int eq_before = 0, take_before = 0;
-  for (int w = 0; w < warp; ++w) {
-    const int eq_w = sh_cnt[1][w];
-    const int take_eq = max(0, min(eq_w, need - eq_before));
-    take_before += sh_cnt[0][w] + take_eq;
-    eq_before += eq_w;
+  int eq_total = 0;
+  for (int w = 0; w < kTkWarps; ++w) eq_total += sh_cnt[1][w];
+  // Keys equal to the k-th are taken lowest tokens first: when only `need` of them fit, a second
+  // select over their token indices (key ~j, larger for lower tokens) finds the need-th lowest.
+  uint32_t jcut = 0;  // tie tokens with ~j >= jcut are taken
+  if (need < eq_total) {
+    int dummy2 = 0;
+    jcut = tk_select(
+        [&](auto f) {
+          each_token([&](int64_t j, float, uint32_t key) { f(key == kth, ~(uint32_t)j); });
+        },
+        need, hist, sel, &dummy2);
   }
-  int taken = 0, eq_seen = 0;
+  auto take_tie = [&](int64_t j, uint32_t key) {
+    return key == kth && (need >= eq_total || ~(uint32_t)j >= jcut);
+  };
+  int eq_take = 0;
+  if (need < eq_total) {
+    each_token([&](int64_t j, float, uint32_t key) {
+      eq_take += __popc(__ballot_sync(0xffffffffu, take_tie(j, key)));
+    });
+  } else {
+    eq_take = eq;
+  }
+  __syncthreads();  // every warp has read the tie counts before they are replaced
+  if (lane == 0) sh_cnt[1][warp] = eq_take;
+  __syncthreads();
+  int take_before = 0;
+  for (int w = 0; w < warp; ++w) take_before += sh_cnt[0][w] + sh_cnt[1][w];
+  int taken = 0;
   const unsigned below = (1u << lane) - 1u;
   each_token([&](int64_t j, float p, uint32_t key) {
-    const bool is_eq = key == kth;
-    const unsigned eq_b = __ballot_sync(0xffffffffu, is_eq);
-    const bool take = key > kth || (is_eq && eq_before + eq_seen + __popc(eq_b & below) < need);
+    const bool take = key > kth || take_tie(j, key);
     const unsigned tk_b = __ballot_sync(0xffffffffu, take);
     if (take) {
       const int slot = take_before + taken + __popc(tk_b & below);
       if (slot < k) out[slot] = Cand{p > 0.f ? m + logf(p) : -INFINITY, (int32_t)j};
     }
     taken += __popc(tk_b);
-    eq_seen += __popc(eq_b);
   });
 }
 

@@ -292,6 +292,8 @@ def test_phase_timing_levels():
     w = W.scaled(BASE_BATCH, V=8192, d=512, B=2)
     case = GpuCase(w)
     sampler = case.sampler
+    for _ in range(5):  # first launches of a fresh sampler are not representative
+        case.run_step(case.state())
     totals = {}
     for level, coarse in ((1, False), (2, True)):
         sampler.set_phase_timing(True, coarse=coarse)
@@ -309,3 +311,24 @@ def test_phase_timing_levels():
     assert abs(totals[1] - totals[2]) <= 0.25 * totals[1]
     lib = C.load_library()
     assert lib.ds_sampler_set_phase_timing(sampler.handle, 3) == C.DS_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("V,d", [(4096, 256), (264192, 64)], ids=["v4096", "v264192_fallback"])
+def test_topk_uniform_logits_take_the_lowest_tokens(V, d):
+    # H = 0: every logit ties, so the top 8 are tokens 0..7 (ties go to the lower token), each
+    # with probability 1/8 after truncation, and the Gumbel draws decide among them exactly as in
+    # the oracle. At V = 264192 the 2064 segments all reach the floor: more than the candidate
+    # list holds, so the selection scans the segment maxima instead.
+    from dataclasses import replace
+    w = replace(W.scaled(BASE_PEAKED, V=V, d=d, B=1), top_k=8)
+    inp = W.make_inputs(w)
+    inp["H"] = np.zeros_like(inp["H"])
+    case = GpuCase(w, inputs=inp, impl="tensor")
+    state = case.state()
+    pre = state_np(state)
+    g = out_np(case.run_step(state))
+    assert np.all((g["sampled"] >= 0) & (g["sampled"] < 8))
+    np.testing.assert_allclose(g["conf"], 1.0 / 8, rtol=1e-6)
+    pos = np.arange(0, w.L, 8)
+    ref = oracle_step(case, pre, positions=pos)
+    assert np.array_equal(g["sampled"][0, pos], ref["sampled"][0, pos])
