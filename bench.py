@@ -150,10 +150,13 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# the files each tensor-core kernel is compiled from (its own file first)
 KERNEL_SOURCES = {
-    k: [os.path.join(ROOT, "canvas_sampler_gb300", "csrc", f)
-        for f in (main, "ds_tc_common.cuh", "ds_common.cuh")]
-    for k, main in (("vocab_pass", "ds_tc_fused.cu"), ("selfcond", "ds_tc_selfcond.cu"))}
+    k: [os.path.join(ROOT, "canvas_sampler_gb300", "csrc", f) for f in files]
+    for k, files in (
+        ("vocab_pass", ("ds_tc_fused.cu", "ds_tc_common.cuh", "ds_internal.h", "ds_common.cuh")),
+        ("selfcond", ("ds_tc_selfcond.cu", "ds_sample.cuh", "ds_tc_common.cuh", "ds_internal.h",
+                      "ds_common.cuh")))}
 
 
 def kernel_source_hash(kernel: str = "vocab_pass") -> str:

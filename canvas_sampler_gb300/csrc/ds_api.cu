@@ -69,6 +69,10 @@ struct ds_sampler {
   float* mref = nullptr;     // fused pass: reference maxima of the range partials [Q, B*L]
   uint32_t* vp_sync = nullptr;
   uint32_t* err = nullptr;
+  // tensor-core step without top-k: the Gumbel race runs inside the self-conditioning launch
+  // (off with DS_GUMBEL_IN_SELFCOND=0: a launch of its own), with its queue counters gq[2]
+  bool gumbel_in_sc = false;
+  uint32_t* gq = nullptr;
   int32_t* iter = nullptr;
   int last_batch = 0;
   // device staging for ds_sampler_step_host (allocated on first use)
@@ -180,7 +184,7 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
     launch_row_merge(s->seg, (int)(V / kVpSegment), R, L, a->done, s->rs, st);
     mark(s, 1, st);
     mark(s, 2, st);
-    launch_gumbel_seg(s->Phi, s->Plo, s->seg, s->rs, R, V, L, a->done, a->step, a->seed, s->blk,
+    launch_gumbel_items(s->Phi, s->Plo, s->seg, s->rs, R, V, L, a->done, a->step, a->seed, s->blk,
                       false, s->best, st);
     mark(s, 3, st);
     mark(s, 4, st);
@@ -202,19 +206,23 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
     if (k > 0)
       launch_topk_row(s->Phi, s->Plo, s->cs, s->mseg_t, s->rs, R, V, L, a->done, k, s->cand, st);
     mark(s, 2, st);
-    if (k == 0)
-      launch_gumbel_seg(s->Phi, s->Plo, s->cs, s->rs, R, V, L, a->done, a->step, a->seed, s->blk,
+    const bool race_in_sc = k == 0 && s->gumbel_in_sc;
+    if (k == 0 && !race_in_sc)
+      launch_gumbel_items(s->Phi, s->Plo, s->cs, s->rs, R, V, L, a->done, a->step, a->seed, s->blk,
                         true, s->best, st);
     mark(s, 3, st);
+    const GumbelWork gw{s->Phi, s->Plo, s->cs, s->rs, a->done,     a->step, s->blk,
+                        a->seed, s->best, s->gq, R,    L,       s->n_chunks, 1};
     e = launch_selfcond_tc(s->Phi, s->Plo, static_cast<const uint16_t*>(a->E), R, V, d, L,
-                           a->done, S, s->Opart, s->mseg_t, s->mref, s->err, st);
+                           a->done, S, s->Opart, s->mseg_t, s->mref, s->err,
+                           race_in_sc ? &gw : nullptr, st);
     if (e != cudaSuccess) return cuda_status(e);
     mark(s, 4, st);
     // with top-k the candidate pool of a row is its k candidates (one "chunk")
     launch_finalize_with_s(s->rs, s->best, k > 0 ? s->cand : nullptr, k > 0 ? 1 : s->n_chunks, k,
                            R, L, a->done, a->step, a->seed, s->blk, a->sampled, a->conf,
                            a->entropy, a->argmax, s->Opart, S, d, a->s, s->mref, st);
-    s->launches += 5;
+    s->launches += race_in_sc ? 4 : 5;
   } else {
     launch_logits_simt(a->H, a->E, fp32, R, V, d, L, T, a->done, s->Y, st);
     mark(s, 0, st);
@@ -397,6 +405,10 @@ ds_status ds_sampler_create(const ds_sampler_config* cfg, ds_sampler** out) {
     // producer / consumer split of the fused pass (a tuning knob; 0 = in proportion to work)
     if (const char* env = getenv("DS_VP_PRODUCERS")) s->vp_producers = atoi(env);
   }
+  if (s->impl == DS_IMPL_TENSOR) {
+    const char* env = getenv("DS_GUMBEL_IN_SELFCOND");
+    s->gumbel_in_sc = !(env && env[0] == '0');
+  }
   size_t opart = 0, nref = 0;
   for (int b = 1; b <= c.max_batch; ++b) {
     const size_t Rb = (size_t)b * c.canvas_len;
@@ -437,7 +449,9 @@ ds_status ds_sampler_create(const ds_sampler_config* cfg, ds_sampler** out) {
   s->err = carve<uint32_t>(s, 4, &e);
   s->iter = carve<int32_t>(s, 4, &e);
   s->blk = carve<int32_t>(s, 4, &e);
+  s->gq = carve<uint32_t>(s, 4, &e);
   if (e == cudaSuccess) e = cudaMemset(s->err, 0, 4 * sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMemset(s->gq, 0, 4 * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(s->blk, 0, 4 * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s->capture_stream, cudaStreamNonBlocking);
   if (e != cudaSuccess) {

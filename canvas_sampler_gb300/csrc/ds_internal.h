@@ -70,10 +70,29 @@ void launch_finalize_with_s(const RowStat* rs, const Best* best, const Cand* can
                             uint64_t seed, const int32_t* blk, int32_t* sampled, float* conf,
                             float* entropy, int32_t* argmax, const float* Opart, int S, int d,
                             float* s, const float* mref, cudaStream_t st);
+// The Gumbel race of a step over (row, 8192-token chunk) items, each raced by one warp (see
+// gumbel_chunk_warp). As a queue (inside the self-conditioning launch): ctr[0] is the next item,
+// ctr[1] counts the CTAs of the launch that have finished; the last CTA returns both to zero, so
+// they are zero between launches (zero them once when allocated).
+struct GumbelWork {
+  const uint16_t* Phi;
+  const uint16_t* Plo;
+  const ChunkStat* seg;  // segment statistics [R, V/128]
+  const RowStat* rs;
+  const uint8_t* done;
+  const int32_t* step;
+  const int32_t* blk;
+  uint64_t seed;
+  Best* best;  // [R, n_chunks]
+  uint32_t* ctr;
+  int R, L, n_chunks;
+  int tile_ref;  // probabilities relative to 256-token tile maxima (else to segment maxima)
+};
+
 // Gumbel-max sample per (row, chunk) from probabilities stored relative to each 128-token
 // segment's maximum (tile_ref = false, the fused pass) or to the maximum over each 256-token
 // tile (tile_ref = true), with the segment statistics seg [R, V/128] (Best records).
-void launch_gumbel_seg(const uint16_t* Phi, const uint16_t* Plo, const ChunkStat* seg,
+void launch_gumbel_items(const uint16_t* Phi, const uint16_t* Plo, const ChunkStat* seg,
                        const RowStat* rs, int R, int64_t V, int L, const uint8_t* done,
                        const int32_t* step, uint64_t seed, const int32_t* blk, bool tile_ref,
                        Best* best, cudaStream_t st);
@@ -167,9 +186,12 @@ void launch_standin_gather(const float* s_prev, const uint16_t* E, const int32_t
 // With mtile_t set, P is relative to the row's maximum over each 256-token tile (mtile_t
 // [V/256, R]) and the reference maximum of each split's partial goes to mref [S, R] (see
 // ds_tc_selfcond.cu).
+// With gw (not nullptr; tensor-core step without top-k) the same launch also runs the Gumbel race
+// of the step (the work of launch_gumbel_items with tile_ref) on warps of its own beside the GEMM.
 cudaError_t launch_selfcond_tc(const uint16_t* Phi, const uint16_t* Plo, const uint16_t* E, int R,
                                int64_t V, int d, int L, const uint8_t* done, int S, float* Opart,
-                               const float* mtile_t, float* mref, uint32_t* err, cudaStream_t st);
+                               const float* mtile_t, float* mref, uint32_t* err,
+                               const GumbelWork* gw, cudaStream_t st);
 // Split count of the tensor-core self-conditioning GEMM for a shape.
 int selfcond_tc_splits(int R, int64_t V, int d, int num_sms);
 

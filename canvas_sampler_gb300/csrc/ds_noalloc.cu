@@ -153,7 +153,7 @@ extern "C" ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg,
   launch_convert(Y, rs, R, V, L, a->done, a->step, a->seed, nullptr, k == 0, Phi, Plo, best, s);
   if (tensor) {
     if (launch_selfcond_tc(Phi, Plo, static_cast<const uint16_t*>(a->E), R, V, d, L, a->done, S,
-                           Opart, nullptr, nullptr, err, s) != cudaSuccess)
+                           Opart, nullptr, nullptr, err, nullptr, s) != cudaSuccess)
       return DS_ERR_CUDA;
   } else {
     launch_selfcond_simt(Phi, Plo, a->E, fp32, R, V, d, L, a->done, S, Opart, s);

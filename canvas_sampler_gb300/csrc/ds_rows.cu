@@ -359,90 +359,17 @@ __global__ void __launch_bounds__(kThreads, 4) k_convert(const float* __restrict
   }
 }
 
-// Gumbel-max over stored probabilities, one CTA per (row, 8192-token chunk): the chunk's winner
-// of the exponential race argmin_j E_j / p_j (the form of k_convert) with
-// p_j = (P_hi + P_lo)[j] exp(m_ref - m), where m_ref is the maximum the probabilities were taken
-// against (of token j's 128-token segment, or with tile_ref of its 256-token tile, i.e. of the
-// segment pair) and m the row maximum. A segment whose maximum is more than kGumbelReach below m
-// cannot hold the winner and is skipped without reading its probabilities. The winner's y - m is
-// returned as ln p_j (p_j carries ~17 significant bits: hi + lo is exact in fp32), with
-// Best::rel = 1. Latency-bound (fixed-latency dependences of the Philox rounds): four CTAs per SM
-// (64 registers) measured faster than three (80) or five (48).
-__global__ void __launch_bounds__(kThreads, 4) k_gumbel_seg(
-    const uint16_t* __restrict__ Phi, const uint16_t* __restrict__ Plo,
-    const ChunkStat* __restrict__ seg, const RowStat* __restrict__ rs, int64_t V, int L,
-    const uint8_t* __restrict__ done, const int32_t* __restrict__ step, uint64_t seed,
-    const int32_t* blk, int tile_ref, Best* __restrict__ best, int n_chunks) {
-  // each thread: kGroups8 groups of 8 tokens, in pairs of adjacent groups (16 tokens)
-  constexpr int kSegTok = 128, kGroups8 = kChunk / 8 / kThreads;
-  __shared__ float sh_scale[kChunk / kSegTok];
-  __shared__ float shv[32], shy;
-  __shared__ int32_t shj[32];
+// Gumbel-max over stored probabilities as a launch of its own (the fused vocabulary pass; the
+// tensor-core step runs the same race inside its self-conditioning launch): one warp per
+// (row, 8192-token chunk) item, gumbel_chunk_warp (ds_sample.cuh).
+__global__ void __launch_bounds__(kThreads) k_gumbel_items(const __grid_constant__ GumbelWork g,
+                                                           int64_t V) {
   pdl_wait();
-  const int c = blockIdx.x, r = blockIdx.y;
-  const int b = r / L, i = r % L;
-  if (done && done[b]) return;
-  const float m = rs[r].m;
-  const int64_t j0 = (int64_t)c * kChunk, j1 = min(V, j0 + kChunk);
-  const int nseg = (int)((j1 - j0) / kSegTok);
-  bool reach = false;
-  if ((int)threadIdx.x < nseg) {
-    const ChunkStat* sg = seg + (size_t)r * (V / kSegTok) + j0 / kSegTok;
-    const float mg = sg[threadIdx.x].m;
-    // chunks and tiles start at multiples of 256 tokens, so segment pairs (2u, 2u + 1) are tiles
-    const float mref = tile_ref ? fmaxf(mg, sg[threadIdx.x ^ 1].m) : mg;
-    reach = mg >= m - kGumbelReach;
-    sh_scale[threadIdx.x] = reach ? expf(mref - m) : 0.f;
-  }
-  if (!__syncthreads_or(reach)) {  // no token of the chunk can win
-    if (threadIdx.x == 0) best[(size_t)r * n_chunks + c] = Best{-INFINITY, INT_MAX, 0.f, 1};
-    return;
-  }
-  const uint32_t st = (uint32_t)step[b];
-  const uint16_t* ph = Phi + (size_t)r * V;
-  const uint16_t* pl = Plo + (size_t)r * V;
-  float kbest = INFINITY, bp = 1.f;
-  int32_t bj = INT_MAX;
-  uint4 h[kGroups8], lo[kGroups8];
-  float sc[kGroups8];
-  // group k of thread t is group 2 t + (k & 1) + 2 kThreads (k >> 1) of the chunk, so a thread's
-  // pairs are 16 consecutive tokens and a warp covers 512 consecutive tokens
-#pragma unroll
-  for (int k = 0; k < kGroups8; ++k) {  // all loads first
-    const int g = 2 * threadIdx.x + (k & 1) + 2 * kThreads * (k >> 1);
-    const int64_t j = j0 + 8 * (int64_t)g;
-    sc[k] = j < j1 ? sh_scale[g >> 4] : 0.f;
-    if (sc[k] > 0.f) {
-      h[k] = __ldcs(reinterpret_cast<const uint4*>(ph + j));
-      lo[k] = __ldcs(reinterpret_cast<const uint4*>(pl + j));
-    } else {
-      h[k] = make_uint4(0u, 0u, 0u, 0u);
-      lo[k] = h[k];
-    }
-  }
-  const uint32_t sid = stream_id((uint32_t)b, blk);
-  // every lane races its first four tokens in full; the warp's best key so far then cuts the
-  // rest (refreshed after each 16 tokens), so few lanes reach the logarithm
-  if (sc[0] > 0.f)
-    gumbel_seed4(h[0], lo[0], sc[0], j0 + 16 * (int64_t)threadIdx.x, (uint32_t)i, sid, st, seed,
-                 kbest, bj, bp);
-  float cut = warp_min(kbest);
-#pragma unroll
-  for (int k = 0; k < kGroups8; k += 2) {
-    if (sc[k] > 0.f || sc[k + 1] > 0.f) {
-      const int64_t j = j0 + 8 * (int64_t)(2 * threadIdx.x + 2 * kThreads * (k >> 1));
-      if (k == 0)
-        gumbel_race16<true>(h[k], lo[k], sc[k], h[k + 1], lo[k + 1], sc[k + 1], j, (uint32_t)i,
-                            sid, st, seed, cut, kbest, bj, bp);
-      else
-        gumbel_race16(h[k], lo[k], sc[k], h[k + 1], lo[k + 1], sc[k + 1], j, (uint32_t)i, sid,
-                      st, seed, cut, kbest, bj, bp);
-    }
-    cut = warp_min(fminf(cut, kbest));
-  }
-  float v = -kbest, y = logf(bp);
-  block_best(v, bj, y, shv, shj, &shy);
-  if (threadIdx.x == 0) best[(size_t)r * n_chunks + c] = Best{v, bj, y, 1};
+  const int w = blockIdx.x * (kThreads / 32) + (int)(threadIdx.x >> 5);
+  if (w >= g.R * g.n_chunks) return;
+  const int r = w / g.n_chunks, c = w % g.n_chunks;
+  if (g.done && g.done[r / g.L]) return;
+  gumbel_chunk_warp(g, V, r, c);
 }
 
 // The k largest logits of a chunk (ties toward lower tokens), written in token order.
@@ -1208,13 +1135,15 @@ void launch_finalize_with_s(const RowStat* rs, const Best* best, const Cand* can
            seed, blk, sampled, conf, entropy, argmax, Opart, S, R, d, s, mref);
 }
 
-void launch_gumbel_seg(const uint16_t* Phi, const uint16_t* Plo, const ChunkStat* seg,
+void launch_gumbel_items(const uint16_t* Phi, const uint16_t* Plo, const ChunkStat* seg,
                        const RowStat* rs, int R, int64_t V, int L, const uint8_t* done,
                        const int32_t* step, uint64_t seed, const int32_t* blk, bool tile_ref,
                        Best* best, cudaStream_t st) {
   const int nc = n_chunks_of(V);
-  launch_k(k_gumbel_seg, dim3(nc, R), dim3(kThreads), 0, st, Phi, Plo, seg, rs, V, L, done, step,
-           seed, blk, tile_ref ? 1 : 0, best, nc);
+  const GumbelWork g{Phi, Plo, seg, rs, done, step, blk, seed, best, nullptr, R, L, nc,
+                     tile_ref ? 1 : 0};
+  const int warps = kThreads / 32;
+  launch_k(k_gumbel_items, dim3((R * nc + warps - 1) / warps), dim3(kThreads), 0, st, g, V);
 }
 
 void launch_reduce_s(const float* Opart, int S, int R, int d, int L, const uint8_t* done,

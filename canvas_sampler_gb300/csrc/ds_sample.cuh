@@ -1,8 +1,11 @@
 // Counter-based random draws and the Gumbel-max race of the sampler step (device code used by
-// the row kernels in ds_rows.cu).
+// the row kernels in ds_rows.cu and by the self-conditioning kernel, which runs the race on
+// warps beside its GEMM).
 #pragma once
 
-#include "ds_common.cuh"
+#include <climits>
+
+#include "ds_internal.h"
 
 namespace ds {
 
@@ -103,17 +106,19 @@ DS_DEV void gumbel_token(float pe, uint32_t r, int32_t j, float kc, float& kbest
   }
 }
 
-// p of the 8 tokens of a bf16 hi / lo group (two tokens per word, the lower token in the low
-// half), times the group's scale.
-DS_DEV void unpack_p8(const uint4& hi, const uint4& lo, float sc, float (&p)[8]) {
-  const uint32_t hw[4] = {hi.x, hi.y, hi.z, hi.w};
-  const uint32_t lw[4] = {lo.x, lo.y, lo.z, lo.w};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    p[2 * e] = (__uint_as_float(hw[e] << 16) + __uint_as_float(lw[e] << 16)) * sc;
-    p[2 * e + 1] = (__uint_as_float(hw[e] & 0xFFFF0000u) + __uint_as_float(lw[e] & 0xFFFF0000u)) * sc;
-  }
+// Token e (0..7) of a group of eight bf16 values (two per word, the lower token in the low half)
+// as fp32; e is a constant after unrolling.
+DS_DEV float bf16_at(const uint4& g, int e) {
+  const uint32_t w = e < 2 ? g.x : (e < 4 ? g.y : (e < 6 ? g.z : g.w));
+  return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
 }
+
+// hi is p rounded to bf16, so |lo| <= 2^-8 hi and hi sc (1 + 2^-7), rounded twice, is above
+// (hi + lo) sc rounded: an upper bound of p from the hi half alone.
+constexpr float kHiBound = 1.0078125f;
+// kc (1 + 2^-19), rounded, exceeds kc / (1 - 2^-20): with it the pre-test of gumbel_race16 skips
+// only tokens that gumbel_token would skip.
+constexpr float kCutBound = 1.0000019073486328f;
 
 // The Gumbel-max exponential race over 16 consecutive tokens j .. j + 15 of position i of
 // sequence b: with E_j = -ln u_j (u_j from the Gumbel stream of Philox) and p_j = exp(y_j - m)
@@ -121,24 +126,24 @@ DS_DEV void unpack_p8(const uint4& hi, const uint4& lo, float sc, float (&p)[8])
 // in two groups of eight with scales sa, sb. Tokens are tested against kc = min(kbest, cut),
 // cut being a key some token has already reached (the warp's best so far): a group of four is
 // skipped without its draw when even the smallest E (> 2^-24) over its largest p cannot beat kc,
-// and a token without its logarithm when 1 - u_j proves it cannot; both skips need a strict
-// inequality, so a token tying the best is never skipped. The four draws are computed together.
-// Tokens arrive in increasing j, so a strict comparison keeps the lowest token on ties. With
-// SKIP4 the first four tokens are left out (already raced by gumbel_seed4).
+// and a token without its logarithm when 1 - u_j proves it cannot. Both tests first use the
+// upper bound of p from the hi half (kHiBound); the exact p = (hi + lo) sc is formed only for the
+// tokens that pass, and gumbel_token then decides with it exactly as without the pre-test. Every
+// skip needs a strict inequality, so a token tying the best is never skipped. The four draws are
+// computed together. Tokens arrive in increasing j, so a strict comparison keeps the lowest token
+// on ties. With SKIP4 the first four tokens are left out (already raced by gumbel_seed4).
 template <bool SKIP4 = false>
 DS_DEV void gumbel_race16(const uint4& hia, const uint4& loa, float sa, const uint4& hib,
                           const uint4& lob, float sb, int64_t j, uint32_t i, uint32_t b,
                           uint32_t step, uint64_t seed, float cut, float& kbest, int32_t& bj,
                           float& bp) {
-  float p[16];
+  float pu[16];
   {
-    float pa[8], pb[8];
-    unpack_p8(hia, loa, sa, pa);
-    unpack_p8(hib, lob, sb, pb);
+    const float sau = sa * kHiBound, sbu = sb * kHiBound;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      p[e] = pa[e];
-      p[8 + e] = pb[e];
+      pu[e] = bf16_at(hia, e) * sau;
+      pu[8 + e] = bf16_at(hib, e) * sbu;
     }
   }
   bool need[4];
@@ -146,7 +151,7 @@ DS_DEV void gumbel_race16(const uint4& hia, const uint4& loa, float sa, const ui
   const float kc0 = fminf(kbest, cut);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const float pm = fmaxf(fmaxf(p[4 * q], p[4 * q + 1]), fmaxf(p[4 * q + 2], p[4 * q + 3]));
+    const float pm = fmaxf(fmaxf(pu[4 * q], pu[4 * q + 1]), fmaxf(pu[4 * q + 2], pu[4 * q + 3]));
     need[q] = !(SKIP4 && q == 0) && !(5.9604645e-8f >= kc0 * pm);
     any |= need[q];
   }
@@ -159,12 +164,17 @@ DS_DEV void gumbel_race16(const uint4& hia, const uint4& loa, float sa, const ui
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     if (!need[q]) continue;
+    const float kcs = fminf(kbest, cut) * kCutBound;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float pe = p[4 * q + e];
+      const int t = 4 * q + e;
+      const uint32_t r = word_of(w[q], e);
+      const float f = __uint_as_float(0x3F800000u | (r >> 9));
+      if ((2.0f - f) - 5.9604644775390625e-8f > kcs * pu[t]) continue;
+      const float pe = t < 8 ? (bf16_at(hia, t) + bf16_at(loa, t)) * sa
+                             : (bf16_at(hib, t - 8) + bf16_at(lob, t - 8)) * sb;
       if (!(pe > 0.f)) continue;
-      gumbel_token(pe, word_of(w[q], e), (int32_t)(j + 4 * q + e), fminf(kbest, cut), kbest, bj,
-                   bp);
+      gumbel_token(pe, r, (int32_t)(j + t), fminf(kbest, cut), kbest, bj, bp);
     }
   }
 }
@@ -175,13 +185,164 @@ DS_DEV void gumbel_race16(const uint4& hia, const uint4& loa, float sa, const ui
 DS_DEV void gumbel_seed4(const uint4& hi, const uint4& lo, float sc, int64_t j, uint32_t i,
                          uint32_t b, uint32_t step, uint64_t seed, float& kbest, int32_t& bj,
                          float& bp) {
-  float p[8];
-  unpack_p8(hi, lo, sc, p);
   u32x4 w[1] = {u32x4{(uint32_t)(j >> 2), i, b, (step << 2) | kGumbelStream}};
   philox4x32_10_n<1>(w, (uint32_t)seed, (uint32_t)(seed >> 32));
 #pragma unroll
-  for (int e = 0; e < 4; ++e)
-    if (p[e] > 0.f) gumbel_token(p[e], word_of(w[0], e), (int32_t)(j + e), INFINITY, kbest, bj, bp);
+  for (int e = 0; e < 4; ++e) {
+    const float pe = (bf16_at(hi, e) + bf16_at(lo, e)) * sc;
+    if (pe > 0.f) gumbel_token(pe, word_of(w[0], e), (int32_t)(j + e), INFINITY, kbest, bj, bp);
+  }
+}
+
+// ----------------------------------------------------------------------------------------
+// The race over one (row, 8192-token chunk) by one warp
+// ----------------------------------------------------------------------------------------
+// Sixteen consecutive tokens of one lane: two groups of eight (bf16 hi and lo) with the scale of
+// their segment (0: nothing to race, nothing loaded).
+struct Slab16 {
+  uint4 h0, h1, l0, l1;
+  float sc;
+};
+
+DS_DEV void slab_load(Slab16& t, const uint16_t* ph, const uint16_t* pl, float sc) {
+  t.sc = sc;
+  if (sc > 0.f) {
+    t.h0 = __ldcs(reinterpret_cast<const uint4*>(ph));
+    t.h1 = __ldcs(reinterpret_cast<const uint4*>(ph + 8));
+    t.l0 = __ldcs(reinterpret_cast<const uint4*>(pl));
+    t.l1 = __ldcs(reinterpret_cast<const uint4*>(pl + 8));
+  } else {
+    t.h0 = t.h1 = t.l0 = t.l1 = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// Position of the n-th set bit (from 0) of m, n < popc(m): halving search on population counts.
+DS_DEV int nth_set_bit(uint32_t m, int n) {
+  int pos = 0;
+#pragma unroll
+  for (int w = 16; w; w >>= 1) {
+    const int c = __popc(m & ((1u << w) - 1u));
+    if (n >= c) {
+      n -= c;
+      m >>= w;
+      pos += w;
+    }
+  }
+  return pos;
+}
+
+// Winner of the exponential race over chunk c of row r, p_j = (P_hi + P_lo)[j] exp(m_ref - m)
+// with m the row maximum and m_ref the maximum the probabilities were taken against: of token j's
+// 128-token segment, or with tile_ref of its 256-token tile (the larger of the two segment
+// maxima). The record is the chunk's argmin of E_j / p_j (lowest token on equal keys): skipped
+// segments and skipped draws are exactly those that cannot win. Segments more than kGumbelReach
+// below m are not read; the others are raced four at a time in token order (lane l takes
+// tokens 16 (l % 8) .. 16 (l % 8) + 15 of the (4 k + l / 8)-th segment in reach in round k), the
+// next round loaded while the current one is raced. The lanes race the first round's first four
+// tokens in full, and the warp's best key then cuts the rest of the chunk.
+DS_DEV void gumbel_chunk_warp(const GumbelWork& g, int64_t V, int r, int c) {
+  constexpr int kSegTok = 128;
+  const int lane = threadIdx.x & 31;
+  const int b = r / g.L, i = r % g.L;
+  const float m = g.rs[r].m;
+  const int64_t j0 = (int64_t)c * kChunk, j1 = min(V, j0 + kChunk);
+  const int nseg = (int)((j1 - j0) / kSegTok);  // whole segments: V is a multiple of 256
+  const ChunkStat* sg = g.seg + (size_t)r * (V / kSegTok) + j0 / kSegTok;
+  // segment scales: lane l holds segments l and l + 32 of the chunk
+  float sc[2];
+  uint32_t in[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int u = lane + 32 * h;
+    float v = 0.f;
+    if (u < nseg) {
+      const float mg = sg[u].m;
+      // chunks start at multiples of 256 tokens, so segment pairs (2w, 2w + 1) are tiles
+      if (mg >= m - kGumbelReach) v = expf((g.tile_ref ? fmaxf(mg, sg[u ^ 1].m) : mg) - m);
+    }
+    sc[h] = v;
+    in[h] = __ballot_sync(0xffffffffu, v > 0.f);
+  }
+  const int n0 = __popc(in[0]), n_in = n0 + __popc(in[1]);
+  Best* out = g.best + (size_t)r * g.n_chunks + c;
+  if (n_in == 0) {  // no token of the chunk can win
+    if (lane == 0) *out = Best{-INFINITY, INT_MAX, 0.f, 1};
+    return;
+  }
+  // this lane's 16 tokens in round k (offset in the chunk) and their scale (0: none)
+  auto locate = [&](int k, float& s) -> int {
+    const int n = 4 * k + (lane >> 3);
+    int u = 0;
+    if (n < n_in) u = n < n0 ? nth_set_bit(in[0], n) : 32 + nth_set_bit(in[1], n - n0);
+    const float a0 = __shfl_sync(0xffffffffu, sc[0], u & 31);
+    const float a1 = __shfl_sync(0xffffffffu, sc[1], u & 31);
+    s = n < n_in ? (u < 32 ? a0 : a1) : 0.f;
+    return kSegTok * u + 16 * (lane & 7);
+  };
+  const uint32_t st = (uint32_t)g.step[b];
+  const uint32_t sid = stream_id((uint32_t)b, g.blk);
+  const uint16_t* ph = g.Phi + (size_t)r * V + j0;
+  const uint16_t* pl = g.Plo + (size_t)r * V + j0;
+  const int rounds = (n_in + 3) / 4;
+  float kbest = INFINITY, bp = 1.f, cut, s;
+  int32_t bj = INT_MAX;
+  Slab16 cur, nxt;
+  int off = locate(0, s);
+  slab_load(cur, ph + off, pl + off, s);
+  for (int k = 0; k < rounds; ++k) {
+    int off_n = 0;
+    if (k + 1 < rounds) {
+      off_n = locate(k + 1, s);
+      slab_load(nxt, ph + off_n, pl + off_n, s);
+    }
+    const int64_t j = j0 + off;
+    if (k == 0) {
+      if (cur.sc > 0.f)
+        gumbel_seed4(cur.h0, cur.l0, cur.sc, j, (uint32_t)i, sid, st, g.seed, kbest, bj, bp);
+      cut = warp_min(kbest);
+      if (cur.sc > 0.f)
+        gumbel_race16<true>(cur.h0, cur.l0, cur.sc, cur.h1, cur.l1, cur.sc, j, (uint32_t)i, sid,
+                            st, g.seed, cut, kbest, bj, bp);
+    } else if (cur.sc > 0.f) {
+      gumbel_race16(cur.h0, cur.l0, cur.sc, cur.h1, cur.l1, cur.sc, j, (uint32_t)i, sid, st,
+                    g.seed, cut, kbest, bj, bp);
+    }
+    cut = warp_min(fminf(cut, kbest));
+    cur = nxt;
+    off = off_n;
+  }
+  // the warp's winner: largest -key, then lowest token; its p comes from the lane that holds it
+  float v = -kbest;
+  int32_t jw = bj;
+  warp_best(v, jw);
+  const uint32_t owner = __ballot_sync(0xffffffffu, bj == jw);
+  const float pw = __shfl_sync(0xffffffffu, bp, __ffs(owner) - 1);
+  if (lane == 0) *out = Best{v, jw, logf(pw), 1};
+}
+
+// One warp's share of the queue of (row, chunk) items: items are taken one at a time until the
+// queue is empty; finished sequences' items are skipped (their records are not written).
+DS_DEV void gumbel_queue_warp(const GumbelWork& g, int64_t V) {
+  const uint32_t n_items = (uint32_t)g.R * (uint32_t)g.n_chunks;
+  for (;;) {
+    uint32_t it = 0;
+    if ((threadIdx.x & 31) == 0) it = atomicAdd(g.ctr, 1u);
+    it = __shfl_sync(0xffffffffu, it, 0);
+    if (it >= n_items) return;
+    const int r = (int)(it / (uint32_t)g.n_chunks), c = (int)(it % (uint32_t)g.n_chunks);
+    if (g.done && g.done[r / g.L]) continue;
+    gumbel_chunk_warp(g, V, r, c);
+  }
+}
+
+// After every warp of the CTA has left gumbel_queue_warp (a __syncthreads in between), one
+// thread of each CTA: the last CTA of the grid returns the queue counters to zero.
+DS_DEV void gumbel_queue_release(const GumbelWork& g) {
+  __threadfence();
+  if (atomicAdd(g.ctr + 1, 1u) == gridDim.x - 1) {
+    atomicExch(g.ctr, 0u);
+    atomicExch(g.ctr + 1, 0u);
+  }
 }
 
 }  // namespace ds

@@ -22,7 +22,7 @@
 //     afterwards (k_finalize), so s does not depend on timing.
 // CTAs with blockIdx.x < producers start on the producer queue and move to the consumer queue
 // when it runs dry. The Gumbel-max sample is drawn afterwards from the stored probabilities
-// (k_gumbel_seg, ds_rows.cu).
+// (k_gumbel_items, ds_rows.cu).
 //
 // Definitions: DiffusionGemma Technical Report, section 6 "Sampling" (full-precision softmax
 // over the vocabulary and the self-conditioning embedding matmul).

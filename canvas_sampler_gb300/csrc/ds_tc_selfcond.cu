@@ -9,8 +9,13 @@
 // is stored beside the partial, O_s = sum_t exp(m_t - M_s) sum_{j in t} P_t[r, j] E[j, n].
 // Definitions: DiffusionGemma Technical Report, section 6 "Sampling" (the self-conditioning
 // embedding matmul, in full precision). Pipeline structure: ds_tc_common.cuh.
+// With Gumbel work the kernel also runs the step's Gumbel-max race (ds_sample.cuh): the GEMM is
+// bound by the tensor pipe and leaves the SM's issue slots mostly idle, so two warps of its own
+// race (row, chunk) items from a queue from the start, and every other warp joins the queue once
+// its part of the GEMM is done (all warps of a CTA without a GEMM item race from the start).
 #include <algorithm>
 
+#include "ds_sample.cuh"
 #include "ds_tc_common.cuh"
 
 namespace ds {
@@ -26,15 +31,17 @@ constexpr uint32_t SC_A_BYTES = SC_BM * SC_BK * 2;        // one of hi / lo
 constexpr uint32_t SC_BOX_BYTES = 64 * SC_BK * 2;          // 64 d-columns x 64 tokens
 constexpr uint32_t SC_STAGE_BYTES = 2 * SC_A_BYTES + (SC_BN_MAX / 64) * SC_BOX_BYTES;
 constexpr size_t SC_SMEM = (size_t)SC_STAGES * SC_STAGE_BYTES + 1024;
+// the pipeline's warps (producer, MMA, 8 epilogue) and two racing warps
+constexpr int SC_THREADS = kThreadsTC + 64;
 
 template <int BN, bool SCALED>
-__global__ void __launch_bounds__(kThreadsTC, 1)
+__global__ void __launch_bounds__(SC_THREADS, 1)
     k_selfcond_tc(const __grid_constant__ CUtensorMap mapPhi,
                   const __grid_constant__ CUtensorMap mapPlo,
                   const __grid_constant__ CUtensorMap mapE, int R, int64_t V, int d, int L,
                   int S, int kb_per_split, const uint8_t* __restrict__ done,
                   float* __restrict__ Opart, const float* __restrict__ mtile_t,
-                  float* __restrict__ mref, uint32_t* err) {
+                  float* __restrict__ mref, uint32_t* err, const __grid_constant__ GumbelWork gw) {
   constexpr int COLS = BN / 2;
   constexpr int CHUNK_KB = SC_CHUNK_KB;  // 4 K blocks = one 256-token tile
   static_assert(CHUNK_KB * SC_BK == 256, "a chunk is one tile of the P reference maxima");
@@ -159,7 +166,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       umma_commit(smem_u32(&ctl.mma_done));
       mbar_wait_quiet(smem_u32(&ctl.mma_done), 0);
     }
-  } else {
+  } else if (warp < 2 + kEpiWarps) {
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
@@ -214,12 +221,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
     }
   }
+  if (gw.best) gumbel_queue_warp(gw, V);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  if (gw.best && threadIdx.x == 0) gumbel_queue_release(gw);
 }
 
 int selfcond_bn(int d) { return d % 256 == 0 ? 256 : (d % 128 == 0 ? 128 : 64); }
@@ -265,7 +274,7 @@ int selfcond_tc_splits(int R, int64_t V, int d, int num_sms) {
 cudaError_t launch_selfcond_tc(const uint16_t* Phi, const uint16_t* Plo, const uint16_t* E, int R,
                                int64_t V, int d, int L, const uint8_t* done, int S, float* Opart,
                                const float* mtile_t, float* mref, uint32_t* err,
-                               cudaStream_t st) {
+                               const GumbelWork* gw, cudaStream_t st) {
   if (!tc_available()) return cudaErrorNotSupported;
   const int bn = selfcond_bn(d);
   CUtensorMap mPh, mPl, mE;
@@ -278,11 +287,14 @@ cudaError_t launch_selfcond_tc(const uint16_t* Phi, const uint16_t* Plo, const u
   int per = (nkb + S - 1) / S;
   if (scaled) per = (per + SC_CHUNK_KB - 1) / SC_CHUNK_KB * SC_CHUNK_KB;  // splits start on a tile
   const int n_items = (R / SC_BM) * (d / bn) * S;
-  const int grid = std::max(1, std::min(n_items, tc_num_sms()));
+  // with the race every SM takes part (CTAs beyond the GEMM items only race)
+  const int grid = gw ? tc_num_sms() : std::max(1, std::min(n_items, tc_num_sms()));
+  GumbelWork g{};
+  if (gw) g = *gw;
   cudaError_t e = cudaSuccess;
 #define DS_SELFCOND_LAUNCH(BN, SC)                                                             \
-  e = launch_k(k_selfcond_tc<BN, SC>, dim3(grid), dim3(kThreadsTC), SC_SMEM, st, mPh, mPl, mE, \
-               R, V, d, L, S, per, done, Opart, mtile_t, mref, err)
+  e = launch_k(k_selfcond_tc<BN, SC>, dim3(grid), dim3(SC_THREADS), SC_SMEM, st, mPh, mPl, mE, \
+               R, V, d, L, S, per, done, Opart, mtile_t, mref, err, g)
   if (scaled) {
     if (bn == 256)
       DS_SELFCOND_LAUNCH(256, true);

@@ -189,6 +189,33 @@ def test_done_sequence_inside_a_pair_tile(done):
     compare_outputs(g, ref, [(live, i) for i in range(w.L)])
 
 
+@pytest.mark.parametrize("done", [(0, 0, 0), (0, 1, 0)])
+def test_race_beside_selfcond_matches_its_own_launch(monkeypatch, done):
+    # the Gumbel race on warps of the self-conditioning launch (the default) against its own
+    # launch: every output and state bit for bit over three steps in a row (the race's queue
+    # counters must be back at zero after each launch); the last chunk is a ragged 256 tokens
+    w = W.scaled(BASE_BATCH, V=41216, d=512, B=3)
+    inp = W.make_inputs(w)
+    inp["done"] = np.array(done, np.uint8)
+    live = [b for b in range(3) if not done[b]]
+    runs = []
+    for env in ("0", "1"):
+        monkeypatch.setenv("DS_GUMBEL_IN_SELFCOND", env)
+        case = GpuCase(w, inputs=inp)
+        state = case.state()
+        steps = []
+        for t in range(3):
+            out = case.run_step(state, seed=inp["seed"] + t)
+            steps.append(({k: v[live] for k, v in out_np(out).items()}, state_np(state)))
+        runs.append(steps)
+    for (o0, s0), (o1, s1) in zip(*runs):
+        for k in o0:
+            assert np.array_equal(o0[k], o1[k]), k
+        for k in s0:
+            assert np.array_equal(s0[k], s1[k]), k
+    assert np.all(runs[1][0][0]["sampled"] >= 0)
+
+
 def test_deterministic_bits():
     w = W.scaled(BASE_PEAKED, V=8192, d=512, B=1)
     case = GpuCase(w)
