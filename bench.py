@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--vocab", type=int, default=None, help="override V (profiling runs)")
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling runs)")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--sustained-seconds", type=float, default=3.0,
+                    help="length of the power-capped sustained pass (0: none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--loop", action="store_true",
                     help="time the whole denoising loop (ds_denoise_loop) of the workload, as a "
@@ -130,7 +132,7 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.t.join(timeout=2)
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
@@ -141,13 +143,20 @@ class ClockSampler:
                 mx.append(float(f[2]))
             except ValueError:
                 continue
+            try:
+                pw.append(float(f[3]))
+            except ValueError:
+                pass
             for n, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm), "sm_max_mhz": max(mx),
+               "reasons": sorted(reasons), "samples": len(sm)}
+        if pw:
+            out["power_w"] = statistics.median(pw)
+        return out
 
 
 # the files each tensor-core kernel is compiled from (its own file first)
@@ -397,6 +406,24 @@ def run_ours(args):
         vp_ach = 4.0 * w.B * w.L * w.V * w.d / (vp_ms / 1e3) / 1e12
         vp = {"bound": "tensor", "ms": vp_ms, "achieved": vp_ach, "peak": peak_tf,
               "unit": "TFLOP/s", "frac": vp_ach / peak_tf, "frac_cap": 2.0 / 3.0}
+    # sustained (last, so that the passes above run on a GPU that has not been throttled):
+    # seconds of back-to-back steps, long enough for the power controller to settle (the timed
+    # region above is a fraction of a second at full clocks)
+    sustained = None
+    if args.sustained_seconds > 0:
+        n_sus = max(1, int(args.sustained_seconds * 1e3 / max(ms / args.steps, 1e-3)))
+        sclk = ClockSampler(clocks.gpu)
+        sclk.start()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s0.record(stream)
+        for _ in range(n_sus):
+            one_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        sus_ms = reduce_max(s0.elapsed_time(s1), dist if world > 1 else None, dev)
+        sustained = {"value": world * n_sus / (sus_ms / 1e3), "unit": "steps/s", "steps": n_sus,
+                     "ms_per_step": sus_ms / n_sus, "clocks": sclk.stop()}
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
@@ -419,6 +446,7 @@ def run_ours(args):
         "e2e": {"value": world * args.e2e_steps / e2e_s, "unit": "steps/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "clocks": clk,
+        "sustained": sustained,
         "device_status": status,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
