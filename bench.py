@@ -385,8 +385,8 @@ def run_ours(args):
     else:
         dom_flops = {"logits": 2.0 * w.B * w.L * w.V * w.d,
                      "selfcond": 2.0 * w.B * w.L * w.V * w.d}.get(dom)
-    # the kernel runs back to back for the whole timed region (seconds under the power cap):
-    # the sustained bf16 peak is its denominator
+    # the kernel runs back to back for the whole timed region, under the power cap: the
+    # sustained bf16 peak is its denominator
     peak_key = "bf16_tflops_sustained" if "bf16_tflops_sustained" in peaks else "bf16_tflops"
     peak_tf = float(peaks.get(peak_key, FALLBACK_PEAKS[peak_key]))
     roof = None
@@ -396,6 +396,10 @@ def run_ours(args):
         roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": ach / peak_tf, "traffic": traffic,
                 "peak_source": f"{peak_key} ({peak_src})"}
+        if (dom == "selfcond" and sampler.impl == "tensor" and w.top_k == 0
+                and os.environ.get("DS_GUMBEL_IN_SELFCOND", "1") != "0"):
+            roof["note"] = ("the launch also runs the step's Gumbel-max race on warps of its own; "
+                            "only the GEMM's 2 B L V d FLOP are counted")
     # the vocabulary pass (both GEMMs with the epilogues fused into them: the logits and
     # self-conditioning phases, or the fused kernel) against the tensor roofline of its
     # 4 B L V d algorithmic FLOP; the bf16 hi/lo split makes its tensor work 6 B L V d, so no

@@ -131,3 +131,72 @@ def test_adaptive_topk_standin_loop_full_size():
                                   case.inp["seed"], top_k=w.top_k, max_steps=w.max_steps,
                                   positions=pos)
         compare_outputs(g, ref, [(b, int(i)) for i in pos], top_k=w.top_k)
+
+
+def test_largest_vocabulary_closed_form():
+    """V = 2^24, the largest vocabulary the boundary accepts (d = 256, one canvas). E is zero
+    except unit rows at K special tokens (first and last tokens, chunk and tile edges), and
+    H_i = a_i e_k(i), so each position has exactly one hot token with logit a_i and 2^24 - 1
+    tokens at 0: the softmax, entropy, argmax, confidences and s have closed forms for every
+    position, and the oracle's Philox gives the exact Gumbel-max winner (no matmul) for a sample
+    of positions. Logits above 19.6 put every other segment out of the race's reach; the others
+    race all 2^24 tokens."""
+    V, d, L, T = 1 << 24, 256, 256, 1.0
+    special = np.array([0, 5, 8191, 8192, 262143, 1 << 23, 12345678, V - 256, V - 1], np.int64)
+    K = len(special)
+    a_vals = np.array([-5.0, 0.0, 3.0, 10.0, 17.0, 25.0, 40.0])
+    k_of = np.arange(L) % K
+    a = a_vals[np.arange(L) % len(a_vals)]
+    E = torch.zeros(V, d, dtype=torch.bfloat16, device="cuda")
+    E[torch.from_numpy(special).cuda(), torch.arange(K, device="cuda")] = 1.0
+    Hn = np.zeros((1, L, d), np.float32)
+    Hn[0, np.arange(L), k_of] = a
+    H = torch.from_numpy(Hn).to(torch.bfloat16).cuda()
+    seed = 20240601
+    Tt = torch.full((1,), T, dtype=torch.float32, device="cuda")
+    tau = torch.full((1,), 0.9, dtype=torch.float32, device="cuda")
+    from canvas_sampler_gb300.sampler import CanvasState, Sampler
+    sampler = Sampler(V, d, canvas_len=L, max_batch=1, dtype="bf16", max_steps=48)
+    assert sampler.impl == "tensor"
+    rng = np.random.default_rng(3)
+    canvas = rng.integers(0, V, size=(1, L), dtype=np.int32)
+    state = CanvasState.from_numpy(canvas, np.zeros((1, L), np.uint8), np.zeros(1, np.int32),
+                                   np.zeros(1, np.uint8))
+    out = sampler.step(H, E, Tt, tau, state, seed)
+    torch.cuda.synchronize()
+    g = out_np(out)
+    del E
+    # closed forms (fp64)
+    hot = special[k_of]
+    m = np.maximum(a, 0.0)
+    l = np.exp(a - m) + (V - 1) * np.exp(-m)
+    p_hot, p_oth = np.exp(a - m) / l, np.exp(-m) / l
+    ent = -(p_hot * np.log(p_hot) + (V - 1) * p_oth * np.log(p_oth))
+    s_ref = np.tile(p_oth[:, None], (1, d))
+    s_ref[:, K:] = 0.0
+    s_ref[np.arange(L), k_of] = p_hot
+    # ties at 0 go to the lowest token: token 0 unless it is the hot token below 0
+    arg_ref = np.where(a > 0, hot, np.where((a < 0) & (hot == 0), 1, 0))
+    assert np.array_equal(g["argmax"][0], arg_ref)
+    assert np.all(np.abs(g["entropy"][0] - ent) <= 2e-5 * np.maximum(1.0, ent))
+    err = np.linalg.norm(g["s"][0] - s_ref, axis=1) / np.linalg.norm(s_ref, axis=1)
+    assert err.max() <= 2e-5, err.max()
+    # every sample is the hot token or a 0-logit token; its confidence is the matching p
+    x = g["sampled"][0]
+    c_ref = np.where(x == hot, p_hot, p_oth)
+    assert np.all(np.abs(g["conf"][0] - c_ref) <= 2e-5 * c_ref)
+    # exact winners for a sample of positions, one per logit value. With 2^24 draws of a 24-bit
+    # uniform about two tokens share the largest draw, so exact ties of the top perturbed logits
+    # are common here; they go to the lowest token on both sides and are checked too. Only
+    # near-ties (a nonzero margin below 1e-4) are left out.
+    checked = 0
+    for i in range(len(a_vals)):
+        u = oracle.gumbel_uniforms(seed, 0, [i], 0, V)[0]
+        v = -np.log(-np.log(u))
+        v[hot[i]] += a[i]
+        top2 = np.partition(v, -2)[-2:]
+        if 0.0 < top2[1] - top2[0] < 1e-4:
+            continue
+        assert x[i] == int(np.argmax(v)), (i, x[i], int(np.argmax(v)))
+        checked += 1
+    assert checked >= len(a_vals) - 1
