@@ -164,6 +164,34 @@ def test_done_sequences_are_untouched():
     compare_outputs(g, ref, [(b, i) for b in (0, 2) for i in range(w.L)])
 
 
+@pytest.mark.parametrize("impl", ["tensor", "simt", "fused"])
+def test_all_finished_batch_is_a_no_op(impl):
+    # every sequence finished on entry: the step writes nothing, and the sampler is left ready
+    # for the next step (which must match the oracle: no queue counter or stale record left)
+    w = W.scaled(BASE_BATCH, V=8192, d=256, B=2)
+    inp = W.make_inputs(w)
+    inp["done"] = np.ones(2, np.uint8)
+    case = GpuCase(w, inputs=inp, impl=impl)
+    state = case.state()
+    out = StepOutputs.empty(2, w.L, w.d)
+    for t in (out.s, out.conf, out.entropy):
+        t.fill_(-7.0)
+    out.sampled.fill_(-7)
+    out.argmax.fill_(-7)
+    pre = state_np(state)
+    case.sampler.step(case.H, case.E, case.T, case.tau, state, inp["seed"], out=out)
+    torch.cuda.synchronize()
+    post, g = state_np(state), out_np(out)
+    for k in pre:
+        assert np.array_equal(post[k], pre[k]), k
+    assert np.all(g["s"] == -7.0) and np.all(g["conf"] == -7.0) and np.all(g["entropy"] == -7.0)
+    assert np.all(g["sampled"] == -7) and np.all(g["argmax"] == -7)
+    assert case.sampler.device_status() == C.DS_OK
+    inp["done"] = np.zeros(2, np.uint8)
+    _, _, rep = full_step_check(case, case.state())
+    assert rep["excluded"] <= 2 and rep["undecidable"] <= 1
+
+
 @pytest.mark.parametrize("done", [(1, 0), (0, 1)])
 def test_done_sequence_inside_a_pair_tile(done):
     # 128-token canvases: one 256-row tile of the paired logits GEMM holds both sequences, one
@@ -287,6 +315,8 @@ def test_invalid_arguments_are_rejected():
     out = StepOutputs.empty(1, w.L, w.d)
     a = case.sampler._step_args(case.H, case.E, case.T, case.tau, st, out, 1)
     a.batch = 2
+    assert lib.ds_sampler_step(case.sampler.handle, ctypes.byref(a), None) == C.DS_ERR_INVALID_ARG
+    a.batch = 0  # an empty batch is rejected: there is no step to take
     assert lib.ds_sampler_step(case.sampler.handle, ctypes.byref(a), None) == C.DS_ERR_INVALID_ARG
     a.batch = 1
     a.conf = None
