@@ -67,6 +67,20 @@ def test_step_parity(impl, name, base, B, V, d, L):
     assert rep["undecidable"] <= 1
 
 
+@pytest.mark.parametrize("impl", ["tensor", "simt", "fused"])
+@pytest.mark.parametrize("T", [0.1, 2.5])
+def test_extreme_temperatures(impl, T):
+    # T = 0.1 multiplies the logits by ten (peaked rows reach y - mean ~ 10 c ln V, hundreds);
+    # T = 2.5 flattens them: both against the oracle on every position
+    w = W.scaled(BASE_BATCH, V=16384, d=256, B=2)
+    inp = W.make_inputs(w)
+    inp["T"] = np.full(w.B, T, np.float32)
+    case = GpuCase(w, inputs=inp, impl=impl)
+    _, _, rep = full_step_check(case, case.state())
+    assert rep["excluded"] <= max(2, rep["checked"] // 100)
+    assert rep["undecidable"] <= 1
+
+
 @pytest.mark.parametrize("k", [1, 64, 256])
 def test_topk_step_parity(k):
     # the top-k recipe with fixed peaked hidden states (the stand-in loop is tested elsewhere)
