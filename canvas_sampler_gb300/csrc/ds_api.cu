@@ -69,9 +69,10 @@ struct ds_sampler {
   float* mref = nullptr;     // fused pass: reference maxima of the range partials [Q, B*L]
   uint32_t* vp_sync = nullptr;
   uint32_t* err = nullptr;
-  // tensor-core step without top-k: the Gumbel race runs inside the self-conditioning launch
-  // (off with DS_GUMBEL_IN_SELFCOND=0: a launch of its own), with its queue counters gq[2]
-  bool gumbel_in_sc = false;
+  // tensor-core step without top-k: where the Gumbel race runs (inside the self-conditioning
+  // launch, with its queue counters gq[2], or as a launch of its own): -1 by shape (race_in_sc),
+  // 0 / 1 forced by DS_GUMBEL_IN_SELFCOND
+  int gumbel_in_sc = -1;
   uint32_t* gq = nullptr;
   int32_t* iter = nullptr;
   int last_batch = 0;
@@ -123,6 +124,16 @@ void mark(ds_sampler* s, int phase, cudaStream_t st) {
 }
 
 int esize(int dtype) { return dtype == DS_DTYPE_FP32 ? 4 : 2; }
+
+// Whether a step's Gumbel race runs on warps of the self-conditioning launch. Measured on GB300
+// (step time, race inside / own launch), d = 2816: B = 1, V = 262144: 0.886 / 0.892 ms and on
+// another box 0.904 / 0.913; V = 65536 and 131072: 0.276 / 0.293 and 0.469 / 0.481 ms; B = 2 and
+// 8 at V = 262144: 1.686 / 1.660 and 6.81 / 6.62 ms. B = 1, V = 32768, d = 1024: 0.154 / 0.116 ms
+// (a short GEMM leaves the race to a few warps). So inside for one canvas of rows, d >= 2048.
+bool race_in_selfcond(const ds_sampler* s, int R, int d) {
+  if (s->gumbel_in_sc >= 0) return s->gumbel_in_sc == 1;
+  return R <= 256 && d >= 2048;
+}
 
 int splits_for(const ds_sampler* s, int batch) {
   const int R = batch * s->cfg.canvas_len;
@@ -206,7 +217,7 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
     if (k > 0)
       launch_topk_row(s->Phi, s->Plo, s->cs, s->mseg_t, s->rs, R, V, L, a->done, k, s->cand, st);
     mark(s, 2, st);
-    const bool race_in_sc = k == 0 && s->gumbel_in_sc;
+    const bool race_in_sc = k == 0 && race_in_selfcond(s, R, d);
     if (k == 0 && !race_in_sc)
       launch_gumbel_items(s->Phi, s->Plo, s->cs, s->rs, R, V, L, a->done, a->step, a->seed, s->blk,
                         true, s->best, st);
@@ -405,10 +416,7 @@ ds_status ds_sampler_create(const ds_sampler_config* cfg, ds_sampler** out) {
     // producer / consumer split of the fused pass (a tuning knob; 0 = in proportion to work)
     if (const char* env = getenv("DS_VP_PRODUCERS")) s->vp_producers = atoi(env);
   }
-  if (s->impl == DS_IMPL_TENSOR) {
-    const char* env = getenv("DS_GUMBEL_IN_SELFCOND");
-    s->gumbel_in_sc = !(env && env[0] == '0');
-  }
+  if (const char* env = getenv("DS_GUMBEL_IN_SELFCOND")) s->gumbel_in_sc = env[0] == '0' ? 0 : 1;
   size_t opart = 0, nref = 0;
   for (int b = 1; b <= c.max_batch; ++b) {
     const size_t Rb = (size_t)b * c.canvas_len;

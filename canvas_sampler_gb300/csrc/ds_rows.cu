@@ -8,6 +8,7 @@
 // truncation of the sampling step); "DiffusionGemma: Google's open diffusion LLM", section "A
 // diffusion language model refines 256 tokens in 12 steps" (accept confident tokens,
 // re-noise the rest uniformly, at most 48 steps).
+#include <algorithm>
 #include <cfloat>
 #include <climits>
 
@@ -359,17 +360,61 @@ __global__ void __launch_bounds__(kThreads, 4) k_convert(const float* __restrict
   }
 }
 
-// Gumbel-max over stored probabilities as a launch of its own (the fused vocabulary pass; the
-// tensor-core step runs the same race inside its self-conditioning launch): one warp per
-// (row, 8192-token chunk) item, gumbel_chunk_warp (ds_sample.cuh).
-__global__ void __launch_bounds__(kThreads) k_gumbel_items(const __grid_constant__ GumbelWork g,
-                                                           int64_t V) {
+// Gumbel-max over stored probabilities as a launch of its own (the fused vocabulary pass, and
+// shapes where the self-conditioning launch does not carry the race): (row, 8192-token chunk)
+// items, each raced by wpi warps (1, 2, 4 or 8; more when there are few items to fill the GPU)
+// over consecutive parts of the chunk's segments (gumbel_race_segments, ds_sample.cuh), sharing
+// their best key through shared memory; the item's record is the best of its warps' bests
+// (largest -key, then lowest token), with ln p of the winner.
+__global__ void __launch_bounds__(kThreads, 2) k_gumbel_items(const __grid_constant__ GumbelWork g,
+                                                           int64_t V, int wpi) {
+  constexpr int kWarps = kThreads / 32;
+  __shared__ unsigned sh_cut[kWarps];
+  __shared__ float sh_v[kWarps], sh_y[kWarps];
+  __shared__ int32_t sh_j[kWarps];
   pdl_wait();
-  const int w = blockIdx.x * (kThreads / 32) + (int)(threadIdx.x >> 5);
-  if (w >= g.R * g.n_chunks) return;
-  const int r = w / g.n_chunks, c = w % g.n_chunks;
-  if (g.done && g.done[r / g.L]) return;
-  gumbel_chunk_warp(g, V, r, c);
+  const int w = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
+  const int slot = w / wpi, part = w % wpi;
+  const int64_t item = (int64_t)blockIdx.x * (kWarps / wpi) + slot;
+  if (lane == 0 && part == 0) sh_cut[slot] = 0x7F800000u;  // +inf
+  __syncthreads();
+  bool active = item < (int64_t)g.R * g.n_chunks;
+  int r = 0, c = 0;
+  if (active) {
+    r = (int)(item / g.n_chunks);
+    c = (int)(item % g.n_chunks);
+    active = !(g.done && g.done[r / g.L]);
+  }
+  float kbest = INFINITY, bp = 1.f;
+  int32_t bj = INT_MAX;
+  if (active) {
+    const int64_t j0 = (int64_t)c * kChunk, j1 = min(V, j0 + kChunk);
+    const int nseg = (int)((j1 - j0) / 128);
+    gumbel_race_segments(g, V, r, c, nseg * part / wpi, nseg * (part + 1) / wpi, kbest, bj, bp,
+                         wpi > 1 ? &sh_cut[slot] : nullptr);
+  }
+  float v = -kbest;
+  int32_t jw = bj;
+  warp_best(v, jw);
+  const uint32_t owner = __ballot_sync(0xffffffffu, bj == jw);
+  const float pw = __shfl_sync(0xffffffffu, bp, __ffs(owner) - 1);
+  if (lane == 0) {
+    sh_v[w] = v;
+    sh_j[w] = jw;
+    sh_y[w] = logf(pw);
+  }
+  __syncthreads();
+  if (active && part == 0 && lane == 0) {
+    float bv = sh_v[w], by = sh_y[w];
+    int32_t bjj = sh_j[w];
+    for (int q = 1; q < wpi; ++q)
+      if (better(sh_v[w + q], sh_j[w + q], bv, bjj)) {
+        bv = sh_v[w + q];
+        bjj = sh_j[w + q];
+        by = sh_y[w + q];
+      }
+    g.best[(size_t)r * g.n_chunks + c] = Best{bv, bjj, bjj == INT_MAX ? 0.f : by, 1};
+  }
 }
 
 // The k largest logits of a chunk (ties toward lower tokens), written in token order.
@@ -1142,8 +1187,14 @@ void launch_gumbel_items(const uint16_t* Phi, const uint16_t* Plo, const ChunkSt
   const int nc = n_chunks_of(V);
   const GumbelWork g{Phi, Plo, seg, rs, done, step, blk, seed, best, nullptr, R, L, nc,
                      tile_ref ? 1 : 0};
-  const int warps = kThreads / 32;
-  launch_k(k_gumbel_items, dim3((R * nc + warps - 1) / warps), dim3(kThreads), 0, st, g, V);
+  // warps per item: enough items in flight to fill every SM (two CTAs of 8 warps resident)
+  const int64_t items = (int64_t)R * nc;
+  const int64_t want = (int64_t)std::max(1, tc_num_sms()) * 16;
+  int wpi = 1;
+  while (wpi < kThreads / 32 && items * wpi * 2 <= want) wpi *= 2;
+  const int per_cta = kThreads / 32 / wpi;
+  launch_k(k_gumbel_items, dim3((unsigned)((items + per_cta - 1) / per_cta)), dim3(kThreads), 0, st,
+           g, V, wpi);
 }
 
 void launch_reduce_s(const float* Opart, int S, int R, int d, int L, const uint8_t* done,

@@ -231,31 +231,39 @@ DS_DEV int nth_set_bit(uint32_t m, int n) {
   return pos;
 }
 
-// Winner of the exponential race over chunk c of row r, p_j = (P_hi + P_lo)[j] exp(m_ref - m)
-// with m the row maximum and m_ref the maximum the probabilities were taken against: of token j's
-// 128-token segment, or with tile_ref of its 256-token tile (the larger of the two segment
-// maxima). The record is the chunk's argmin of E_j / p_j (lowest token on equal keys): skipped
-// segments and skipped draws are exactly those that cannot win. Segments more than kGumbelReach
-// below m are not read; the others are raced four at a time in token order (lane l takes
-// tokens 16 (l % 8) .. 16 (l % 8) + 15 of the (4 k + l / 8)-th segment in reach in round k), the
-// next round loaded while the current one is raced. The lanes race the first round's first four
-// tokens in full, and the warp's best key then cuts the rest of the chunk.
-DS_DEV void gumbel_chunk_warp(const GumbelWork& g, int64_t V, int r, int c) {
+// The exponential race over segments u0 .. u1 - 1 (u1 - u0 <= 64) of chunk c of row r by one
+// warp, p_j = (P_hi + P_lo)[j] exp(m_ref - m) with m the row maximum and m_ref the maximum the
+// probabilities were taken against: of token j's 128-token segment, or with tile_ref of its
+// 256-token tile (the larger of the two segment maxima). Leaves in each lane its best key
+// E_j / p_j, token and p (lowest token on equal keys within the lane); skipped segments and
+// skipped draws are exactly those that cannot win. Segments more than kGumbelReach below m are
+// not read; the others are raced four at a time in token order (lane l takes tokens
+// 16 (l % 8) .. 16 (l % 8) + 15 of the (4 k + l / 8)-th segment in reach in round k), the next
+// round loaded while the current one is raced. The lanes race the first round's first four
+// tokens in full, and the warp's best key then cuts the rest. With shared_cut (a key as its bit
+// pattern, in shared memory) several warps racing parts of the same chunk exchange their best
+// keys after every round: any key a token of the chunk has reached is a valid cutoff for the
+// chunk's winner (keys are >= 0, so their bit patterns order like the values).
+DS_DEV void gumbel_race_segments(const GumbelWork& g, int64_t V, int r, int c, int u0, int u1,
+                                 float& kbest, int32_t& bj, float& bp,
+                                 unsigned* shared_cut = nullptr) {
   constexpr int kSegTok = 128;
   const int lane = threadIdx.x & 31;
   const int b = r / g.L, i = r % g.L;
   const float m = g.rs[r].m;
-  const int64_t j0 = (int64_t)c * kChunk, j1 = min(V, j0 + kChunk);
-  const int nseg = (int)((j1 - j0) / kSegTok);  // whole segments: V is a multiple of 256
+  const int64_t j0 = (int64_t)c * kChunk;
   const ChunkStat* sg = g.seg + (size_t)r * (V / kSegTok) + j0 / kSegTok;
-  // segment scales: lane l holds segments l and l + 32 of the chunk
+  kbest = INFINITY;
+  bp = 1.f;
+  bj = INT_MAX;
+  // segment scales: lane l holds segments u0 + l and u0 + l + 32
   float sc[2];
   uint32_t in[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const int u = lane + 32 * h;
+    const int u = u0 + lane + 32 * h;
     float v = 0.f;
-    if (u < nseg) {
+    if (u < u1) {
       const float mg = sg[u].m;
       // chunks start at multiples of 256 tokens, so segment pairs (2w, 2w + 1) are tiles
       if (mg >= m - kGumbelReach) v = expf((g.tile_ref ? fmaxf(mg, sg[u ^ 1].m) : mg) - m);
@@ -264,28 +272,23 @@ DS_DEV void gumbel_chunk_warp(const GumbelWork& g, int64_t V, int r, int c) {
     in[h] = __ballot_sync(0xffffffffu, v > 0.f);
   }
   const int n0 = __popc(in[0]), n_in = n0 + __popc(in[1]);
-  Best* out = g.best + (size_t)r * g.n_chunks + c;
-  if (n_in == 0) {  // no token of the chunk can win
-    if (lane == 0) *out = Best{-INFINITY, INT_MAX, 0.f, 1};
-    return;
-  }
+  if (n_in == 0) return;  // no token of these segments can win
   // this lane's 16 tokens in round k (offset in the chunk) and their scale (0: none)
   auto locate = [&](int k, float& s) -> int {
     const int n = 4 * k + (lane >> 3);
-    int u = 0;
-    if (n < n_in) u = n < n0 ? nth_set_bit(in[0], n) : 32 + nth_set_bit(in[1], n - n0);
-    const float a0 = __shfl_sync(0xffffffffu, sc[0], u & 31);
-    const float a1 = __shfl_sync(0xffffffffu, sc[1], u & 31);
-    s = n < n_in ? (u < 32 ? a0 : a1) : 0.f;
-    return kSegTok * u + 16 * (lane & 7);
+    int t = 0;
+    if (n < n_in) t = n < n0 ? nth_set_bit(in[0], n) : 32 + nth_set_bit(in[1], n - n0);
+    const float a0 = __shfl_sync(0xffffffffu, sc[0], t & 31);
+    const float a1 = __shfl_sync(0xffffffffu, sc[1], t & 31);
+    s = n < n_in ? (t < 32 ? a0 : a1) : 0.f;
+    return kSegTok * (u0 + t) + 16 * (lane & 7);
   };
   const uint32_t st = (uint32_t)g.step[b];
   const uint32_t sid = stream_id((uint32_t)b, g.blk);
   const uint16_t* ph = g.Phi + (size_t)r * V + j0;
   const uint16_t* pl = g.Plo + (size_t)r * V + j0;
   const int rounds = (n_in + 3) / 4;
-  float kbest = INFINITY, bp = 1.f, cut, s;
-  int32_t bj = INT_MAX;
+  float cut, s;
   Slab16 cur, nxt;
   int off = locate(0, s);
   slab_load(cur, ph + off, pl + off, s);
@@ -308,16 +311,32 @@ DS_DEV void gumbel_chunk_warp(const GumbelWork& g, int64_t V, int r, int c) {
                     g.seed, cut, kbest, bj, bp);
     }
     cut = warp_min(fminf(cut, kbest));
+    if (shared_cut) {
+      if (lane == 0) atomicMin(shared_cut, __float_as_uint(cut));
+      __syncwarp();
+      cut = fminf(cut, __uint_as_float(*(volatile unsigned*)shared_cut));
+    }
     cur = nxt;
     off = off_n;
   }
-  // the warp's winner: largest -key, then lowest token; its p comes from the lane that holds it
+}
+
+// Winner of the exponential race over chunk c of row r (all its segments) by one warp, written
+// to best[r, c] as a Best record (v = -key, rel = 1, y = ln p of the winner): largest -key, then
+// lowest token.
+DS_DEV void gumbel_chunk_warp(const GumbelWork& g, int64_t V, int r, int c) {
+  const int64_t j0 = (int64_t)c * kChunk, j1 = min(V, j0 + kChunk);
+  const int nseg = (int)((j1 - j0) / 128);  // whole segments: V is a multiple of 256
+  float kbest, bp;
+  int32_t bj;
+  gumbel_race_segments(g, V, r, c, 0, nseg, kbest, bj, bp);
   float v = -kbest;
   int32_t jw = bj;
   warp_best(v, jw);
+  // the winner's p comes from the lane that holds it (every lane when there is none: p = 1)
   const uint32_t owner = __ballot_sync(0xffffffffu, bj == jw);
   const float pw = __shfl_sync(0xffffffffu, bp, __ffs(owner) - 1);
-  if (lane == 0) *out = Best{v, jw, logf(pw), 1};
+  if ((threadIdx.x & 31) == 0) g.best[(size_t)r * g.n_chunks + c] = Best{v, jw, logf(pw), 1};
 }
 
 // One warp's share of the queue of (row, chunk) items: items are taken one at a time until the

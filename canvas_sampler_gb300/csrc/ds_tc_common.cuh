@@ -2,7 +2,8 @@
 // the control block of the warp-specialised pipeline, bounded waits used while draining, and
 // the promotion of short TMEM accumulation chains into fp32 registers.
 //
-// Structure of both kernels: one persistent CTA per SM, 10 warps.
+// Structure of both kernels: one persistent CTA per SM, 10 warps (the self-conditioning kernel
+// adds two that run the Gumbel-max race beside its GEMM).
 //   warp 0  one thread issues TMA copies of the operand tiles into a ring of shared-memory
 //           stages (128-byte swizzle), completion counted on "full" mbarriers;
 //   warp 1  allocates 512 TMEM columns; one thread issues tcgen05.mma into one of two TMEM

@@ -37,10 +37,11 @@ constexpr uint32_t LG_STAGE_BYTES = LG_A_BYTES + LG_B_BYTES;
 // hi and lo parts of P.
 constexpr uint32_t LG_STG_BYTES = 32 * 32 * 4;
 // CTA pair: each CTA stages its 128 rows of H and 128 of the tile's 256 rows of E (32 KB a
-// stage), so an SM takes in 2/3 of the bytes per MAC of a one-CTA tile; the smaller stages
-// leave room for two staging boxes per warp, used in turn, so a warp writes the next box while
-// the TMA store of the previous one is still reading shared memory.
-constexpr int LG2_STAGES = 5, LG2_STG_BOXES = 2;
+// stage), so an SM takes in 2/3 of the bytes per MAC of a one-CTA tile. Measured at the bench
+// size (logits kernel per step): 5 stages with one staging box per warp 0.323 ms, with two boxes
+// used in turn (a warp writes the next box while the store of the previous one still reads it)
+// 0.328 ms, 6 stages with one box 0.327 ms, 4 stages with two 0.344 ms.
+constexpr int LG2_STAGES = 5, LG2_STG_BOXES = 1;
 constexpr uint32_t LG2_STAGE_BYTES = LG_A_BYTES + LG_B_BYTES / 2;
 static_assert(LG2_STAGES <= tcpipe::kMaxStages && LG_STAGES <= tcpipe::kMaxStages, "stages");
 constexpr size_t LG_SMEM =
