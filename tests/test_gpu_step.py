@@ -49,6 +49,9 @@ CASES = [
     ("peaked_v16384_d512", BASE_PEAKED, 1, 16384, 512, 256),
     ("peaked_ragged_v8960_d320", BASE_PEAKED, 1, 8960, 320, 256),
     ("batched_b3_v8192_d256", BASE_BATCH, 3, 8192, 256, 256),
+    # 1536 (row, chunk) items: the race's own launch takes two warps per item (8 and 4 warps per
+    # item in the smaller cases, one in the larger)
+    ("batched_b3_v16384_d256", BASE_BATCH, 3, 16384, 256, 256),
     ("canvas128_b3_v8192_d512", BASE_BATCH, 3, 8192, 512, 128),
     ("canvas128_b2_v8960_d256", BASE_BATCH, 2, 8960, 256, 128),
 ]
