@@ -396,8 +396,9 @@ def run_ours(args):
         roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": ach / peak_tf, "traffic": traffic,
                 "peak_source": f"{peak_key} ({peak_src})"}
-        # the tensor-core step without top-k launches 4 kernels when the race runs inside the
-        # self-conditioning launch, 5 when it has a launch of its own
+        # the tensor-core step without top-k launches 4 kernels when the row merge and the race
+        # run inside the self-conditioning launch (logits, self-conditioning, finalize, lock),
+        # 6 when they have launches of their own
         if dom == "selfcond" and sampler.impl == "tensor" and launches == 4 * args.steps:
             roof["note"] = ("the launch also runs the step's Gumbel-max race on warps of its own; "
                             "only the GEMM's 2 B L V d FLOP are counted")

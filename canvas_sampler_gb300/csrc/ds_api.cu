@@ -74,6 +74,7 @@ struct ds_sampler {
   // 0 / 1 forced by DS_GUMBEL_IN_SELFCOND
   int gumbel_in_sc = -1;
   uint32_t* gq = nullptr;
+  uint32_t* row_flags = nullptr;  // [max_batch * L]: rows merged inside the launch (generation)
   int32_t* iter = nullptr;
   int last_batch = 0;
   // device staging for ds_sampler_step_host (allocated on first use)
@@ -212,18 +213,21 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
                                        s->Phi, s->Plo, s->cs, s->mseg_t, s->err, st);
     if (e != cudaSuccess) return cuda_status(e);
     mark(s, 0, st);
-    launch_row_merge(s->cs, (int)(V / kTcSegment), R, L, a->done, s->rs, st);
+    // with the race inside the self-conditioning launch, the row merge is the first work of its
+    // racing warps (the GEMM does not need it); otherwise a launch of its own
+    const bool race_in_sc = k == 0 && race_in_selfcond(s, R, d);
+    if (!race_in_sc) launch_row_merge(s->cs, (int)(V / kTcSegment), R, L, a->done, s->rs, st);
     mark(s, 1, st);
     if (k > 0)
       launch_topk_row(s->Phi, s->Plo, s->cs, s->mseg_t, s->rs, R, V, L, a->done, k, s->cand, st);
     mark(s, 2, st);
-    const bool race_in_sc = k == 0 && race_in_selfcond(s, R, d);
     if (k == 0 && !race_in_sc)
       launch_gumbel_items(s->Phi, s->Plo, s->cs, s->rs, R, V, L, a->done, a->step, a->seed, s->blk,
                         true, s->best, st);
     mark(s, 3, st);
-    const GumbelWork gw{s->Phi, s->Plo, s->cs, s->rs, a->done,     a->step, s->blk,
-                        a->seed, s->best, s->gq, R,    L,       s->n_chunks, 1};
+    const GumbelWork gw{s->Phi, s->Plo, s->cs,  s->rs, a->done, a->step, s->blk,
+                        a->seed, s->best, s->gq, R,    L,       s->n_chunks, 1,
+                        s->rs,   s->row_flags, s->err};
     e = launch_selfcond_tc(s->Phi, s->Plo, static_cast<const uint16_t*>(a->E), R, V, d, L,
                            a->done, S, s->Opart, s->mseg_t, s->mref, s->err,
                            race_in_sc ? &gw : nullptr, st);
@@ -233,7 +237,7 @@ ds_status enqueue_step(ds_sampler* s, const ds_step_args* a, cudaStream_t st) {
     launch_finalize_with_s(s->rs, s->best, k > 0 ? s->cand : nullptr, k > 0 ? 1 : s->n_chunks, k,
                            R, L, a->done, a->step, a->seed, s->blk, a->sampled, a->conf,
                            a->entropy, a->argmax, s->Opart, S, d, a->s, s->mref, st);
-    s->launches += race_in_sc ? 4 : 5;
+    s->launches += race_in_sc ? 3 : 5;
   } else {
     launch_logits_simt(a->H, a->E, fp32, R, V, d, L, T, a->done, s->Y, st);
     mark(s, 0, st);
@@ -458,8 +462,10 @@ ds_status ds_sampler_create(const ds_sampler_config* cfg, ds_sampler** out) {
   s->iter = carve<int32_t>(s, 4, &e);
   s->blk = carve<int32_t>(s, 4, &e);
   s->gq = carve<uint32_t>(s, 4, &e);
+  s->row_flags = carve<uint32_t>(s, Rm, &e);
   if (e == cudaSuccess) e = cudaMemset(s->err, 0, 4 * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(s->gq, 0, 4 * sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMemset(s->row_flags, 0, Rm * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(s->blk, 0, 4 * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s->capture_stream, cudaStreamNonBlocking);
   if (e != cudaSuccess) {

@@ -73,7 +73,8 @@ void launch_finalize_with_s(const RowStat* rs, const Best* best, const Cand* can
 // The Gumbel race of a step over (row, 8192-token chunk) items, each raced by one warp (see
 // gumbel_chunk_warp). As a queue (inside the self-conditioning launch): ctr[0] is the next item,
 // ctr[1] counts the CTAs of the launch that have finished; the last CTA returns both to zero, so
-// they are zero between launches (zero them once when allocated).
+// they are zero between launches, and advances the generation ctr[2] (zero all three once when
+// allocated).
 struct GumbelWork {
   const uint16_t* Phi;
   const uint16_t* Plo;
@@ -87,6 +88,13 @@ struct GumbelWork {
   uint32_t* ctr;
   int R, L, n_chunks;
   int tile_ref;  // probabilities relative to 256-token tile maxima (else to segment maxima)
+  // In the queue only: with rs_out, the queue's first R items merge the rows' segment statistics
+  // into rs_out (= rs) as k_row_merge does, bit for bit, and each row's race items wait until
+  // row_flags[r] holds this launch's generation (ctr[2] + 1); a wait that runs out sets
+  // kErrTimeout in err.
+  RowStat* rs_out;
+  uint32_t* row_flags;  // [R], zero when allocated
+  uint32_t* err;
 };
 
 // Gumbel-max sample per (row, chunk) from probabilities stored relative to each 128-token

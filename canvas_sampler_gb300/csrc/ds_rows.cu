@@ -224,7 +224,9 @@ __global__ void __launch_bounds__(kThreads) k_row_merge(const ChunkStat* __restr
   // l = sum_g l_g e^{m_g - m} and a = sum_g (a_g + l_g (m_g - m)) e^{m_g - m}: every term has one
   // sign (l_g > 0, a_g <= 0, m_g <= m), so there is no cancellation; each thread sums its terms
   // in fp32 with a compensation term (Kahan), the warps by a shuffle tree and the block's eight
-  // warp sums in fp64, a relative error of a few fp32 units
+  // warp sums in fp64, a relative error of a few fp32 units. The products are rounded on their
+  // own (no contraction into the compensated sum), so row_merge_warp (ds_sample.cuh) reproduces
+  // this kernel bit for bit
   float l = 0.f, a = 0.f, cl = 0.f, ca = 0.f;
   auto kahan = [](float& sum, float& comp, float x) {
     const float y = x - comp;
@@ -239,8 +241,8 @@ __global__ void __launch_bounds__(kThreads) k_row_merge(const ChunkStat* __restr
       if (mine[k].arg == INT_MAX) continue;
       const float dm = mine[k].m - m;
       const float sc = expf(dm);
-      kahan(l, cl, mine[k].l * sc);
-      kahan(a, ca, fmaf(mine[k].l, dm, mine[k].a) * sc);
+      kahan(l, cl, __fmul_rn(mine[k].l, sc));
+      kahan(a, ca, __fmul_rn(fmaf(mine[k].l, dm, mine[k].a), sc));
     }
   }
   l -= cl;
@@ -1185,8 +1187,8 @@ void launch_gumbel_items(const uint16_t* Phi, const uint16_t* Plo, const ChunkSt
                        const int32_t* step, uint64_t seed, const int32_t* blk, bool tile_ref,
                        Best* best, cudaStream_t st) {
   const int nc = n_chunks_of(V);
-  const GumbelWork g{Phi, Plo, seg, rs, done, step, blk, seed, best, nullptr, R, L, nc,
-                     tile_ref ? 1 : 0};
+  const GumbelWork g{Phi, Plo, seg,     rs, done,    step, blk, seed, best, nullptr, R, L, nc,
+                     tile_ref ? 1 : 0, nullptr, nullptr, nullptr};
   // warps per item: doubled while the items' warps would not fill the warps every SM holds
   // (two CTAs of 8). Race time measured against the rule at 1024 / 2048 / 4096 items:
   // 0.024 / 0.031 / 0.118 ms (4, 2, 1 warps), 0.025 / 0.039 / 0.118 with half as many warps,

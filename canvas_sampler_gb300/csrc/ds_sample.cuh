@@ -250,7 +250,9 @@ DS_DEV void gumbel_race_segments(const GumbelWork& g, int64_t V, int r, int c, i
   constexpr int kSegTok = 128;
   const int lane = threadIdx.x & 31;
   const int b = r / g.L, i = r % g.L;
-  const float m = g.rs[r].m;
+  // from L2: in the queue the record may have been written in this launch, after another
+  // record of the same line was read here
+  const float m = __ldcg(&g.rs[r].m);
   const int64_t j0 = (int64_t)c * kChunk;
   const ChunkStat* sg = g.seg + (size_t)r * (V / kSegTok) + j0 / kSegTok;
   kbest = INFINITY;
@@ -339,28 +341,130 @@ DS_DEV void gumbel_chunk_warp(const GumbelWork& g, int64_t V, int r, int c) {
   if ((threadIdx.x & 31) == 0) g.best[(size_t)r * g.n_chunks + c] = Best{v, jw, logf(pw), 1};
 }
 
-// One warp's share of the queue of (row, chunk) items: items are taken one at a time until the
-// queue is empty; finished sequences' items are skipped (their records are not written).
+// The row statistics of k_row_merge computed by one warp, bit for bit: lane l stands for the
+// eight threads l + 32 j (j = 0 .. 7) of that kernel's 256-thread CTA, each taking the segments
+// q = base + t + 256 k in the same order, with the same fp32 Kahan sums per thread, the same
+// shuffle tree per warp of eight and the same fp64 sum over the eight warps: m and argmax
+// (lowest token on equal maxima), l = sum_g l_g e^{m_g - m}, a = sum_g (a_g + l_g (m_g - m))
+// e^{m_g - m}, entropy ln l - a / l. Valid in lane 0.
+DS_DEV RowStat row_merge_warp(const ChunkStat* __restrict__ c, int n) {
+  constexpr int kT = 256, kPer = 16, kJ = kT / 32;
+  const int lane = threadIdx.x & 31;
+  float m = -INFINITY;
+  int32_t arg = INT_MAX;
+  for (int base = 0; base < n; base += kT * kPer)
+    for (int k = 0; k < kPer; ++k) {
+#pragma unroll
+      for (int j = 0; j < kJ; ++j) {
+        const int q = base + lane + 32 * j + kT * k;
+        if (q < n) {
+          const ChunkStat t = c[q];
+          if (better(t.m, t.arg, m, arg)) {
+            m = t.m;
+            arg = t.arg;
+          }
+        }
+      }
+    }
+  warp_best(m, arg);  // the maximum and its lowest token do not depend on the order
+  float l[kJ], a[kJ], cl[kJ], ca[kJ];
+#pragma unroll
+  for (int j = 0; j < kJ; ++j) l[j] = a[j] = cl[j] = ca[j] = 0.f;
+  auto kahan = [](float& sum, float& comp, float x) {
+    const float y = x - comp;
+    const float t = sum + y;
+    comp = (t - sum) - y;
+    sum = t;
+  };
+  for (int base = 0; base < n; base += kT * kPer)
+    for (int k = 0; k < kPer; ++k) {
+#pragma unroll
+      for (int j = 0; j < kJ; ++j) {
+        const int q = base + lane + 32 * j + kT * k;
+        if (q < n) {
+          const ChunkStat t = c[q];
+          if (t.arg == INT_MAX) continue;
+          const float dm = t.m - m;
+          const float sc = expf(dm);
+          kahan(l[j], cl[j], __fmul_rn(t.l, sc));
+          kahan(a[j], ca[j], __fmul_rn(fmaf(t.l, dm, t.a), sc));
+        }
+      }
+    }
+  double tl = 0.0, ta = 0.0;
+#pragma unroll
+  for (int j = 0; j < kJ; ++j) {
+    float lj = l[j] - cl[j], aj = a[j] - ca[j];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      lj += __shfl_xor_sync(0xffffffffu, lj, o);
+      aj += __shfl_xor_sync(0xffffffffu, aj, o);
+    }
+    tl += (double)lj;
+    ta += (double)aj;
+  }
+  return RowStat{m, (float)tl, (float)(log(tl) - ta / tl), arg};
+}
+
+// One warp's share of the queue: items are taken one at a time until the queue is empty;
+// finished sequences' items are skipped (their records are not written). With g.rs_out the first
+// R items are row merges, and a race item first waits (bounded) for its row's merge.
 DS_DEV void gumbel_queue_warp(const GumbelWork& g, int64_t V) {
-  const uint32_t n_items = (uint32_t)g.R * (uint32_t)g.n_chunks;
+  const int lane = threadIdx.x & 31;
+  const bool merge = g.rs_out != nullptr;
+  const uint32_t n_merge = merge ? (uint32_t)g.R : 0u;
+  const uint32_t n_items = n_merge + (uint32_t)g.R * (uint32_t)g.n_chunks;
+  const uint32_t gen = merge ? *(volatile const uint32_t*)(g.ctr + 2) + 1u : 0u;
+  const int n_seg = (int)(V / 128);
   for (;;) {
     uint32_t it = 0;
-    if ((threadIdx.x & 31) == 0) it = atomicAdd(g.ctr, 1u);
+    if (lane == 0) it = atomicAdd(g.ctr, 1u);
     it = __shfl_sync(0xffffffffu, it, 0);
     if (it >= n_items) return;
+    if (it < n_merge) {
+      const int r = (int)it;
+      if (g.done && g.done[r / g.L]) continue;
+      const RowStat st = row_merge_warp(g.seg + (size_t)r * n_seg, n_seg);
+      if (lane == 0) {
+        g.rs_out[r] = st;
+        __threadfence();
+        st_release_gpu(g.row_flags + r, gen);
+      }
+      continue;
+    }
+    it -= n_merge;
     const int r = (int)(it / (uint32_t)g.n_chunks), c = (int)(it % (uint32_t)g.n_chunks);
     if (g.done && g.done[r / g.L]) continue;
+    if (merge) {
+      int ok = 1;
+      if (lane == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_gpu(g.row_flags + r) != gen) {
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(g.err, kErrTimeout);
+            ok = 0;
+            break;
+          }
+          __nanosleep(64);
+        }
+      }
+      // the other lanes read the row's record after lane 0's acquire
+      __syncwarp();
+      if (!__shfl_sync(0xffffffffu, ok, 0)) continue;
+    }
     gumbel_chunk_warp(g, V, r, c);
   }
 }
 
 // After every warp of the CTA has left gumbel_queue_warp (a __syncthreads in between), one
-// thread of each CTA: the last CTA of the grid returns the queue counters to zero.
+// thread of each CTA: the last CTA of the grid returns the queue counters to zero and advances
+// the generation.
 DS_DEV void gumbel_queue_release(const GumbelWork& g) {
   __threadfence();
   if (atomicAdd(g.ctr + 1, 1u) == gridDim.x - 1) {
     atomicExch(g.ctr, 0u);
     atomicExch(g.ctr + 1, 0u);
+    atomicAdd(g.ctr + 2, 1u);  // the next launch's row flags
   }
 }
 
