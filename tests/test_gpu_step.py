@@ -54,6 +54,9 @@ CASES = [
     ("batched_b3_v16384_d256", BASE_BATCH, 3, 16384, 256, 256),
     ("canvas128_b3_v8192_d512", BASE_BATCH, 3, 8192, 512, 128),
     ("canvas128_b2_v8960_d256", BASE_BATCH, 2, 8960, 256, 128),
+    # B * L = 256 and d >= 2048: the row merge and the race run inside the self-conditioning
+    # launch by default
+    ("canvas128_b2_v8192_d2048", BASE_BATCH, 2, 8192, 2048, 128),
 ]
 
 
@@ -209,11 +212,13 @@ def test_all_finished_batch_is_a_no_op(impl):
     assert rep["excluded"] <= 2 and rep["undecidable"] <= 1
 
 
+@pytest.mark.parametrize("d", [256, 2048])
 @pytest.mark.parametrize("done", [(1, 0), (0, 1)])
-def test_done_sequence_inside_a_pair_tile(done):
+def test_done_sequence_inside_a_pair_tile(done, d):
     # 128-token canvases: one 256-row tile of the paired logits GEMM holds both sequences, one
     # of them finished; the live one must match the oracle and the finished one stay untouched
-    w = W.scaled(BASE_BATCH, V=8192, d=256, B=2, L=128)
+    # (at d = 2048 the row merge and the race run inside the self-conditioning launch)
+    w = W.scaled(BASE_BATCH, V=8192, d=d, B=2, L=128)
     inp = W.make_inputs(w)
     inp["done"] = np.array(done, np.uint8)
     case = GpuCase(w, inputs=inp)
