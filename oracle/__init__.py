@@ -32,9 +32,9 @@ closed forms (uniform softmax, s -> E[j] for H = alpha E[j], T -> 0 argmax), bru
 with math.fsum on tiny vocabularies, invariants (probabilities sum to 1, entropy in
 [0, ln V], locked tokens never change, >= 1 lock per step, termination), a hand-derived
 worked example under tests/golden/, chi-squared tests of Gumbel-max frequencies and of
-re-noise uniformity, and a second, scalar implementation plus bijectivity and statistical
-tests for Philox. Philox parity with the published known-answer vectors is UNPINNED (those
-vectors are not available here).
+re-noise uniformity, and for Philox an implementation written by others (the header-only
+Philox4x32-10 engine of PyTorch's C++ headers, compiled into a small driver and compared block
+for block), a second, scalar implementation, bijectivity and statistical tests.
 """
 from .philox import philox4x32_10, philox4x32_10_scalar  # noqa: F401
 from .sampler import (  # noqa: F401
