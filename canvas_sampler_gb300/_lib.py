@@ -81,6 +81,7 @@ SIGNATURES = {
     "ds_sampler_launch_count": (c_int32, [c_void_p, POINTER(c_int64)]),
     "ds_sampler_selftest_wait": (c_int32, [c_void_p, c_int64, c_void_p]),
     "ds_sampler_step_noalloc": (c_int32, [POINTER(ds_sampler_config), POINTER(ds_step_args), c_void_p]),
+    "ds_sampler_noalloc_status": (c_int32, [c_void_p, POINTER(c_int32)]),
 }
 
 PHASES = ["logits", "stats", "topk", "convert", "selfcond", "finalize", "lock"]

@@ -281,8 +281,8 @@ ds_status enqueue_standin(ds_sampler* s, const void* W, const float* s_prev, con
                           cudaStream_t st) {
   const int d = s->cfg.d_model, L = s->cfg.canvas_len, R = batch * L;
   if (s->impl != DS_IMPL_SIMT && s->U && d % 256 == 0) {
-    launch_standin_gather(s_prev, static_cast<const uint16_t*>(E), canvas, done, R, d, L, s->U,
-                          st);
+    launch_standin_gather(s_prev, static_cast<const uint16_t*>(E), canvas, done, R, d, L,
+                          s->cfg.vocab, s->err, s->U, st);
     cudaError_t e = launch_standin_tc(s->U, static_cast<const uint16_t*>(W), R, d, L, done,
                                       static_cast<uint16_t*>(H_out), s->err, st);
     s->launches += 2;
@@ -290,7 +290,7 @@ ds_status enqueue_standin(ds_sampler* s, const void* W, const float* s_prev, con
   }
   launch_standin_simt(static_cast<const uint16_t*>(W), s_prev, static_cast<const uint16_t*>(E),
                       canvas, done, batch * s->cfg.canvas_len, s->cfg.d_model, s->cfg.canvas_len,
-                      static_cast<uint16_t*>(H_out), st);
+                      s->cfg.vocab, s->err, static_cast<uint16_t*>(H_out), st);
   s->launches += 1;
   return cuda_status(cudaGetLastError());
 }
@@ -344,6 +344,30 @@ void free_all(ds_sampler* s) {
 
 }  // namespace
 
+namespace ds {
+
+ds_status validate_config(const ds_sampler_config& c) {
+  if (c.canvas_len < 128 || c.canvas_len > 1024 || c.canvas_len % 128) return DS_ERR_INVALID_ARG;
+  if (c.vocab < 256 || c.vocab > (1 << 24) || c.vocab % 256) return DS_ERR_INVALID_ARG;
+  if (c.d_model < 64 || c.d_model > 16384 || c.d_model % 64) return DS_ERR_INVALID_ARG;
+  if (c.dtype != DS_DTYPE_BF16 && c.dtype != DS_DTYPE_FP32) return DS_ERR_INVALID_ARG;
+  if (c.top_k < 0 || c.top_k > kMaxTopK) return DS_ERR_INVALID_ARG;
+  if (c.max_steps < 1 || c.max_steps > (1 << 28)) return DS_ERR_INVALID_ARG;
+  if (c.impl != DS_IMPL_AUTO && c.impl != DS_IMPL_TENSOR && c.impl != DS_IMPL_SIMT &&
+      c.impl != DS_IMPL_FUSED)
+    return DS_ERR_INVALID_ARG;
+  if (c.lock_rule != DS_LOCK_THRESHOLD && c.lock_rule != DS_LOCK_ENTROPY_BUDGET)
+    return DS_ERR_INVALID_ARG;
+  if (!(c.entropy_budget >= 0.f) || !(c.stop_entropy >= 0.f) || !(c.t_end == c.t_end) ||
+      (c.t_start > 0.f && !(c.t_end > 0.f)))
+    return DS_ERR_INVALID_ARG;
+  if (c.top_k > 0 && (int64_t)n_chunks_of(c.vocab) * c.top_k > kMaxTopKPool)
+    return DS_ERR_UNSUPPORTED;
+  return DS_OK;
+}
+
+}  // namespace ds
+
 extern "C" {
 
 int32_t ds_abi_version(void) { return DS_SAMPLER_ABI_VERSION; }
@@ -367,23 +391,10 @@ ds_status ds_sampler_create(const ds_sampler_config* cfg, ds_sampler** out) {
   if (!cfg || !out) return DS_ERR_INVALID_ARG;
   *out = nullptr;
   const ds_sampler_config& c = *cfg;
-  if (c.canvas_len < 128 || c.canvas_len > 1024 || c.canvas_len % 128) return DS_ERR_INVALID_ARG;
-  if (c.vocab < 256 || c.vocab > (1 << 24) || c.vocab % 256) return DS_ERR_INVALID_ARG;
-  if (c.d_model < 64 || c.d_model > 16384 || c.d_model % 64) return DS_ERR_INVALID_ARG;
   if (c.max_batch < 1 || (int64_t)c.max_batch * c.canvas_len > 65535) return DS_ERR_INVALID_ARG;
-  if (c.dtype != DS_DTYPE_BF16 && c.dtype != DS_DTYPE_FP32) return DS_ERR_INVALID_ARG;
-  if (c.top_k < 0 || c.top_k > kMaxTopK) return DS_ERR_INVALID_ARG;
-  if (c.max_steps < 1 || c.max_steps > (1 << 28)) return DS_ERR_INVALID_ARG;
-  if (c.impl != DS_IMPL_AUTO && c.impl != DS_IMPL_TENSOR && c.impl != DS_IMPL_SIMT &&
-      c.impl != DS_IMPL_FUSED)
-    return DS_ERR_INVALID_ARG;
-  if (c.lock_rule != DS_LOCK_THRESHOLD && c.lock_rule != DS_LOCK_ENTROPY_BUDGET)
-    return DS_ERR_INVALID_ARG;
-  if (!(c.entropy_budget >= 0.f) || !(c.stop_entropy >= 0.f) || !(c.t_end == c.t_end) ||
-      (c.t_start > 0.f && !(c.t_end > 0.f)))
-    return DS_ERR_INVALID_ARG;
+  const ds_status vs = ds::validate_config(c);
+  if (vs != DS_OK) return vs;
   const int n_chunks = n_chunks_of(c.vocab);
-  if (c.top_k > 0 && (int64_t)n_chunks * c.top_k > kMaxTopKPool) return DS_ERR_UNSUPPORTED;
 
   ds_sampler* s = new (std::nothrow) ds_sampler();
   if (!s) return DS_ERR_OOM;
@@ -514,6 +525,13 @@ ds_status ds_sampler_step_host(ds_sampler* s, const ds_step_args* h, void* strea
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t B = (size_t)h->batch, L = (size_t)s->cfg.canvas_len, d = (size_t)s->cfg.d_model;
   const size_t Bm = (size_t)s->cfg.max_batch;
+  // the canvas is in host memory here, so its tokens are checked before anything is enqueued
+  // (the device step itself never indexes E by them; the stand-in does)
+  {
+    const int32_t* cv = static_cast<const int32_t*>(h->canvas);
+    for (size_t i = 0; i < B * L; ++i)
+      if (cv[i] < 0 || (int64_t)cv[i] >= s->cfg.vocab) return DS_ERR_INVALID_ARG;
+  }
   const size_t es = esize(s->cfg.dtype);
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   auto up16 = [](size_t x) { return (x + 15) & ~size_t(15); };

@@ -6,6 +6,7 @@
 
 #include <cstdint>
 
+#include "../../include/ds_sampler.h"
 #include "ds_common.cuh"
 
 namespace ds {
@@ -41,6 +42,11 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   cfg.numAttrs = pdl_enabled() ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
+
+// Checks of a sampler configuration shared by ds_sampler_create and the no-allocation step
+// (everything but max_batch): DS_OK, DS_ERR_INVALID_ARG or DS_ERR_UNSUPPORTED (a top-k candidate
+// pool beyond kMaxTopKPool).
+ds_status validate_config(const ds_sampler_config& c);
 
 // ---- row kernels (ds_rows.cu) ----
 void launch_chunk_stats(const float* Y, int R, int64_t V, int L, const uint8_t* done,
@@ -150,9 +156,11 @@ void launch_logits_simt(const void* H, const void* E, bool fp32_inputs, int R, i
 void launch_selfcond_simt(const uint16_t* Phi, const uint16_t* Plo, const void* E,
                           bool fp32_inputs, int R, int64_t V, int d, int L, const uint8_t* done,
                           int S, float* Opart, cudaStream_t st);
+// Both stand-in launchers read E[canvas[r]]: a token outside [0, V) is clamped into E and sets
+// kErrBounds in err.
 void launch_standin_simt(const uint16_t* W, const float* s_prev, const uint16_t* E,
                          const int32_t* canvas, const uint8_t* done, int R, int d, int L,
-                         uint16_t* H_out, cudaStream_t st);
+                         int64_t V, uint32_t* err, uint16_t* H_out, cudaStream_t st);
 
 // ---- tensor-core GEMMs (ds_tc.cu host side, ds_tc_logits.cu, ds_tc_selfcond.cu) ----
 // Resolves the driver's tensor-map encoder; false when unavailable.
@@ -189,8 +197,8 @@ cudaError_t launch_standin_tc(const uint16_t* U, const uint16_t* W, int R, int d
                               cudaStream_t st);
 // U [R, 2d] = [bf16(s_prev) | E[canvas]] for the stand-in (rows of done sequences skipped).
 void launch_standin_gather(const float* s_prev, const uint16_t* E, const int32_t* canvas,
-                           const uint8_t* done, int R, int d, int L, uint16_t* U,
-                           cudaStream_t st);
+                           const uint8_t* done, int R, int d, int L, int64_t V, uint32_t* err,
+                           uint16_t* U, cudaStream_t st);
 // With mtile_t set, P is relative to the row's maximum over each 256-token tile (mtile_t
 // [V/256, R]) and the reference maximum of each split's partial goes to mref [S, R] (see
 // ds_tc_selfcond.cu).

@@ -8,9 +8,13 @@
 //
 // The scratch array is a file-scope __device__ array, so every GPU that loads the library
 // holds it until the process exits. Host code cannot use the array's name as a device
-// address (on the host it names a stand-in object); the address is looked up once per device
-// with cudaGetSymbolAddress while that device is current, and passed to the kernels.
+// address (on the host it names a stand-in object); the address is looked up with
+// cudaGetSymbolAddress once per device context, while that device is current, and passed to the
+// kernels. The lookup is keyed on the context's unique id, so a device reset (which unloads the
+// module and may place the array elsewhere) leads to a fresh lookup instead of a stale pointer.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <mutex>
@@ -22,25 +26,67 @@ namespace {
 
 constexpr size_t kNoAllocScratchBytes = 64ull << 20;  // 64 MiB
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+// The first 256 bytes of the array hold the device error word of the last call (cleared at the
+// start of every call), at a fixed place so that ds_sampler_noalloc_status can read it.
+constexpr size_t kErrWordBytes = 256;
 
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kMaxDevices] = {};
+struct ScratchAddr {
+  unsigned long long ctx_id = 0;  // the context the address belongs to (0: none yet)
+  void* addr = nullptr;
+};
+ScratchAddr g_noalloc_addr[kMaxDevices];
 
-// Device address of the scratch array on the current device (looked up on first use).
+// Driver entry points for the current context's unique id (resolved once; a device reset or a
+// new primary context gives a new id, and the array may then sit at a new address).
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
+
+void resolve_ctx_entry_points() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+  fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+}
+
+// The unique id of the calling thread's current context; false when none is current.
+bool current_ctx_id(unsigned long long* id) {
+  std::call_once(g_ctx_once, resolve_ctx_entry_points);
+  CUcontext ctx = nullptr;
+  return g_ctx_current && g_ctx_id && g_ctx_current(&ctx) == CUDA_SUCCESS && ctx &&
+         g_ctx_id(ctx, id) == CUDA_SUCCESS && *id != 0;
+}
+
+// Device address of the scratch array in the current device's context: looked up with
+// cudaGetSymbolAddress (which also makes the device's primary context current) the first time a
+// context is seen on the device, and kept while that context lives.
 ds_status scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DS_ERR_CUDA;
+  unsigned long long id = 0;
+  const bool have = current_ctx_id(&id);
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
+  ScratchAddr& a = g_noalloc_addr[dev];
+  if (!have || a.ctx_id != id || !a.addr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
       cudaGetLastError();
       return DS_ERR_CUDA;
     }
-    g_noalloc_addr[dev] = p;
+    if (!current_ctx_id(&id)) return DS_ERR_CUDA;
+    a.addr = p;
+    a.ctx_id = id;
   }
-  *out = g_noalloc_addr[dev];
+  *out = a.addr;
   return DS_OK;
 }
 
@@ -62,16 +108,11 @@ extern "C" ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg,
   using namespace ds;
   if (!cfg || !a) return DS_ERR_INVALID_ARG;
   const ds_sampler_config& c = *cfg;
-  if (c.canvas_len < 128 || c.canvas_len > 1024 || c.canvas_len % 128) return DS_ERR_INVALID_ARG;
-  if (c.vocab < 256 || c.vocab > (1 << 24) || c.vocab % 256) return DS_ERR_INVALID_ARG;
-  if (c.d_model < 64 || c.d_model > 16384 || c.d_model % 64) return DS_ERR_INVALID_ARG;
-  if (c.dtype != DS_DTYPE_BF16 && c.dtype != DS_DTYPE_FP32) return DS_ERR_INVALID_ARG;
-  if (c.top_k < 0 || c.top_k > kMaxTopK || c.max_steps < 1) return DS_ERR_INVALID_ARG;
-  if (c.impl != DS_IMPL_AUTO && c.impl != DS_IMPL_TENSOR && c.impl != DS_IMPL_SIMT &&
-      c.impl != DS_IMPL_FUSED)
-    return DS_ERR_INVALID_ARG;
-  if (c.lock_rule != DS_LOCK_THRESHOLD && c.lock_rule != DS_LOCK_ENTROPY_BUDGET)
-    return DS_ERR_INVALID_ARG;
+  const ds_status vs = validate_config(c);
+  if (vs != DS_OK) return vs;
+  // the fused vocabulary pass needs a control block and range partials of its own, which this
+  // entry point does not carve: it is refused rather than replaced by another path
+  if (c.impl == DS_IMPL_FUSED) return DS_ERR_UNSUPPORTED;
   if (c.lock_rule == DS_LOCK_ENTROPY_BUDGET && !a->prev_argmax) return DS_ERR_INVALID_ARG;
   if (a->batch < 1 || (int64_t)a->batch * c.canvas_len > 65535) return DS_ERR_INVALID_ARG;
   if (!a->H || !a->E || !a->temperature || !a->tau || !a->step || !a->canvas || !a->lock ||
@@ -80,12 +121,11 @@ extern "C" ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg,
   auto aligned16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
   if (!aligned16(a->H) || !aligned16(a->E) || !aligned16(a->s)) return DS_ERR_INVALID_ARG;
   const int nc = n_chunks_of(c.vocab);
-  if (c.top_k > 0 && (int64_t)nc * c.top_k > kMaxTopKPool) return DS_ERR_UNSUPPORTED;
 
   bool tensor = false;
   if (c.impl != DS_IMPL_SIMT) {
     const bool ok = c.dtype == DS_DTYPE_BF16 && tc_available();
-    if ((c.impl == DS_IMPL_TENSOR || c.impl == DS_IMPL_FUSED) && !ok) return DS_ERR_UNSUPPORTED;
+    if (c.impl == DS_IMPL_TENSOR && !ok) return DS_ERR_UNSUPPORTED;
     tensor = ok;
   }
   int dev = 0, sms = 1;
@@ -111,13 +151,14 @@ extern "C" ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg,
   const size_t need = up(RV * 4) + 2 * up(RV * 2) + up((size_t)R * nstat * sizeof(ChunkStat)) +
                       up((size_t)R * sizeof(RowStat)) + up((size_t)R * nc * sizeof(Best)) +
                       (k > 0 ? up((size_t)R * nc * k * sizeof(Cand)) : 0) +
-                      up((size_t)S * R * d * 4) + up((size_t)B * 4) + 256;
+                      up((size_t)S * R * d * 4) + up((size_t)B * 4) + kErrWordBytes;
   if (need > kNoAllocScratchBytes) return DS_ERR_UNSUPPORTED;
 
   void* base = nullptr;
   ds_status st = scratch_address(&base);
   if (st != DS_OK) return st;
   Carver cv{static_cast<unsigned char*>(base)};
+  uint32_t* err = cv.take<uint32_t>(kErrWordBytes / sizeof(uint32_t));
   float* Y = cv.take<float>(RV);
   uint16_t* Phi = cv.take<uint16_t>(RV);
   uint16_t* Plo = cv.take<uint16_t>(RV);
@@ -127,7 +168,6 @@ extern "C" ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg,
   Cand* cand = k > 0 ? cv.take<Cand>((size_t)R * nc * k) : nullptr;
   float* Opart = cv.take<float>((size_t)S * R * d);
   float* Teff = cv.take<float>((size_t)B);
-  uint32_t* err = cv.take<uint32_t>(64);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The array keeps the previous call's contents: the error word must start at zero. Every
@@ -169,4 +209,22 @@ extern "C" ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg,
     launch_lock(B, L, V, c.max_steps, a->seed, nullptr, a->tau, a->sampled, a->conf, a->step,
                 a->canvas, a->lock, a->done, s);
   return cudaGetLastError() == cudaSuccess ? DS_OK : DS_ERR_CUDA;
+}
+
+extern "C" ds_status ds_sampler_noalloc_status(void* stream, ds_status* out) {
+  if (!out) return DS_ERR_INVALID_ARG;
+  void* base = nullptr;
+  const ds_status st = scratch_address(&base);
+  if (st != DS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t w = 0;
+  // pageable host memory: the copy completes before cudaMemcpyAsync returns or at the
+  // synchronisation below; nothing is allocated
+  if (cudaMemcpyAsync(&w, base, sizeof(w), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess ||
+      cudaMemsetAsync(base, 0, sizeof(uint32_t), s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return DS_ERR_CUDA;
+  *out = (w & ds::kErrTimeout) ? DS_ERR_TIMEOUT : (w ? DS_ERR_DEVICE : DS_OK);
+  return DS_OK;
 }

@@ -145,19 +145,29 @@ __global__ void __launch_bounds__(THREADS) k_selfcond_simt(const uint16_t* __res
     for (int q = 0; q < TN; ++q) out[(size_t)(m0 + ty + 16 * p) * d + n0 + tx + 16 * q] = acc[p][q];
 }
 
+// A canvas token outside [0, V) is a caller error that no host check can see in a device
+// buffer: the row read is clamped into E (so no access leaves it) and kErrBounds is recorded in
+// the device error word (ds_sampler_device_status -> DS_ERR_DEVICE).
+DS_DEV int64_t checked_token(int32_t t, int64_t V, uint32_t* err) {
+  if (t >= 0 && (int64_t)t < V) return t;
+  atomicOr(err, kErrBounds);
+  return t < 0 ? 0 : V - 1;
+}
+
 __global__ void __launch_bounds__(THREADS) k_standin_simt(const uint16_t* __restrict__ W,
                                                           const float* __restrict__ s_prev,
                                                           const uint16_t* __restrict__ E,
                                                           const int32_t* __restrict__ canvas,
                                                           const uint8_t* __restrict__ done, int d,
-                                                          int L, uint16_t* __restrict__ H) {
+                                                          int L, int64_t V, uint32_t* err,
+                                                          uint16_t* __restrict__ H) {
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * 64;
   if (done && done[m0 / L]) return;
   gemm_nt_tile<64>(
       m0, n0, 2 * d,
       [&](int m, int k) {
         if (k < d) return __bfloat162float(__float2bfloat16_rn(s_prev[(size_t)m * d + k]));
-        return bf16_to_f32(E[(size_t)canvas[m] * d + (k - d)]);
+        return bf16_to_f32(E[(size_t)checked_token(canvas[m], V, err) * d + (k - d)]);
       },
       [&](int n, int k) { return bf16_to_f32(W[(size_t)n * 2 * d + k]); },
       [&](int m, int n, float acc) {
@@ -168,8 +178,8 @@ __global__ void __launch_bounds__(THREADS) k_standin_simt(const uint16_t* __rest
 // U[r, k] = k < d ? bf16(s_prev[r, k]) : E[canvas[r], k - d], eight bf16 per thread.
 __global__ void k_standin_gather(const float* __restrict__ s_prev, const uint16_t* __restrict__ E,
                                  const int32_t* __restrict__ canvas,
-                                 const uint8_t* __restrict__ done, int R, int d, int L,
-                                 uint16_t* __restrict__ U) {
+                                 const uint8_t* __restrict__ done, int R, int d, int L, int64_t V,
+                                 uint32_t* err, uint16_t* __restrict__ U) {
   const int per_row = (2 * d) / 8;
   for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < (int64_t)R * per_row;
        q += (int64_t)gridDim.x * blockDim.x) {
@@ -184,7 +194,8 @@ __global__ void k_standin_gather(const float* __restrict__ s_prev, const uint16_
       out = make_uint4(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1),
                        *reinterpret_cast<const uint32_t*>(&h2), *reinterpret_cast<const uint32_t*>(&h3));
     } else {
-      out = *reinterpret_cast<const uint4*>(E + (size_t)canvas[r] * d + (k - d));
+      out = *reinterpret_cast<const uint4*>(E + (size_t)checked_token(canvas[r], V, err) * d +
+                                            (k - d));
     }
     *reinterpret_cast<uint4*>(U + (size_t)r * 2 * d + k) = out;
   }
@@ -193,11 +204,11 @@ __global__ void k_standin_gather(const float* __restrict__ s_prev, const uint16_
 }  // namespace
 
 void launch_standin_gather(const float* s_prev, const uint16_t* E, const int32_t* canvas,
-                           const uint8_t* done, int R, int d, int L, uint16_t* U,
-                           cudaStream_t st) {
+                           const uint8_t* done, int R, int d, int L, int64_t V, uint32_t* err,
+                           uint16_t* U, cudaStream_t st) {
   const int64_t n = (int64_t)R * (2 * d) / 8;
   const int blocks = (int)std::min<int64_t>((n + 255) / 256, 4096);
-  k_standin_gather<<<blocks, 256, 0, st>>>(s_prev, E, canvas, done, R, d, L, U);
+  k_standin_gather<<<blocks, 256, 0, st>>>(s_prev, E, canvas, done, R, d, L, V, err, U);
 }
 
 void launch_logits_simt(const void* H, const void* E, bool fp32_inputs, int R, int64_t V, int d,
@@ -223,9 +234,9 @@ void launch_selfcond_simt(const uint16_t* Phi, const uint16_t* Plo, const void* 
 
 void launch_standin_simt(const uint16_t* W, const float* s_prev, const uint16_t* E,
                          const int32_t* canvas, const uint8_t* done, int R, int d, int L,
-                         uint16_t* H_out, cudaStream_t st) {
+                         int64_t V, uint32_t* err, uint16_t* H_out, cudaStream_t st) {
   const dim3 grid((unsigned)(d / 64), (unsigned)(R / BM));
-  k_standin_simt<<<grid, THREADS, 0, st>>>(W, s_prev, E, canvas, done, d, L, H_out);
+  k_standin_simt<<<grid, THREADS, 0, st>>>(W, s_prev, E, canvas, done, d, L, V, err, H_out);
 }
 
 }  // namespace ds

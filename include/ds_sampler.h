@@ -114,7 +114,11 @@ typedef struct ds_sampler ds_sampler;
  *   temperature [B] float           T_b > 0 (input)
  *   tau         [B] float           lock threshold (input)
  *   step        [B] int32           steps already taken by each sequence (in/out)
- *   canvas      [B, L] int32        canvas tokens in [0, V) (in/out)
+ *   canvas      [B, L] int32        canvas tokens in [0, V) (in/out); ds_sampler_step_host
+ *                                   refuses others (DS_ERR_INVALID_ARG); in device memory the
+ *                                   stand-in, the one reader that indexes E by them, clamps an
+ *                                   out-of-range token into E and records DS_ERR_DEVICE for
+ *                                   ds_sampler_device_status
  *   lock        [B, L] uint8        1 = locked (in/out)
  *   done        [B] uint8           1 = finished; finished sequences are left untouched (in/out)
  *   s           [B, L, d] float     self-conditioning vector (out)
@@ -283,13 +287,26 @@ ds_status ds_sampler_launch_count(const ds_sampler* sampler, int64_t* count);
  * nothing; the scratch is about 8*B*L*V + 4*S*B*L*d bytes (S = vocabulary splits of the
  * self-conditioning GEMM), e.g. B=1, L=256, V=32768, d=1024 does not fit and V=16384 does.
  * The first call on a device looks up the array's device address (a one-time set-up with that
- * device current); make that first call before any stream capture. Every call shares the one
- * array and it keeps the last call's contents (the call clears what must start at zero): calls
- * whose work overlaps on the GPU -- two streams, or two host threads -- race on it and must be
- * serialised by the caller. Nothing is allocated: no cudaMalloc, cudaFree or allocating library
- * routine is called. */
+ * device current, repeated only if the device's context is replaced, e.g. after a device
+ * reset); make that first call before any stream capture. Every call shares the one array and
+ * it keeps the last call's contents (the call clears what must start at zero): calls whose work
+ * overlaps on the GPU -- two streams, or two host threads -- race on it and must be serialised
+ * by the caller. Nothing is allocated: no cudaMalloc, cudaFree or allocating library routine is
+ * called. The configuration is checked as by ds_sampler_create (max_batch aside);
+ * cfg->impl == DS_IMPL_FUSED is refused with DS_ERR_UNSUPPORTED (this entry point runs the
+ * separate logits and self-conditioning GEMMs only). A bounded wait that runs out inside the
+ * step's kernels is not reported by the return value (the call returns once the work is
+ * enqueued): read it with ds_sampler_noalloc_status after the step's work has completed. */
 ds_status ds_sampler_step_noalloc(const ds_sampler_config* cfg, const ds_step_args* args,
                                   void* stream);
+
+/* Device status of the last ds_sampler_step_noalloc call on the current device: synchronises
+ * `stream` (the stream that call used), reads the device error word kept in the same fixed
+ * array and clears it. *out = DS_OK, DS_ERR_TIMEOUT (a kernel's bounded wait ran out, so that
+ * step's outputs and state update are not valid) or DS_ERR_DEVICE (another device-side check
+ * failed). Each no-allocation step clears the word when it starts, so read it before the next
+ * one. Allocates nothing. */
+ds_status ds_sampler_noalloc_status(void* stream, ds_status* out);
 
 /* Self-test of the kernels' bounded waits: enqueues one small kernel that waits on an
  * mbarrier no thread will ever complete, gives up after limit_ns nanoseconds (1 us .. 1 s),
@@ -301,11 +318,13 @@ ds_status ds_sampler_selftest_wait(ds_sampler* sampler, int64_t limit_ns, void* 
 /* Read-only view of an internal buffer of the last step, for tests and profiling.
  * which: 0 = scaled logits y [B*L, V] float (only where the step materialises them: top_k > 0
  * or the CUDA-core path; else DS_ERR_UNSUPPORTED); 1 = row statistics [B*L] x {m, l, entropy,
- * argmax}; 2 = bf16 high part of the probabilities [B*L, V]; 3 = bf16 low part (exp(y - m) with
- * m the row maximum where y is materialised; on the tensor-core paths without top-k,
- * exp(y - m_g) with m_g the maximum of the token's 128-token segment); 4 = the segment records
- * of those paths [B*L, V/128] x {m_g, sum exp(y - m_g), sum exp(y - m_g)(y - m_g), argmax_g}
- * (16 bytes each; DS_ERR_UNSUPPORTED on the other paths). *ptr is [device]. */
+ * argmax}; 2 = bf16 high part of the probabilities [B*L, V]; 3 = bf16 low part. Their reference:
+ * exp(y - m) with m the row maximum where y is materialised (CUDA-core path); on the tensor-core
+ * path (DS_IMPL_TENSOR / AUTO), exp(y - m_t) with m_t the row's maximum over the token's
+ * 256-token tile; in the fused pass (DS_IMPL_FUSED), exp(y - m_g) with m_g the maximum of the
+ * token's 128-token segment. 4 = the 128-token segment records of the tensor-core paths
+ * [B*L, V/128] x {m_g, sum exp(y - m_g), sum exp(y - m_g)(y - m_g), argmax_g} (16 bytes each;
+ * DS_ERR_UNSUPPORTED on the other paths). *ptr is [device]. */
 ds_status ds_sampler_debug_buffer(ds_sampler* sampler, int32_t which, const void** ptr,
                                   size_t* bytes);
 

@@ -105,4 +105,12 @@ def test_product_path_never_imports_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(from|import)\s+oracle", text, re.M), f
-    assert "oracle" not in sys.modules or True
+    # importing the product (every module of the package) loads no oracle module
+    code = ("import sys, importlib, pkgutil, canvas_sampler_gb300 as p\n"
+            "for m in pkgutil.iter_modules(p.__path__):\n"
+            "    if m.name != 'build':\n"
+            "        importlib.import_module('canvas_sampler_gb300.' + m.name)\n"
+            "bad = [n for n in sys.modules if n == 'oracle' or n.startswith('oracle.')]\n"
+            "assert not bad, bad\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-2000:]

@@ -35,35 +35,72 @@ def _args(sampler, H, E, T, tau, state, out, seed):
     return sampler._step_args(H, E, T, tau, state, out, seed)
 
 
-def _close(a: StepOutputs, b: StepOutputs):
-    for k in ("sampled", "argmax"):
-        assert torch.equal(getattr(a, k), getattr(b, k)), k
-    for k in ("conf", "entropy"):
-        x, y = getattr(a, k).double(), getattr(b, k).double()
-        assert torch.all((x - y).abs() <= REL_TOL * y.abs().clamp_min(1.0)), k
+def _close(a: StepOutputs, b: StepOutputs, ref: dict, rows):
+    """a (no-allocation step) against b (the sampler's step) within the tests' tolerance, on the
+    rows where the oracle's (ref) top-two perturbed logits are at least 1e-4 apart: elsewhere
+    the two steps' different probability representations (row-relative there, tile-relative
+    here) may pick either of two near-tied tokens. Returns the number of excluded rows."""
+    ga, gb = out_np(a), out_np(b)
+    excluded = 0
+    for bb, i in rows:
+        if ref["gumbel_margin"][bb, i] < 1e-4:
+            excluded += 1
+            continue
+        assert ga["sampled"][bb, i] == gb["sampled"][bb, i], (bb, i)
+        ca, cb = float(ga["conf"][bb, i]), float(gb["conf"][bb, i])
+        assert abs(ca - cb) <= REL_TOL * max(abs(cb), 1e-30), (bb, i, ca, cb)
+    for bb, i in rows:
+        if ref["argmax_gap"][bb, i] >= 1e-4:
+            assert ga["argmax"][bb, i] == gb["argmax"][bb, i], (bb, i)
+    x, y = a.entropy.double(), b.entropy.double()
+    assert torch.all((x - y).abs() <= REL_TOL * y.abs().clamp_min(1.0)), "entropy"
     rel = (a.s.double() - b.s.double()).norm(dim=-1) / b.s.double().norm(dim=-1)
     assert rel.max().item() <= REL_TOL
+    return excluded
 
 
 def test_no_alloc_step_matches_the_sampler_step_twice_in_a_row():
     lib = C.load_library()
     w, inp, E, H, T, tau = _inputs()
-    ref = Sampler(w.V, w.d, canvas_len=w.L, max_batch=w.B, dtype="bf16", max_steps=w.max_steps)
+    case = GpuCase(w, inputs=inp)
+    ref = case.sampler
     cfg = ref._cfg
     st_ref = CanvasState.from_numpy(inp["canvas"], inp["lock"], inp["step"], inp["done"])
     st_new = st_ref.clone()
+    rows = [(b, i) for b in range(w.B) for i in range(w.L)]
+    stream = torch.cuda.current_stream().cuda_stream
     for call in range(2):  # the second call continues the canvas from the first call's state
+        pre = state_np(st_new)
+        oracle_ref = oracle_step(case, pre)
         out_ref = ref.step(H, E, T, tau, st_ref, inp["seed"])
         out_new = StepOutputs.empty(w.B, w.L, w.d)
         a = _args(ref, H, E, T, tau, st_new, out_new, inp["seed"])
-        rc = lib.ds_sampler_step_noalloc(ctypes.byref(cfg), ctypes.byref(a),
-                                         torch.cuda.current_stream().cuda_stream)
+        rc = lib.ds_sampler_step_noalloc(ctypes.byref(cfg), ctypes.byref(a), stream)
         assert rc == C.DS_OK, C.status_string(rc)
+        status = ctypes.c_int32(-1)
+        assert lib.ds_sampler_noalloc_status(stream, ctypes.byref(status)) == C.DS_OK
+        assert status.value == C.DS_OK
         torch.cuda.synchronize()
-        _close(out_new, out_ref)
-        for k in ("canvas", "lock", "step", "done"):
-            assert torch.equal(getattr(st_new, k), getattr(st_ref, k)), (call, k)
+        excluded = _close(out_new, out_ref, oracle_ref, rows)
+        assert excluded <= max(2, len(rows) // 100), excluded
+        # the no-allocation step against the oracle as well
+        rep = compare_outputs(out_np(out_new), oracle_ref, rows)
+        assert rep["excluded"] <= max(2, len(rows) // 100)
+        if excluded == 0:
+            for k in ("canvas", "lock", "step", "done"):
+                assert torch.equal(getattr(st_new, k), getattr(st_ref, k)), (call, k)
+        else:  # a near-tie may lock a different token: continue both from the same state
+            for k in ("canvas", "lock", "step", "done"):
+                getattr(st_ref, k).copy_(getattr(st_new, k))
     assert int(st_new.step[0]) == 2
+
+
+def test_no_alloc_status_reads_and_clears():
+    lib = C.load_library()
+    status = ctypes.c_int32(-1)
+    assert lib.ds_sampler_noalloc_status(None, ctypes.byref(status)) == C.DS_OK
+    assert status.value == C.DS_OK
+    assert lib.ds_sampler_noalloc_status(None, None) == C.DS_ERR_INVALID_ARG
 
 
 def test_no_alloc_step_rejects_what_does_not_fit():
