@@ -104,6 +104,7 @@ def test_standin_loop_teacher_forced():
     Wt = torch.from_numpy(case.inp["W"].view(np.int16)).view(torch.bfloat16).cuda()
     s_prev = torch.zeros(w.B, w.L, w.d, dtype=torch.float32, device="cuda")
     Hbuf = torch.zeros(w.B, w.L, w.d, dtype=torch.bfloat16, device="cuda")
+    checked = excluded = 0
     for it in range(w.max_steps):
         pre = state_np(state)
         if pre["done"].all():
@@ -123,7 +124,13 @@ def test_standin_loop_teacher_forced():
         g, post = out_np(out), state_np(state)
         ref = oracle_step(case, pre, H64=oracle.bf16_bits_to_f64(H_bits))
         rows = [(b, i) for b in range(w.B) if active[b] for i in range(w.L)]
-        compare_outputs(g, ref, rows, top_k=w.top_k)
+        rep = compare_outputs(g, ref, rows, top_k=w.top_k)
+        checked += rep["checked"]
+        excluded += rep["excluded"]
         check_lock_update(pre, g, post, ref, case.inp["tau"], case.inp["seed"], w.V, w.max_steps)
         s_prev = out.s.clone()
     assert state.done.all().item()
+    # near-uniform stand-in softmaxes put ~1.5% of positions at a top-64 boundary the oracle
+    # calls ambiguous (a token within 1e-4 of the 64th logit could win); 3% bounds it
+    print(f"standin loop: {checked} positions checked, {excluded} excluded")
+    assert excluded <= max(2, int(0.03 * checked)), (excluded, checked)
