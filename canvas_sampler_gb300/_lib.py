@@ -58,6 +58,16 @@ class ds_block_args(ctypes.Structure):
                 ("init_canvas", c_void_p), ("out_canvas", c_void_p), ("out_steps", c_void_p)]
 
 
+class ds_shard_partial(ctypes.Structure):
+    _fields_ = [("rows", c_void_p), ("best", c_void_p), ("O", c_void_p), ("cand", c_void_p)]
+
+
+# bytes of one record of each part of a shard's partial (ds_shard_row, ds_shard_best,
+# ds_shard_cand)
+SHARD_ROW_BYTES = 16
+SHARD_BEST_BYTES = 16
+SHARD_CAND_BYTES = 8
+
 # name -> (restype, argtypes): every function declared in include/ds_sampler.h
 SIGNATURES = {
     "ds_abi_version": (c_int32, []),
@@ -82,6 +92,10 @@ SIGNATURES = {
     "ds_sampler_selftest_wait": (c_int32, [c_void_p, c_int64, c_void_p]),
     "ds_sampler_step_noalloc": (c_int32, [POINTER(ds_sampler_config), POINTER(ds_step_args), c_void_p]),
     "ds_sampler_noalloc_status": (c_int32, [c_void_p, POINTER(c_int32)]),
+    "ds_sampler_step_shard": (c_int32, [c_void_p, POINTER(ds_step_args), c_int32, c_int64,
+                                        POINTER(ds_shard_partial), c_void_p]),
+    "ds_merge_shards": (c_int32, [c_void_p, POINTER(ds_step_args), c_int32,
+                                  POINTER(ds_shard_partial), c_int64, c_void_p]),
 }
 
 PHASES = ["logits", "stats", "topk", "convert", "selfcond", "finalize", "lock"]

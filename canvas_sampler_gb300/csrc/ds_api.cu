@@ -463,8 +463,11 @@ ds_status ds_sampler_create(const ds_sampler_config* cfg, ds_sampler** out) {
   s->Plo = carve<uint16_t>(s, Rm * V, &e);
   if (!s->fused) s->cs = carve<ChunkStat>(s, Rm * std::max<size_t>(n_chunks, V / kTcSegment), &e);
   s->rs = carve<RowStat>(s, Rm, &e);
-  s->best = carve<Best>(s, Rm * n_chunks, &e);
-  if (c.top_k > 0) s->cand = carve<Cand>(s, Rm * n_chunks * c.top_k, &e);
+  // best / cand also hold a shard merge's records (one per shard, or k candidates per shard)
+  s->best = carve<Best>(s, Rm * std::max(n_chunks, kMaxShards), &e);
+  if (c.top_k > 0)
+    s->cand = carve<Cand>(
+        s, Rm * std::max(n_chunks, std::min(kMaxShards, kMaxTopKPool / c.top_k)) * c.top_k, &e);
   s->Opart = carve<float>(s, opart, &e);
   s->Teff = carve<float>(s, (size_t)c.max_batch, &e);
   if (s->impl != DS_IMPL_SIMT && c.d_model % 256 == 0) s->U = carve<uint16_t>(s, Rm * 2 * d, &e);
@@ -639,6 +642,94 @@ ds_status ds_sampler_step_host(ds_sampler* s, const ds_step_args* h, void* strea
     std::memcpy(h->argmax + b * L, blk_h + oarg + b * L * 4, L * 4);
   }
   return DS_OK;
+}
+
+static_assert(sizeof(ds_shard_row) == sizeof(RowStat) && sizeof(ds_shard_best) == sizeof(Best) &&
+                  sizeof(ds_shard_cand) == sizeof(Cand),
+              "the shard records are the kernels' row, winner and candidate records");
+
+ds_status ds_sampler_step_shard(ds_sampler* s, const ds_step_args* a, int32_t token_offset,
+                               int64_t vocab_total, const ds_shard_partial* out, void* stream) {
+  if (!s || !a || !out) return DS_ERR_INVALID_ARG;
+  if (a->batch < 1 || a->batch > s->cfg.max_batch) return DS_ERR_INVALID_ARG;
+  if (!a->H || !a->E || !a->temperature || !a->step || !a->done || !out->rows || !out->best ||
+      !out->O || (s->cfg.top_k > 0 && !out->cand))
+    return DS_ERR_INVALID_ARG;
+  if (!aligned(a->H, 16) || !aligned(a->E, 16) || !aligned(out->O, 16)) return DS_ERR_INVALID_ARG;
+  if (token_offset < 0 || token_offset % 256 || vocab_total > (1 << 24) ||
+      (int64_t)token_offset + s->cfg.vocab > vocab_total)
+    return DS_ERR_INVALID_ARG;
+  // the shard step runs the tensor-core path (logits as tile-relative probabilities)
+  if (s->impl != DS_IMPL_TENSOR || s->fused) return DS_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int L = s->cfg.canvas_len, d = s->cfg.d_model, B = a->batch, R = B * L;
+  const int64_t V = s->cfg.vocab;
+  const int k = s->cfg.top_k;
+  const int S = splits_for(s, B);
+  s->last_batch = B;
+  const float* T = a->temperature;
+  if (s->cfg.t_start > 0.f) {
+    launch_temperature(a->step, B, s->cfg.t_start, s->cfg.t_end, s->cfg.max_steps, s->Teff, st);
+    T = s->Teff;
+    s->launches += 1;
+  }
+  cudaError_t e = launch_logits_p_tc(static_cast<const uint16_t*>(a->H),
+                                     static_cast<const uint16_t*>(a->E), R, V, d, L, T, a->done,
+                                     s->Phi, s->Plo, s->cs, s->mseg_t, s->err, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  const bool race_in_sc = k == 0 && race_in_selfcond(s, R, d);
+  if (!race_in_sc) launch_row_merge(s->cs, (int)(V / kTcSegment), R, L, a->done, s->rs, st);
+  if (k > 0)
+    launch_topk_row(s->Phi, s->Plo, s->cs, s->mseg_t, s->rs, R, V, L, a->done, k, s->cand, st,
+                    token_offset);
+  if (k == 0 && !race_in_sc)
+    launch_gumbel_items(s->Phi, s->Plo, s->cs, s->rs, R, V, L, a->done, a->step, a->seed, s->blk,
+                        true, s->best, st, token_offset);
+  GumbelWork gw{s->Phi, s->Plo, s->cs,  s->rs, a->done, a->step, s->blk,
+                a->seed, s->best, s->gq, R,    L,       s->n_chunks, 1,
+                s->rs,   s->row_flags, s->err};
+  gw.j_offset = token_offset;
+  e = launch_selfcond_tc(s->Phi, s->Plo, static_cast<const uint16_t*>(a->E), R, V, d, L, a->done,
+                         S, s->Opart, s->mseg_t, s->mref, s->err, race_in_sc ? &gw : nullptr, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  launch_shard_export(s->rs, s->best, s->n_chunks, s->cand, k, R, L, a->done, s->Opart, S, d,
+                      s->mref, token_offset, reinterpret_cast<RowStat*>(out->rows),
+                      reinterpret_cast<Best*>(out->best), out->O,
+                      reinterpret_cast<Cand*>(out->cand), st);
+  // logits, [row merge], [top-k | race], self-conditioning, export
+  s->launches += 3 + (race_in_sc ? 0 : 1) + ((k > 0 || !race_in_sc) ? 1 : 0);
+  return cuda_status(cudaGetLastError());
+}
+
+ds_status ds_merge_shards(ds_sampler* s, const ds_step_args* a, int32_t n_shards,
+                          const ds_shard_partial* parts, int64_t vocab_total, void* stream) {
+  if (!s || !parts) return DS_ERR_INVALID_ARG;
+  ds_status r = check_step_args(s, a);
+  if (r != DS_OK) return r;
+  const int k = s->cfg.top_k;
+  if (n_shards < 1 || n_shards > kMaxShards || !parts->rows || !parts->best || !parts->O ||
+      (k > 0 && !parts->cand) || !aligned(parts->O, 16))
+    return DS_ERR_INVALID_ARG;
+  if (vocab_total < 256 || vocab_total > (1 << 24)) return DS_ERR_INVALID_ARG;
+  // the merge keeps one record (or k candidates) per shard and row in the workspace
+  if (k > 0 && (int64_t)n_shards * k > kMaxTopKPool) return DS_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int L = s->cfg.canvas_len, d = s->cfg.d_model, B = a->batch, R = B * L;
+  launch_shard_merge(n_shards, reinterpret_cast<const RowStat*>(parts->rows),
+                     reinterpret_cast<const Best*>(parts->best), parts->O,
+                     reinterpret_cast<const Cand*>(parts->cand), k, R, d, L, a->done, s->rs,
+                     s->best, s->cand, a->s, st);
+  launch_finalize(s->rs, s->best, k > 0 ? s->cand : nullptr, n_shards, k, R, L, a->done, a->step,
+                  a->seed, s->blk, a->sampled, a->conf, a->entropy, a->argmax, st);
+  if (s->cfg.lock_rule == DS_LOCK_ENTROPY_BUDGET)
+    launch_lock_entropy(B, L, vocab_total, s->cfg.max_steps, a->seed, s->blk,
+                        s->cfg.entropy_budget, s->cfg.stop_entropy, a->sampled, a->entropy,
+                        a->argmax, a->prev_argmax, a->step, a->canvas, a->lock, a->done, st);
+  else
+    launch_lock(B, L, vocab_total, s->cfg.max_steps, a->seed, s->blk, a->tau, a->sampled,
+                a->conf, a->step, a->canvas, a->lock, a->done, st);
+  s->launches += 3;
+  return cuda_status(cudaGetLastError());
 }
 
 ds_status ds_standin_hidden(ds_sampler* s, const void* W, const float* s_prev, const void* E,

@@ -15,6 +15,8 @@ namespace ds {
 constexpr int kChunk = 8192;
 // Most partial sums of s that the finalize kernel combines.
 constexpr int kMaxSplits = 256;
+// Most vocabulary shards one merge combines.
+constexpr int kMaxShards = 64;
 // Largest top-k the sampler supports, and the largest candidate pool its merge takes.
 constexpr int kMaxTopK = 256;
 constexpr int kMaxTopKPool = 8192;
@@ -65,7 +67,8 @@ void launch_topk_chunk(const float* Y, int R, int64_t V, int L, const uint8_t* d
 // row (cand [R, k]) carrying y = m + ln p.
 void launch_topk_row(const uint16_t* Phi, const uint16_t* Plo, const ChunkStat* seg,
                      const float* mtile_t, const RowStat* rs, int R, int64_t V, int L,
-                     const uint8_t* done, int k, Cand* cand, cudaStream_t st);
+                     const uint8_t* done, int k, Cand* cand, cudaStream_t st,
+                     int64_t j_offset = 0);
 void launch_finalize(const RowStat* rs, const Best* best, const Cand* cand, int n_chunks, int k,
                      int R, int L, const uint8_t* done, const int32_t* step, uint64_t seed,
                      const int32_t* blk, int32_t* sampled, float* conf, float* entropy,
@@ -101,6 +104,9 @@ struct GumbelWork {
   RowStat* rs_out;
   uint32_t* row_flags;  // [R], zero when allocated
   uint32_t* err;
+  // Global index of the first token of the vocabulary the probabilities cover (a vocabulary
+  // shard's step): the race's draws and its winners use global token indices.
+  int64_t j_offset;
 };
 
 // Gumbel-max sample per (row, chunk) from probabilities stored relative to each 128-token
@@ -109,9 +115,20 @@ struct GumbelWork {
 void launch_gumbel_items(const uint16_t* Phi, const uint16_t* Plo, const ChunkStat* seg,
                        const RowStat* rs, int R, int64_t V, int L, const uint8_t* done,
                        const int32_t* step, uint64_t seed, const int32_t* blk, bool tile_ref,
-                       Best* best, cudaStream_t st);
+                       Best* best, cudaStream_t st, int64_t j_offset = 0);
 void launch_reduce_s(const float* Opart, int S, int R, int d, int L, const uint8_t* done,
                      const RowStat* rs, float* s, cudaStream_t st);
+// A vocabulary shard's step record (k_shard_export) and the merge of n shards' records
+// (k_shard_merge, then launch_finalize over its row statistics and winner / candidate pool);
+// see ds_rows.cu.
+void launch_shard_export(const RowStat* rs, const Best* best, int n_chunks, const Cand* cand,
+                         int k, int R, int L, const uint8_t* done, const float* Opart, int S,
+                         int d, const float* mref, int64_t j_offset, RowStat* rows_out,
+                         Best* best_out, float* O_out, Cand* cand_out, cudaStream_t st);
+void launch_shard_merge(int n, const RowStat* rows, const Best* best, const float* O,
+                        const Cand* cand, int k, int R, int d, int L, const uint8_t* done,
+                        RowStat* rs_out, Best* best_out, Cand* pool_out, float* s_out,
+                        cudaStream_t st);
 void launch_lock(int B, int L, int64_t V, int max_steps, uint64_t seed, const int32_t* blk,
                  const float* tau, const int32_t* sampled, const float* conf, int32_t* step,
                  int32_t* canvas, uint8_t* lock, uint8_t* done, cudaStream_t st);

@@ -521,7 +521,8 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(const uint16_t* __restric
                                                        const RowStat* __restrict__ rs, int R,
                                                        int64_t V, int L,
                                                        const uint8_t* __restrict__ done, int k,
-                                                       Cand* __restrict__ cand) {
+                                                       Cand* __restrict__ cand,
+                                                       int64_t j_offset) {
   __shared__ int hist[256];
   __shared__ int sel[2];
   __shared__ int sh_cnt[2][kTkWarps];
@@ -644,7 +645,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(const uint16_t* __restric
     const unsigned tk_b = __ballot_sync(0xffffffffu, take);
     if (take) {
       const int slot = take_before + taken + __popc(tk_b & below);
-      if (slot < k) out[slot] = Cand{p > 0.f ? m + logf(p) : -INFINITY, (int32_t)j};
+      if (slot < k) out[slot] = Cand{p > 0.f ? m + logf(p) : -INFINITY, (int32_t)(j + j_offset)};
     }
     taken += __popc(tk_b);
   });
@@ -1160,9 +1161,10 @@ void launch_topk_chunk(const float* Y, int R, int64_t V, int L, const uint8_t* d
 
 void launch_topk_row(const uint16_t* Phi, const uint16_t* Plo, const ChunkStat* seg,
                      const float* mtile_t, const RowStat* rs, int R, int64_t V, int L,
-                     const uint8_t* done, int k, Cand* cand, cudaStream_t st) {
+                     const uint8_t* done, int k, Cand* cand, cudaStream_t st,
+                     int64_t j_offset) {
   launch_k(k_topk_row, dim3(R), dim3(kThreads), 0, st, Phi, Plo, seg, mtile_t, rs, R, V, L, done,
-           k, cand);
+           k, cand, j_offset);
 }
 
 void launch_finalize(const RowStat* rs, const Best* best, const Cand* cand, int n_chunks, int k,
@@ -1185,10 +1187,10 @@ void launch_finalize_with_s(const RowStat* rs, const Best* best, const Cand* can
 void launch_gumbel_items(const uint16_t* Phi, const uint16_t* Plo, const ChunkStat* seg,
                        const RowStat* rs, int R, int64_t V, int L, const uint8_t* done,
                        const int32_t* step, uint64_t seed, const int32_t* blk, bool tile_ref,
-                       Best* best, cudaStream_t st) {
+                       Best* best, cudaStream_t st, int64_t j_offset) {
   const int nc = n_chunks_of(V);
   const GumbelWork g{Phi, Plo, seg,     rs, done,    step, blk, seed, best, nullptr, R, L, nc,
-                     tile_ref ? 1 : 0, nullptr, nullptr, nullptr};
+                     tile_ref ? 1 : 0, nullptr, nullptr, nullptr, j_offset};
   // warps per item: doubled while the items' warps would not fill the warps every SM holds
   // (two CTAs of 8). Race time measured against the rule at 1024 / 2048 / 4096 items:
   // 0.024 / 0.031 / 0.118 ms (4, 2, 1 warps), 0.025 / 0.039 / 0.118 with half as many warps,
@@ -1229,6 +1231,168 @@ void launch_loop_begin(const uint8_t* done, int B, int32_t* iter, int max_iters,
 void launch_loop_end(const uint8_t* done, int B, int32_t* iter, int max_iters,
                      cudaGraphConditionalHandle h, cudaStream_t st) {
   k_loop_end<<<1, 32, 0, st>>>(done, B, iter, max_iters, h);
+}
+
+// ------------------------------------------------------------------------------------------
+// vocabulary shards: one step's partial record over a token range, and the merge of the records
+// of every range (DiffusionGemma Technical Report, section 6 "Multi-user throughput": scaling
+// the sampler; the softmax, its entropy and s decompose over any partition of the vocabulary)
+// ------------------------------------------------------------------------------------------
+
+// Per row of a shard's step: the row statistics with the global argmax token, the shard's race
+// winner (best of its chunk records: score -key and ln p relative to the shard's maximum m_r),
+// the un-normalised self-conditioning sum O_r = sum_split exp(mref - m_r) O_split (split order)
+// and, with top-k, the row's k candidates.
+__global__ void __launch_bounds__(kThreads) k_shard_export(
+    const RowStat* __restrict__ rs, const Best* __restrict__ best, int n_chunks,
+    const Cand* __restrict__ cand, int k, int L, const uint8_t* __restrict__ done,
+    const float* __restrict__ Opart, int S, int R, int d, const float* __restrict__ mref,
+    int64_t j_offset, RowStat* __restrict__ rows_out, Best* __restrict__ best_out,
+    float* __restrict__ O_out, Cand* __restrict__ cand_out) {
+  __shared__ float shv[32], shy;
+  __shared__ int32_t shj[32];
+  __shared__ float sh_sc[kMaxSplits];
+  pdl_wait();
+  const int r = blockIdx.x;
+  if (done && done[r / L]) return;
+  const RowStat st = rs[r];
+  for (int sp = threadIdx.x; sp < S; sp += kThreads)
+    sh_sc[sp] = mref ? expf(mref[(size_t)sp * R + r] - st.m) : 1.f;
+  __syncthreads();
+  const int64_t plane = (int64_t)R * d;
+  const float4* src = reinterpret_cast<const float4*>(Opart + (size_t)r * d);
+  float4* dst = reinterpret_cast<float4*>(O_out + (size_t)r * d);
+  for (int q = threadIdx.x; q < d / 4; q += kThreads) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp = 0; sp < S; ++sp) {
+      const float4 t = src[sp * plane / 4 + q];
+      const float c = sh_sc[sp];
+      acc.x = fmaf(t.x, c, acc.x);
+      acc.y = fmaf(t.y, c, acc.y);
+      acc.z = fmaf(t.z, c, acc.z);
+      acc.w = fmaf(t.w, c, acc.w);
+    }
+    dst[q] = acc;
+  }
+  if (k == 0) {
+    float bv = -INFINITY, by = 0.f;
+    int32_t bj = INT_MAX;
+    for (int q = threadIdx.x; q < n_chunks; q += kThreads) {
+      const Best t = best[(size_t)r * n_chunks + q];
+      if (better(t.v, t.j, bv, bj)) {
+        bv = t.v;
+        bj = t.j;
+        by = t.y;
+      }
+    }
+    block_best(bv, bj, by, shv, shj, &shy);
+    if (threadIdx.x == 0) best_out[r] = Best{bv, bj, bj == INT_MAX ? 0.f : by, 1};
+  } else {
+    for (int t = threadIdx.x; t < k; t += kThreads) cand_out[(size_t)r * k + t] = cand[(size_t)r * k + t];
+  }
+  if (threadIdx.x == 0)
+    rows_out[r] = RowStat{st.m, st.l, st.ent, (int32_t)(st.arg + j_offset)};
+}
+
+// Per row, the records of n shards (shard-major arrays, shards in increasing token order):
+// m = max m_q; l = sum_q l_q e^{m_q - m}; entropy by the mixture identity H = sum_q w_q H_q -
+// sum_q w_q ln w_q with w_q = l_q e^{m_q - m} / l (fp64); argmax the largest m_q, lowest token
+// on ties; s = sum_q e^{m_q - m} O_q / l (shard order). Without top-k each shard's race winner
+// becomes a record comparable across shards: key_q is relative to m_q, and relative to m it is
+// key_q e^{m - m_q}, so its score is (m_q - m) - ln key_q and its ln p is lnp_q + (m_q - m);
+// with top-k each shard's candidates go to the row's pool in token order.
+__global__ void __launch_bounds__(kThreads) k_shard_merge(
+    int n, const RowStat* __restrict__ rows, const Best* __restrict__ best,
+    const float* __restrict__ O, const Cand* __restrict__ cand, int k, int R, int d, int L,
+    const uint8_t* __restrict__ done, RowStat* __restrict__ rs_out, Best* __restrict__ best_out,
+    Cand* __restrict__ pool_out, float* __restrict__ s_out) {
+  __shared__ float sh_sc[kMaxShards];
+  __shared__ float sh_l;
+  pdl_wait();
+  const int r = blockIdx.x;
+  if (done && done[r / L]) return;
+  if (threadIdx.x == 0) {
+    float m = -INFINITY;
+    int32_t arg = INT_MAX;
+    for (int q = 0; q < n; ++q) {
+      const RowStat t = rows[(size_t)q * R + r];
+      if (better(t.m, t.arg, m, arg)) {
+        m = t.m;
+        arg = t.arg;
+      }
+    }
+    double l = 0.0;
+    for (int q = 0; q < n; ++q) {
+      const RowStat t = rows[(size_t)q * R + r];
+      const double wq = (double)t.l * exp((double)t.m - (double)m);
+      sh_sc[q] = expf(t.m - m);
+      l += wq;
+    }
+    double h = 0.0;
+    for (int q = 0; q < n; ++q) {
+      const RowStat t = rows[(size_t)q * R + r];
+      const double wq = (double)t.l * exp((double)t.m - (double)m) / l;
+      if (wq > 0.0) h += wq * ((double)t.ent - log(wq));
+    }
+    rs_out[r] = RowStat{m, (float)l, (float)h, arg};
+    sh_l = (float)l;
+    if (k == 0) {
+      for (int q = 0; q < n; ++q) {
+        const Best b = best[(size_t)q * R + r];
+        const float dm = rows[(size_t)q * R + r].m - m;
+        const bool has = b.j != INT_MAX && b.v > -INFINITY;
+        best_out[(size_t)r * n + q] =
+            Best{has ? dm - logf(-b.v) : -INFINITY, b.j, has ? b.y + dm : 0.f, 1};
+      }
+    }
+  }
+  if (k > 0) {
+    // each shard's k candidates (distinct tokens, or unused slots with token INT_MAX) placed in
+    // token order: candidate t goes to the slot of its rank among the shard's tokens
+    for (int e = threadIdx.x; e < n * k; e += kThreads) {
+      const int q = e / k;
+      const Cand c = cand[((size_t)q * R + r) * k + e % k];
+      int rank = 0;
+      for (int u = 0; u < k; ++u) {
+        const int32_t ju = cand[((size_t)q * R + r) * k + u].j;
+        rank += (ju < c.j || (ju == c.j && u < e % k)) ? 1 : 0;
+      }
+      pool_out[(size_t)r * n * k + (size_t)q * k + rank] = c;
+    }
+  }
+  __syncthreads();
+  const float l = sh_l;
+  const int64_t plane = (int64_t)R * d;
+  const float4* src = reinterpret_cast<const float4*>(O + (size_t)r * d);
+  float4* dst = reinterpret_cast<float4*>(s_out + (size_t)r * d);
+  for (int c4 = threadIdx.x; c4 < d / 4; c4 += kThreads) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < n; ++q) {
+      const float4 t = src[q * plane / 4 + c4];
+      const float c = sh_sc[q];
+      acc.x = fmaf(t.x, c, acc.x);
+      acc.y = fmaf(t.y, c, acc.y);
+      acc.z = fmaf(t.z, c, acc.z);
+      acc.w = fmaf(t.w, c, acc.w);
+    }
+    dst[c4] = make_float4(acc.x / l, acc.y / l, acc.z / l, acc.w / l);
+  }
+}
+
+void launch_shard_export(const RowStat* rs, const Best* best, int n_chunks, const Cand* cand,
+                         int k, int R, int L, const uint8_t* done, const float* Opart, int S,
+                         int d, const float* mref, int64_t j_offset, RowStat* rows_out,
+                         Best* best_out, float* O_out, Cand* cand_out, cudaStream_t st) {
+  launch_k(k_shard_export, dim3(R), dim3(kThreads), 0, st, rs, best, n_chunks, cand, k, L, done,
+           Opart, S, R, d, mref, j_offset, rows_out, best_out, O_out, cand_out);
+}
+
+void launch_shard_merge(int n, const RowStat* rows, const Best* best, const float* O,
+                        const Cand* cand, int k, int R, int d, int L, const uint8_t* done,
+                        RowStat* rs_out, Best* best_out, Cand* pool_out, float* s_out,
+                        cudaStream_t st) {
+  launch_k(k_shard_merge, dim3(R), dim3(kThreads), 0, st, n, rows, best, O, cand, k, R, d, L,
+           done, rs_out, best_out, pool_out, s_out);
 }
 
 }  // namespace ds

@@ -300,7 +300,7 @@ DS_DEV void gumbel_race_segments(const GumbelWork& g, int64_t V, int r, int c, i
       off_n = locate(k + 1, s);
       slab_load(nxt, ph + off_n, pl + off_n, s);
     }
-    const int64_t j = j0 + off;
+    const int64_t j = g.j_offset + j0 + off;  // global token index (draws and winners)
     if (k == 0) {
       if (cur.sc > 0.f)
         gumbel_seed4(cur.h0, cur.l0, cur.sc, j, (uint32_t)i, sid, st, g.seed, kbest, bj, bp);

@@ -70,6 +70,39 @@ class StepOutputs:
                            torch.zeros(B, L, dtype=torch.int32, **kw))
 
 
+@dataclass
+class ShardPartial:
+    """Partial records of n vocabulary shards, stacked in token order (device tensors):
+    rows [n, R, 4] (m, l, entropy, argmax bits), best [n, R, 4] (score, token bits, ln p, 0),
+    O [n, R, d] and, with top-k, cand [n, R, k, 2] (y, token bits); R = B L. See
+    ds_sampler_step_shard / ds_merge_shards in include/ds_sampler.h."""
+    rows: torch.Tensor
+    best: torch.Tensor
+    O: torch.Tensor
+    cand: torch.Tensor | None = None
+
+    @staticmethod
+    def empty(n, B, L, d, top_k=0, device="cuda"):
+        R = B * L
+        return ShardPartial(torch.zeros(n, R, 4, dtype=torch.float32, device=device),
+                            torch.zeros(n, R, 4, dtype=torch.float32, device=device),
+                            torch.zeros(n, R, d, dtype=torch.float32, device=device),
+                            torch.zeros(n, R, top_k, 2, dtype=torch.float32, device=device)
+                            if top_k else None)
+
+    @staticmethod
+    def stack(parts: list["ShardPartial"]) -> "ShardPartial":
+        return ShardPartial(torch.cat([p.rows for p in parts]), torch.cat([p.best for p in parts]),
+                            torch.cat([p.O for p in parts]),
+                            None if parts[0].cand is None else torch.cat([p.cand for p in parts]))
+
+    def tensors(self) -> list[torch.Tensor]:
+        return [t for t in (self.rows, self.best, self.O, self.cand) if t is not None]
+
+    def c_struct(self):
+        return C.ds_shard_partial(_ptr(self.rows), _ptr(self.best), _ptr(self.O), _ptr(self.cand))
+
+
 class Sampler:
     """One sampler (workspace + graphs) on one CUDA device."""
 
@@ -217,6 +250,39 @@ class Sampler:
         C.check(self.lib.ds_block_loop(self.handle, byref(ba), _stream_handle(stream)),
                 "ds_block_loop")
         return out_canvas, out_steps
+
+    def step_shard(self, H, E_shard, temperature, tau, state: CanvasState, seed: int,
+                   token_offset: int, vocab_total: int, out: ShardPartial | None = None,
+                   stream=None) -> ShardPartial:
+        """The partial record of one vocabulary shard (E_shard = rows token_offset ..
+        token_offset + vocab of the full table); state is read (step, done), not updated."""
+        B = state.canvas.shape[0]
+        out = ShardPartial.empty(1, B, self.L, self.d, self.top_k) if out is None else out
+        dummy = StepOutputs.empty(B, self.L, self.d) if not hasattr(self, "_shard_dummy") or \
+            self._shard_dummy.s.shape[0] != B else self._shard_dummy
+        self._shard_dummy = dummy
+        a = self._step_args(H, E_shard, temperature, tau, state, dummy, seed)
+        part = out.c_struct()
+        C.check(self.lib.ds_sampler_step_shard(self.handle, byref(a), int(token_offset),
+                                               int(vocab_total), byref(part),
+                                               _stream_handle(stream)), "ds_sampler_step_shard")
+        return out
+
+    def merge_shards(self, parts: ShardPartial, temperature, tau, state: CanvasState, seed: int,
+                     vocab_total: int, out: StepOutputs | None = None, stream=None,
+                     E=None) -> StepOutputs:
+        """Merge n shards' records (token order) into the step's outputs and update state."""
+        B = state.canvas.shape[0]
+        out = StepOutputs.empty(B, self.L, self.d) if out is None else out
+        n = parts.rows.shape[0]
+        # H and E are not read by the merge; any valid device pointers satisfy the argument checks
+        ref = parts.O
+        a = self._step_args(ref, ref, temperature, tau, state, out, seed)
+        part = parts.c_struct()
+        C.check(self.lib.ds_merge_shards(self.handle, byref(a), int(n), byref(part),
+                                         int(vocab_total), _stream_handle(stream)),
+                "ds_merge_shards")
+        return out
 
     def standin_hidden(self, W, s_prev, E, canvas, done, H_out, stream=None):
         B = canvas.shape[0]

@@ -247,6 +247,71 @@ ds_status ds_standin_hidden(ds_sampler* sampler, const void* W, const float* s_p
                             const void* E, const int32_t* canvas, const uint8_t* done,
                             void* H_out, int32_t batch, void* stream);
 
+/* ---- vocabulary shards ----------------------------------------------------------------
+ * The step over a vocabulary split into shards (contiguous token ranges, e.g. one per GPU):
+ * the softmax statistics, the entropy, s = softmax(y) . E and the Gumbel-max sample of the
+ * full vocabulary decompose over any partition of it ("DiffusionGemma Technical Report",
+ * section 6 "Sampling": softmax and self-conditioning matmul over the full vocabulary; the
+ * pages give no multi-GPU sampler, the decomposition is the plain identity). Each shard runs
+ * ds_sampler_step_shard on its rows of E and writes a partial record; the records of all
+ * shards, gathered on one device in token order, are combined by ds_merge_shards, which writes
+ * the step's outputs and the state update exactly as ds_sampler_step does. Draws use global
+ * token indices, so the merged sample is the full-vocabulary one.
+ *
+ * Partial record of one shard (caller-owned [device] buffers; R = B * L rows):
+ *   rows  [R] ds_shard_row   the shard's softmax statistics: maximum m_q of y, normaliser
+ *                            l_q = sum exp(y - m_q), entropy of the shard's renormalised
+ *                            softmax, and its argmax (global token, lowest on ties)
+ *   best  [R] ds_shard_best  top_k == 0: the shard's Gumbel-max race winner: score = -key
+ *                            (key = E_j / exp(y_j - m_q), the exponential-race form), token
+ *                            (global), lnp = y_token - m_q
+ *   O     [R, d] float       sum_j exp(y_j - m_q) E_j over the shard (not divided by l_q)
+ *   cand  [R, top_k]         top_k > 0: the shard's top_k candidates {y, global token}
+ *                            (unused slots: token INT32_MAX); NULL when top_k == 0
+ * For ds_merge_shards the four pointers address n_shards records stacked in token order
+ * (rows [n, R], best [n, R], O [n, R, d], cand [n, R, top_k]). */
+typedef struct ds_shard_row {
+  float m;
+  float l;
+  float entropy;
+  int32_t argmax;
+} ds_shard_row;
+typedef struct ds_shard_best {
+  float score;
+  int32_t token;
+  float lnp;
+  int32_t reserved;
+} ds_shard_best;
+typedef struct ds_shard_cand {
+  float y;
+  int32_t token;
+} ds_shard_cand;
+typedef struct ds_shard_partial {
+  ds_shard_row* rows;
+  ds_shard_best* best;
+  float* O;
+  ds_shard_cand* cand;
+} ds_shard_partial;
+
+/* Enqueue the partial record of one shard: the sampler's vocab is the shard's size (a multiple
+ * of 256), args->E its rows [vocab, d] (bf16, tensor-core path only: else DS_ERR_UNSUPPORTED),
+ * token_offset the global index of its first token (a multiple of 256) and vocab_total the
+ * full vocabulary (token_offset + vocab <= vocab_total <= 2^24; else DS_ERR_INVALID_ARG).
+ * Uses args->batch, seed, H, E, temperature, step and done; canvas, lock and the outputs are
+ * neither read nor written. Finished sequences' records are left untouched. */
+ds_status ds_sampler_step_shard(ds_sampler* sampler, const ds_step_args* args,
+                                int32_t token_offset, int64_t vocab_total,
+                                const ds_shard_partial* out, void* stream);
+
+/* Enqueue the merge of n_shards partial records (1 <= n_shards <= 64, else
+ * DS_ERR_INVALID_ARG; n_shards * top_k <= 8192, else DS_ERR_UNSUPPORTED) into the
+ * step's outputs (s, sampled, conf, entropy, argmax) and the lock / re-noise / stop update of
+ * args (all [device], as for ds_sampler_step), re-noising over vocab_total tokens. The sampler
+ * must have the shards' canvas_len, d_model, top_k, max_steps and lock rule (its vocab is not
+ * used). With top_k > 0 the sample is drawn from the top_k of the shards' pooled candidates. */
+ds_status ds_merge_shards(ds_sampler* sampler, const ds_step_args* args, int32_t n_shards,
+                          const ds_shard_partial* parts, int64_t vocab_total, void* stream);
+
 /* Synchronise the sampler's device and report (then clear) the device error word:
  * DS_OK, DS_ERR_TIMEOUT or DS_ERR_DEVICE. */
 ds_status ds_sampler_device_status(ds_sampler* sampler, ds_status* out);

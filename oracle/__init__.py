@@ -53,3 +53,4 @@ from .sampler import (  # noqa: F401
     denoise_loop,
     block_loop,
 )
+from .shards import merge_shards, shard_partial  # noqa: F401

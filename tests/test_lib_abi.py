@@ -67,6 +67,10 @@ int main(void) {
   printf("ds_sampler_config %zu\nds_step_args %zu\nds_loop_args %zu\nds_block_args %zu\n",
          sizeof(ds_sampler_config), sizeof(ds_step_args), sizeof(ds_loop_args),
          sizeof(ds_block_args));
+  printf("ds_shard_partial %zu\nds_shard_row %zu\nds_shard_best %zu\nds_shard_cand %zu\n",
+         sizeof(ds_shard_partial), sizeof(ds_shard_row), sizeof(ds_shard_best),
+         sizeof(ds_shard_cand));
+  P(ds_shard_partial, O) P(ds_shard_partial, cand)
   P(ds_sampler_config, vocab) P(ds_sampler_config, top_k) P(ds_sampler_config, lock_rule)
   P(ds_sampler_config, entropy_budget) P(ds_sampler_config, t_end)
   P(ds_step_args, seed) P(ds_step_args, H) P(ds_step_args, argmax) P(ds_step_args, prev_argmax)
@@ -92,6 +96,10 @@ def test_struct_layouts_match_c(tmp_path):
     assert int(got["ds_step_args"]) == ctypes.sizeof(C.ds_step_args)
     assert int(got["ds_loop_args"]) == ctypes.sizeof(C.ds_loop_args)
     assert int(got["ds_block_args"]) == ctypes.sizeof(C.ds_block_args)
+    assert int(got["ds_shard_partial"]) == ctypes.sizeof(C.ds_shard_partial)
+    assert int(got["ds_shard_row"]) == C.SHARD_ROW_BYTES
+    assert int(got["ds_shard_best"]) == C.SHARD_BEST_BYTES
+    assert int(got["ds_shard_cand"]) == C.SHARD_CAND_BYTES
     for key, val in got.items():
         if "." in key:
             t, f = key.split(".")
