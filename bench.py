@@ -179,6 +179,85 @@ class ClockSampler:
         return out
 
 
+class NvmlClockSampler:
+    """SM clock, power and clock-event reasons polled through the driver's NVML library
+    (libnvidia-ml, read-only queries) every millisecond on a thread, so that a timed region of a
+    few milliseconds still has samples of its own; the same summary as ClockSampler."""
+    # clock-event reason bits of nvmlDeviceGetCurrentClocksEventReasons
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, gpu_index: int, interval_ms: float = 1.0):
+        import ctypes
+        self.gpu, self.interval_ms = gpu_index, interval_ms
+        self.samples = []  # (host time, sm MHz, max MHz, power W, reasons bitmask)
+        self._stop = threading.Event()
+        self.ok = False
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(gpu_index), ctypes.byref(self.h)):
+                return
+            self.lib, self.ct = lib, ctypes
+            self.reason_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            mx = ctypes.c_uint()
+            lib.nvmlDeviceGetMaxClockInfo(self.h, ctypes.c_uint(1), ctypes.byref(mx))
+            self.max_mhz = float(mx.value)
+            self.ok = True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _poll(self):
+        ct, lib = self.ct, self.lib
+        clk, pw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        while not self._stop.is_set():
+            lib.nvmlDeviceGetClockInfo(self.h, ct.c_uint(1), ct.byref(clk))  # NVML_CLOCK_SM
+            lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(pw))
+            self.reason_fn(self.h, ct.byref(rs))
+            self.samples.append((time.time(), float(clk.value), self.max_mhz,
+                                 pw.value / 1000.0, int(rs.value)))
+            time.sleep(self.interval_ms / 1e3)
+
+    def start(self):
+        if not self.ok:
+            return
+        self.t = threading.Thread(target=self._poll, daemon=True)
+        self.t.start()
+        t0 = time.time()
+        while not self.samples and time.time() - t0 < 2.0:
+            time.sleep(0.001)
+
+    def stop(self, window=None):
+        if not self.ok:
+            return None
+        self._stop.set()
+        self.t.join(timeout=2)
+        sel = self.samples
+        if window is not None:
+            inside = [x for x in self.samples if window[0] <= x[0] <= window[1]]
+            sel = inside or self.samples
+        if not sel:
+            return None
+        reasons = sorted({n for x in sel for bit, n in self.REASONS.items() if x[4] & bit})
+        out = {"sm_mhz": statistics.median(x[1] for x in sel),
+               "sm_min_mhz": min(x[1] for x in sel), "sm_max_mhz": self.max_mhz,
+               "reasons": reasons, "samples": len(sel),
+               "power_w": statistics.median(x[3] for x in sel), "source": "nvml",
+               "interval_ms": self.interval_ms}
+        if window is not None:
+            out["in_region"] = bool([x for x in self.samples if window[0] <= x[0] <= window[1]])
+        return out
+
+
+def clock_sampler(gpu_index: int):
+    """NVML polling when the driver's library loads, else nvidia-smi sampling."""
+    s = NvmlClockSampler(gpu_index)
+    return s if s.ok else ClockSampler(gpu_index)
+
+
 # the files each tensor-core kernel is compiled from (its own file first)
 KERNEL_SOURCES = {
     k: [os.path.join(ROOT, "canvas_sampler_gb300", "csrc", f) for f in files]
@@ -346,8 +425,8 @@ def run_ours(args):
     assert sampler.device_status() == 0
     if world > 1:
         dist.barrier()
-    clocks = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
-                          int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    clocks = clock_sampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                           int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
     clocks.start()  # returns at its first sample: the timed region starts right after
     launches0 = sampler.launch_count
     # coarse phase events inside the timed region (ends of the logits, up-to-self-conditioning,
@@ -371,7 +450,7 @@ def run_ours(args):
     launches = sampler.launch_count - launches0
     # samples that arrived while the timed steps ran (the region's own clock record; a region
     # shorter than the sampling interval has none, and then every sample is summarised)
-    clk = clocks.stop(window=(t_region0, t_region1 + clocks.interval_ms / 1e3))
+    clk = clocks.stop(window=(t_region0, t_region1))
     # every phase, on a short untimed pass after the timed region (informational breakdown)
     sampler.set_phase_timing(True)
     for _ in range(min(args.steps, 20)):
@@ -453,7 +532,7 @@ def run_ours(args):
     sustained = None
     if args.sustained_seconds > 0:
         n_sus = max(1, int(args.sustained_seconds * 1e3 / max(ms / args.steps, 1e-3)))
-        sclk = ClockSampler(clocks.gpu)
+        sclk = clock_sampler(clocks.gpu)
         sclk.start()
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()

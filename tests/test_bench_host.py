@@ -32,3 +32,17 @@ def test_clock_summary_keeps_the_samples_inside_the_window():
 def test_thermal_reason_is_reported():
     out = bench.ClockSampler.summarise([(0.0, _line(1500, 1000, thermal=True))])
     assert out["reasons"] == ["sw_thermal_slowdown"]
+
+
+def test_nvml_summary_keeps_the_samples_inside_the_window():
+    s = bench.NvmlClockSampler.__new__(bench.NvmlClockSampler)
+    s.ok, s.interval_ms, s.max_mhz = True, 1.0, 2070.0
+    s._stop = bench.threading.Event()
+    s.t = bench.threading.Thread(target=lambda: None)
+    s.t.start()
+    s.samples = [(0.0, 2070.0, 2070.0, 180.0, 0), (1.001, 1900.0, 2070.0, 1300.0, 0x4),
+                 (1.002, 1800.0, 2070.0, 1350.0, 0x4 | 0x20), (2.0, 2070.0, 2070.0, 200.0, 0)]
+    out = s.stop(window=(1.0, 1.01))
+    assert out["samples"] == 2 and out["sm_mhz"] == 1850.0 and out["in_region"]
+    assert out["reasons"] == ["sw_power_cap", "sw_thermal_slowdown"]
+    assert out["source"] == "nvml"
