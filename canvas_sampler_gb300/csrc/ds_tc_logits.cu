@@ -28,6 +28,7 @@ using namespace tcpipe;
 // entropy: 2 k-blocks 2.4e-6 / 1.9e-6, 4: 3.6e-6 / 3.2e-6, 6: 3.6e-6 / 4.3e-6, 8: 5.5e-6 /
 // 7.2e-6, with the logits kernel at 0.393, 0.350, 0.335 and 0.327 ms.
 constexpr int LG_BM = 128, LG_BN = 256, LG_BK = 64, LG_STAGES = 4, LG_CHUNK_KB = 6;
+constexpr int LG_FIRST_KB = 6;
 constexpr int LG_COLS = LG_BN / 2;
 constexpr uint32_t LG_A_BYTES = LG_BM * LG_BK * 2;
 constexpr uint32_t LG_B_BYTES = LG_BN * LG_BK * 2;
@@ -70,7 +71,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
                 const __grid_constant__ CUtensorMap mapY, const __grid_constant__ CUtensorMap mapPlo,
                 int R, int64_t V, int d, int L, const float* __restrict__ T,
                 const uint8_t* __restrict__ done, ChunkStat* __restrict__ seg_stats,
-                float* __restrict__ mseg_t, uint16_t* __restrict__ Hout, uint32_t* err) {
+                float* __restrict__ mseg_t, uint16_t* __restrict__ Hout, uint32_t* err,
+                int first_kb) {
   constexpr bool STANDIN = MODE == kStandin;
   constexpr int STAGES = PAIR ? LG2_STAGES : LG_STAGES;
   constexpr uint32_t STAGE_BYTES = PAIR ? LG2_STAGE_BYTES : LG_STAGE_BYTES;
@@ -93,7 +95,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   const int n_ct = (int)(V / LG_BN);
   const int n_tiles = n_it * n_ct;
   const int nk = d / LG_BK;
-  const int n_ch = (nk + LG_CHUNK_KB - 1) / LG_CHUNK_KB;
+  // chunk 0 of a tile takes first_kb k-blocks, the others LG_CHUNK_KB: a longer first chunk
+  // lets the MMAs of a tile run further ahead while the epilogue writes the previous tile's
+  // output (one longer accumulation chain per tile)
+  const int fkb = min(max(first_kb, 1), nk);
+  const int n_ch = 1 + (nk - fkb + LG_CHUNK_KB - 1) / LG_CHUNK_KB;
   if (threadIdx.x == 0) {
     for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&xbar[i]), 2);
     // pair: one arrival per epilogue warp of both CTAs releases a TMEM buffer of the pair
@@ -181,7 +187,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           }
           tc_fence_after();
           const uint32_t dt = tmem + (uint32_t)(buf * LG_BN);
-          const int kc0 = ch * LG_CHUNK_KB, kc1 = min(nk, kc0 + LG_CHUNK_KB);
+          const int kc0 = ch == 0 ? 0 : fkb + (ch - 1) * LG_CHUNK_KB;
+          const int kc1 = ch == 0 ? fkb : min(nk, kc0 + LG_CHUNK_KB);
           for (int kc = kc0; kc < kc1; ++kc) {
             if (!mbar_wait(smem_u32(&ctl.full[stage]), phase, abort_flag, err)) {
               ok = false;
@@ -422,6 +429,17 @@ void tc_prepare_logits() {
   g_pairs_resident = n;
 }
 
+// k-blocks of the first TMEM chunk of each logits tile (LG_FIRST_KB, or DS_LOGITS_FIRST_KB in
+// the environment for measurements).
+int logits_first_kb() {
+  static const int v = [] {
+    const char* e = getenv("DS_LOGITS_FIRST_KB");
+    const int x = e ? atoi(e) : LG_FIRST_KB;
+    return x >= 1 ? x : LG_FIRST_KB;
+  }();
+  return v;
+}
+
 bool logits_pair_enabled(int R) {
   static const bool on = [] {
     const char* e = getenv("DS_LOGITS_PAIR");
@@ -459,12 +477,13 @@ cudaError_t launch_logits_mode(const CUtensorMap& mH, const CUtensorMap& mE1,
     const int pairs = std::max(1, std::min(n_items, g_pairs_resident));
     cfg.gridDim = dim3((unsigned)(2 * pairs));
     return cudaLaunchKernelEx(&cfg, k_logits_tc<MODE, true>, mH, mE2, mOut, mOut2, R, V, d, L, T,
-                              done, seg_stats, mseg_t, (uint16_t*)nullptr, err);
+                              done, seg_stats, mseg_t, (uint16_t*)nullptr, err, logits_first_kb());
   }
   const int n_tiles = (R / LG_BM) * n_ct;
   const int grid = std::max(1, std::min(n_tiles, tc_num_sms()));
   return launch_k(k_logits_tc<MODE, false>, dim3(grid), dim3(kThreadsTC), LG_SMEM, st, mH, mE1,
-                  mOut, mOut2, R, V, d, L, T, done, seg_stats, mseg_t, (uint16_t*)nullptr, err);
+                  mOut, mOut2, R, V, d, L, T, done, seg_stats, mseg_t, (uint16_t*)nullptr, err,
+                  logits_first_kb());
 }
 
 }  // namespace
@@ -512,7 +531,7 @@ cudaError_t launch_standin_tc(const uint16_t* U, const uint16_t* W, int R, int d
   const int grid = std::max(1, std::min(n_tiles, tc_num_sms()));
   k_logits_tc<kStandin, false><<<grid, kThreadsTC, LG_SMEM, st>>>(mU, mW, mU, mU, R, (int64_t)d, 2 * d,
                                                             L, nullptr, done, nullptr, nullptr,
-                                                            H_out, err);
+                                                            H_out, err, LG_CHUNK_KB);
   return cudaGetLastError();
 }
 
