@@ -42,7 +42,9 @@ def _run(cmd, verbose):
     return p.stdout + p.stderr
 
 
-def build(verbose: bool = False, ptxas_verbose: bool = False) -> str:
+def build(verbose: bool = False, ptxas_verbose: bool = False, extra_flags=None) -> str:
+    """Compile every translation unit and link the library; extra_flags (e.g. -D tuning
+    definitions) are passed to every nvcc compile."""
     os.makedirs(OUT_DIR, exist_ok=True)
     obj_dir = os.path.join(OUT_DIR, "obj")
     os.makedirs(obj_dir, exist_ok=True)
@@ -50,6 +52,7 @@ def build(verbose: bool = False, ptxas_verbose: bool = False) -> str:
              "-I", os.path.join(ROOT, "include"), "-I", CSRC] + ARCH
     if ptxas_verbose:
         flags += ["-Xptxas", "-v"]
+    flags += list(extra_flags or [])
 
     def compile_one(src):
         obj = os.path.join(obj_dir, src.replace(".cu", ".o"))

@@ -28,7 +28,16 @@ using namespace tcpipe;
 // entropy: 2 k-blocks 2.4e-6 / 1.9e-6, 4: 3.6e-6 / 3.2e-6, 6: 3.6e-6 / 4.3e-6, 8: 5.5e-6 /
 // 7.2e-6, with the logits kernel at 0.393, 0.350, 0.335 and 0.327 ms.
 constexpr int LG_BM = 128, LG_BN = 256, LG_BK = 64, LG_STAGES = 4, LG_CHUNK_KB = 6;
-constexpr int LG_FIRST_KB = 6;
+// The first chunk of each tile is longer: while the epilogue writes a tile's output the MMAs
+// of the next tile can only fill the two TMEM buffers, so a longer first chunk hides more of
+// that output phase behind MMAs. Same-box A/B at 2070 MHz (logits kernel per step, 6 stages):
+// first chunk 6 / 12 / 18 / 24 k-blocks at B = 1: 0.323 (5 stages) / 0.312 / 0.310 / 0.309 ms;
+// B = 4: 1.117 (5 stages) / 1.060 / 1.045 / 1.033 ms; B = 8: 2.21 (5 stages) / 2.11 / 2.05 / 2.00
+// ms. Largest relative errors against the oracle (s / entropy / confidence; V = 262144, d = 2816,
+// 98 positions, and V = 32768, d = 1024, all 256 positions): 12 k-blocks 5.8e-6 / 8.4e-6 /
+// 6.8e-6, 16: 1.0e-5 / 1.4e-5 / 1.6e-5 (at d = 1024 that is the whole K in one chain), 24: 1.1e-5
+// / 1.4e-5 / 1.6e-5: 12 keeps a 2.4x margin to the 2e-5 tolerance.
+constexpr int LG_FIRST_KB = 12;
 constexpr int LG_COLS = LG_BN / 2;
 constexpr uint32_t LG_A_BYTES = LG_BM * LG_BK * 2;
 constexpr uint32_t LG_B_BYTES = LG_BN * LG_BK * 2;
@@ -39,10 +48,16 @@ constexpr uint32_t LG_STAGE_BYTES = LG_A_BYTES + LG_B_BYTES;
 constexpr uint32_t LG_STG_BYTES = 32 * 32 * 4;
 // CTA pair: each CTA stages its 128 rows of H and 128 of the tile's 256 rows of E (32 KB a
 // stage), so an SM takes in 2/3 of the bytes per MAC of a one-CTA tile. Measured at the bench
-// size (logits kernel per step): 5 stages with one staging box per warp 0.323 ms, with two boxes
-// used in turn (a warp writes the next box while the store of the previous one still reads it)
-// 0.328 ms, 6 stages with one box 0.327 ms, 4 stages with two 0.344 ms.
-constexpr int LG2_STAGES = 5, LG2_STG_BOXES = 1;
+// size (logits kernel per step), first chunks of 6 k-blocks: 5 stages with one staging box per
+// warp 0.323 ms, with two boxes used in turn (a warp writes the next box while the store of the
+// previous one still reads it) 0.328 ms, 6 stages with one box 0.327 ms, 4 stages with two 0.344
+// ms; with first chunks of 12 k-blocks (same box, same day): 5 stages 0.320, 6 stages 0.312 ms
+// at B = 1, 1.066 / 1.060 ms at B = 4, 2.126 / 2.112 ms at B = 8. 6 stages and one box per warp
+// use 225 KB of the 227 KB of shared memory a CTA may have.
+#ifndef DS_LG2_STAGES
+#define DS_LG2_STAGES 6
+#endif
+constexpr int LG2_STAGES = DS_LG2_STAGES, LG2_STG_BOXES = 1;
 constexpr uint32_t LG2_STAGE_BYTES = LG_A_BYTES + LG_B_BYTES / 2;
 static_assert(LG2_STAGES <= tcpipe::kMaxStages && LG_STAGES <= tcpipe::kMaxStages, "stages");
 constexpr size_t LG_SMEM =
