@@ -291,10 +291,16 @@ def measured_traffic(kernel: str):
     return float(m_b.group(1)) if kernel_source_hash(kernel) == m_h.group(1) else None
 
 
-def region_peak_key(region_s: float, peaks: dict) -> str:
+def region_peak_key(region_s: float, peaks: dict, clocks: dict | None = None) -> str:
     """The bf16 peak a timed region is held to: the burst figure for a region shorter than a
-    second (the power controller has not yet lowered the clocks), else the sustained one."""
-    key = "bf16_tflops" if region_s < 1.0 else "bf16_tflops_sustained"
+    second that ran at full clocks (its own clock samples, where there are any, at >= 97% of the
+    maximum SM clock with no power cap), else the sustained one (the power controller has
+    lowered the clocks, as it does within a fraction of a second of back-to-back steps)."""
+    burst = region_s < 1.0
+    if burst and clocks and clocks.get("sm_mhz") and clocks.get("sm_max_mhz"):
+        burst = (clocks["sm_mhz"] >= 0.97 * clocks["sm_max_mhz"] and
+                 "sw_power_cap" not in clocks.get("reasons", []))
+    key = "bf16_tflops" if burst else "bf16_tflops_sustained"
     return key if key in peaks else "bf16_tflops"
 
 
@@ -501,7 +507,7 @@ def run_ours(args):
     # yet lowered them): its kernels are measured against the burst bf16 peak; only a region
     # of a second or more, or the sustained pass below, is held to the sustained peak
     region_s = ms / 1e3
-    peak_key = region_peak_key(region_s, peaks)
+    peak_key = region_peak_key(region_s, peaks, clk)
     peak_tf = float(peaks.get(peak_key, FALLBACK_PEAKS[peak_key]))
     roof = None
     if dom_flops and dom_ms > 0:

@@ -14,6 +14,11 @@ def test_short_region_uses_burst_peak_long_region_sustained():
     assert bench.region_peak_key(0.35, peaks) == "bf16_tflops"
     assert bench.region_peak_key(3.0, peaks) == "bf16_tflops_sustained"
     assert bench.region_peak_key(3.0, {"bf16_tflops": 1.0}) == "bf16_tflops"
+    # a short region that the power controller already throttled is held to the sustained peak
+    capped = {"sm_mhz": 1642.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    full = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    assert bench.region_peak_key(0.36, peaks, capped) == "bf16_tflops_sustained"
+    assert bench.region_peak_key(0.017, peaks, full) == "bf16_tflops"
 
 
 def test_clock_summary_keeps_the_samples_inside_the_window():
