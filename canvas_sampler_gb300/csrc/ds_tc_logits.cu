@@ -57,7 +57,10 @@ constexpr uint32_t LG_STG_BYTES = 32 * 32 * 4;
 #ifndef DS_LG2_STAGES
 #define DS_LG2_STAGES 6
 #endif
-constexpr int LG2_STAGES = DS_LG2_STAGES, LG2_STG_BOXES = 1;
+#ifndef DS_LG2_STG_BOXES
+#define DS_LG2_STG_BOXES 1
+#endif
+constexpr int LG2_STAGES = DS_LG2_STAGES, LG2_STG_BOXES = DS_LG2_STG_BOXES;
 constexpr uint32_t LG2_STAGE_BYTES = LG_A_BYTES + LG_B_BYTES / 2;
 static_assert(LG2_STAGES <= tcpipe::kMaxStages && LG_STAGES <= tcpipe::kMaxStages, "stages");
 constexpr size_t LG_SMEM =

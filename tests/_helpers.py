@@ -83,14 +83,21 @@ def out_np(out: StepOutputs) -> dict:
 
 
 def compare_outputs(gpu: dict, ref: dict, active_rows, *, top_k=0):
-    """Per-position checks of s, conf, entropy, argmax, sampled. Returns counts."""
+    """Per-position checks of s, conf, entropy, argmax, sampled. Returns counts and, for the
+    record, the largest elementwise relative error of s over the components that are not
+    negligible (|s_k| >= 1% of the row's largest |s_k|; the asserted tolerance is the row-norm
+    one)."""
     n_excl = 0
     n = 0
+    s_elem = 0.0
     for b, i in active_rows:
         n += 1
         s_g, s_r = gpu["s"][b, i].astype(np.float64), ref["s"][b, i]
         err = np.linalg.norm(s_g - s_r) / max(np.linalg.norm(s_r), 1e-300)
         assert err <= REL_TOL, f"s mismatch at {(b, i)}: rel err {err:.3g}"
+        big = np.abs(s_r) >= 0.01 * np.abs(s_r).max()
+        if big.any():
+            s_elem = max(s_elem, float(np.max(np.abs(s_g[big] - s_r[big]) / np.abs(s_r[big]))))
         H_r = ref["entropy"][b, i]
         assert abs(gpu["entropy"][b, i] - H_r) <= REL_TOL * max(1.0, abs(H_r)), (
             f"entropy at {(b, i)}: {gpu['entropy'][b, i]} vs {H_r}")
@@ -106,7 +113,7 @@ def compare_outputs(gpu: dict, ref: dict, active_rows, *, top_k=0):
         c_r = ref["conf"][b, i]
         assert abs(gpu["conf"][b, i] - c_r) <= REL_TOL * c_r + 1e-30, (
             f"conf at {(b, i)}: {gpu['conf'][b, i]} vs {c_r}")
-    return {"checked": n, "excluded": n_excl}
+    return {"checked": n, "excluded": n_excl, "s_elem_max": s_elem}
 
 
 def check_lock_update(pre: dict, gpu_out: dict, gpu_post: dict, ref: dict | None, tau, seed, V,

@@ -56,6 +56,7 @@ def test_full_size_step(name, per_seq, impl):
     # oracle per sampled position, one sequence at a time (the others marked done)
     H64 = exact_f64(case.inp["H"], w.dtype)
     checked = 0
+    s_elem = 0.0
     for b in range(w.B):
         pos = np.array([i for bb, i in rows if bb == b])
         only_b = np.ones(w.B, np.uint8)
@@ -64,7 +65,11 @@ def test_full_size_step(name, per_seq, impl):
                                   case.inp["tau"].astype(np.float64), pre["canvas"], pre["lock"],
                                   pre["step"], only_b, case.inp["seed"], top_k=w.top_k,
                                   max_steps=w.max_steps, positions=pos)
-        checked += compare_outputs(g, ref, [(b, int(i)) for i in pos], top_k=w.top_k)["checked"]
+        rep = compare_outputs(g, ref, [(b, int(i)) for i in pos], top_k=w.top_k)
+        checked += rep["checked"]
+        s_elem = max(s_elem, rep["s_elem_max"])
+    print(f"{name} ({impl}): {checked} positions against the oracle; largest elementwise "
+          f"relative error of s on components >= 1% of the row's largest: {s_elem:.2e}")
     assert checked == len(rows)
 
 
