@@ -128,12 +128,17 @@ int esize(int dtype) { return dtype == DS_DTYPE_FP32 ? 4 : 2; }
 
 // Whether a step's Gumbel race runs on warps of the self-conditioning launch. Measured on GB300
 // (step time, race inside / own launch), d = 2816: B = 1, V = 262144: 0.886 / 0.892 ms and on
-// another box 0.904 / 0.913; V = 65536 and 131072: 0.276 / 0.293 and 0.469 / 0.481 ms; B = 2 and
-// 8 at V = 262144: 1.686 / 1.660 and 6.81 / 6.62 ms. B = 1, V = 32768, d = 1024: 0.154 / 0.116 ms
-// (a short GEMM leaves the race to a few warps). So inside for one canvas of rows, d >= 2048.
+// another box 0.904 / 0.913; V = 65536 and 131072: 0.276 / 0.293 and 0.469 / 0.481 ms. B = 1,
+// V = 32768, d = 1024: 0.154 / 0.116 ms (a short GEMM leaves the race to a few warps). At
+// V = 262144 and larger batches the answer depends on the clocks: in short runs at 2070 MHz
+// (same box, two repeats) B = 2: 1.51 / 1.556 ms, B = 4: 2.905 / 2.979, B = 8: 5.884 / 6.000,
+// B = 16: 12.02-12.51 / 12.02-12.33; in runs of 2-3 s under the power cap B = 2: 1.661 / 1.668-
+// 1.675, B = 4: 3.304-3.308 / 3.261-3.268, B = 8: 6.669-6.725 / 6.637-6.657, B = 16: 13.51 /
+// 13.43-13.46 (the race inside draws more power, and the cap lowers the clock further). So
+// inside for up to two canvases of rows (faster in both regimes), with d >= 2048.
 bool race_in_selfcond(const ds_sampler* s, int R, int d) {
   if (s->gumbel_in_sc >= 0) return s->gumbel_in_sc == 1;
-  return R <= 256 && d >= 2048;
+  return R <= 512 && d >= 2048;
 }
 
 int splits_for(const ds_sampler* s, int batch) {

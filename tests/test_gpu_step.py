@@ -54,9 +54,10 @@ CASES = [
     ("batched_b3_v16384_d256", BASE_BATCH, 3, 16384, 256, 256),
     ("canvas128_b3_v8192_d512", BASE_BATCH, 3, 8192, 512, 128),
     ("canvas128_b2_v8960_d256", BASE_BATCH, 2, 8960, 256, 128),
-    # B * L = 256 and d >= 2048: the row merge and the race run inside the self-conditioning
+    # B * L <= 512 and d >= 2048: the row merge and the race run inside the self-conditioning
     # launch by default
     ("canvas128_b2_v8192_d2048", BASE_BATCH, 2, 8192, 2048, 128),
+    ("batched_b2_v8192_d2048", BASE_BATCH, 2, 8192, 2048, 256),
 ]
 
 
