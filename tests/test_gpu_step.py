@@ -412,3 +412,26 @@ def test_topk_uniform_logits_take_the_lowest_tokens(V, d):
     pos = np.arange(0, w.L, 8)
     ref = oracle_step(case, pre, positions=pos)
     assert np.array_equal(g["sampled"][0, pos], ref["sampled"][0, pos])
+
+
+@pytest.mark.parametrize("L", [512, 1024])
+def test_long_canvases_lock_update(L):
+    # canvases longer than the finalize CTA (256 threads): the lock update folded into the
+    # finalize launch takes several positions a thread; the whole step against the oracle, a
+    # forced lock (uniform logits) at the lowest position and the commit at the last step
+    w = W.scaled(BASE_BATCH, V=4096, d=256, B=2, L=L)
+    case = GpuCase(w, impl="tensor")
+    _, post, rep = full_step_check(case, case.state())
+    assert rep["excluded"] <= max(2, rep["checked"] // 100)
+    assert post["step"].tolist() == [1, 1]
+    inp = W.make_inputs(w)
+    inp["H"] = np.zeros_like(inp["H"])
+    case_u = GpuCase(w, inputs=inp, impl="tensor")
+    _, post_u, _ = full_step_check(case_u, case_u.state())
+    assert post_u["lock"].sum(axis=1).tolist() == [1, 1] and np.all(post_u["lock"][:, 0] == 1)
+    inp2 = dict(inp)
+    inp2["step"] = np.full(2, w.max_steps - 1, np.int32)
+    case_f = GpuCase(w, inputs=inp2, impl="tensor")
+    g_f, post_f, _ = full_step_check(case_f, case_f.state())
+    assert post_f["lock"].all() and post_f["done"].all()
+    assert np.array_equal(post_f["canvas"], g_f["sampled"])
