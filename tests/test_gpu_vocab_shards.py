@@ -176,3 +176,41 @@ def test_two_processes_exchange_records_over_gloo():
     assert rep["excluded"] <= 4
     check_lock_update(pre, res[0][0], res[0][1], ref, case.inp["tau"], case.inp["seed"], w.V,
                       w.max_steps)
+
+
+def test_shards_with_the_entropy_budget_rule_and_schedule():
+    # the pages' own sampler (entropy-budget acceptance, stop rule, temperature schedule) over
+    # two shards: the same step as the unsharded sampler, state included, over three steps
+    w = W.scaled(W.WORKLOADS["loop8_bf16_b1_v32768_d1024"], V=8192, d=256, B=2)
+    inp = W.make_inputs(w)
+    kw = dict(canvas_len=w.L, max_batch=w.B, dtype="bf16", max_steps=12, impl="tensor",
+              lock_rule="entropy_budget", entropy_budget=0.1, stop_entropy=0.005,
+              t_schedule=(0.8, 0.4))
+    full = Sampler(w.V, w.d, **kw)
+    shards = [Sampler(b - a, w.d, **kw) for a, b in (shard_range(w.V, 2, q) for q in range(2))]
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
+    E, H = dev(inp["E"]), dev(inp["H"])
+    T, tau = torch.from_numpy(inp["T"]).cuda(), torch.from_numpy(inp["tau"]).cuda()
+    st_full = CanvasState.from_numpy(inp["canvas"], inp["lock"], inp["step"], inp["done"])
+    st_sh = st_full.clone()
+    for t in range(3):
+        o_full = full.step(H, E, T, tau, st_full, inp["seed"])
+        parts = []
+        for q, sq in enumerate(shards):
+            a, b = shard_range(w.V, 2, q)
+            parts.append(sq.step_shard(H, E[a:b], T, tau, st_sh, inp["seed"], a, w.V))
+        o_sh = shards[0].merge_shards(ShardPartial.stack(parts), T, tau, st_sh, inp["seed"], w.V)
+        torch.cuda.synchronize()
+        gf, gs = out_np(o_full), out_np(o_sh)
+        rel = np.linalg.norm(gs["s"] - gf["s"], axis=-1) / np.linalg.norm(gf["s"], axis=-1)
+        assert rel.max() <= REL_TOL
+        assert np.all(np.abs(gs["entropy"] - gf["entropy"]) <= REL_TOL * np.maximum(1.0, gf["entropy"]))
+        assert np.array_equal(gs["argmax"], gf["argmax"])
+        same = (gs["sampled"] == gf["sampled"]).mean()
+        assert same >= 0.99, same
+        if np.array_equal(gs["sampled"], gf["sampled"]):
+            for k in ("canvas", "lock", "step", "done", "prev_argmax"):
+                assert torch.equal(getattr(st_sh, k), getattr(st_full, k)), (t, k)
+        else:  # a near-tie sampled differently: continue both from the same state
+            for k in ("canvas", "lock", "step", "done", "prev_argmax"):
+                getattr(st_sh, k).copy_(getattr(st_full, k))
