@@ -145,7 +145,17 @@ int splits_for(const ds_sampler* s, int batch) {
   const int R = batch * s->cfg.canvas_len;
   const int64_t V = s->cfg.vocab;
   const int d = s->cfg.d_model;
-  if (s->impl != DS_IMPL_SIMT) return selfcond_tc_splits(R, V, d, s->num_sms);
+  if (s->impl != DS_IMPL_SIMT) {
+    // DS_SELFCOND_SPLITS=n (read once) overrides the choice, for measurements; the workspace is
+    // sized with the same function, so the override holds for a sampler's whole life
+    static const int forced = [] {
+      const char* e = getenv("DS_SELFCOND_SPLITS");
+      return e ? atoi(e) : 0;
+    }();
+    if (forced >= 1)
+      return (int)std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(forced, 64), V / 256));
+    return selfcond_tc_splits(R, V, d, s->num_sms);
+  }
   // CUDA-core GEMM: aim at about four waves of 128 x 64 tiles, >= 1024 tokens per split
   const long tiles = (long)(d / 64) * (R / 128);
   long S = (4L * s->num_sms + tiles - 1) / tiles;
