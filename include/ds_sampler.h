@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define DS_SAMPLER_ABI_VERSION 3
+#define DS_SAMPLER_ABI_VERSION 4
 
 typedef enum ds_status {
   DS_OK = 0,

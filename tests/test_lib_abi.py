@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol():
 def test_version_and_status_strings_without_gpu():
     C = _lib()
     lib = C.load_library()
-    assert lib.ds_abi_version() == 3
+    assert lib.ds_abi_version() == 4
     for code in range(7):
         assert lib.ds_status_string(code)
     assert lib.ds_status_string(99) == b"unknown status"
