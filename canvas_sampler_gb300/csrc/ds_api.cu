@@ -22,10 +22,21 @@
 #include <new>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/ds_sampler.h"
 #include "ds_internal.h"
 
 using namespace ds;
+
+namespace {
+// A named range on the host timeline for each entry point that enqueues work (NVTX: shown by
+// profilers that record it, a no-op otherwise).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+}  // namespace
 
 namespace {
 
@@ -528,6 +539,7 @@ ds_status ds_sampler_impl(const ds_sampler* s, int32_t* impl) {
 }
 
 ds_status ds_sampler_step(ds_sampler* s, const ds_step_args* a, void* stream) {
+  NvtxRange nvtx_range("ds_sampler_step");
   if (!s) return DS_ERR_INVALID_ARG;
   ds_status r = check_step_args(s, a);
   if (r != DS_OK) return r;
@@ -535,6 +547,7 @@ ds_status ds_sampler_step(ds_sampler* s, const ds_step_args* a, void* stream) {
 }
 
 ds_status ds_sampler_step_host(ds_sampler* s, const ds_step_args* h, void* stream) {
+  NvtxRange nvtx_range("ds_sampler_step_host");
   if (!s) return DS_ERR_INVALID_ARG;
   if (!h || h->batch < 1 || h->batch > s->cfg.max_batch || !h->E) return DS_ERR_INVALID_ARG;
   if (!h->H || !h->temperature || !h->tau || !h->step || !h->canvas || !h->lock || !h->done ||
@@ -665,6 +678,7 @@ static_assert(sizeof(ds_shard_row) == sizeof(RowStat) && sizeof(ds_shard_best) =
 
 ds_status ds_sampler_step_shard(ds_sampler* s, const ds_step_args* a, int32_t token_offset,
                                int64_t vocab_total, const ds_shard_partial* out, void* stream) {
+  NvtxRange nvtx_range("ds_sampler_step_shard");
   if (!s || !a || !out) return DS_ERR_INVALID_ARG;
   if (a->batch < 1 || a->batch > s->cfg.max_batch) return DS_ERR_INVALID_ARG;
   if (!a->H || !a->E || !a->temperature || !a->step || !a->done || !out->rows || !out->best ||
@@ -718,6 +732,7 @@ ds_status ds_sampler_step_shard(ds_sampler* s, const ds_step_args* a, int32_t to
 
 ds_status ds_merge_shards(ds_sampler* s, const ds_step_args* a, int32_t n_shards,
                           const ds_shard_partial* parts, int64_t vocab_total, void* stream) {
+  NvtxRange nvtx_range("ds_merge_shards");
   if (!s || !parts) return DS_ERR_INVALID_ARG;
   ds_status r = check_step_args(s, a);
   if (r != DS_OK) return r;
@@ -758,6 +773,7 @@ ds_status ds_standin_hidden(ds_sampler* s, const void* W, const float* s_prev, c
 }
 
 ds_status ds_denoise_loop(ds_sampler* s, const ds_loop_args* a, void* stream) {
+  NvtxRange nvtx_range("ds_denoise_loop");
   if (!s || !a) return DS_ERR_INVALID_ARG;
   if (a->max_iters < 1 || a->max_iters > s->cfg.max_steps) return DS_ERR_INVALID_ARG;
   if (a->h_mode != DS_H_FIXED && a->h_mode != DS_H_STANDIN) return DS_ERR_INVALID_ARG;
@@ -842,6 +858,7 @@ ds_status ds_denoise_loop(ds_sampler* s, const ds_loop_args* a, void* stream) {
 }
 
 ds_status ds_block_loop(ds_sampler* s, const ds_block_args* a, void* stream) {
+  NvtxRange nvtx_range("ds_block_loop");
   if (!s || !a) return DS_ERR_INVALID_ARG;
   const ds_loop_args& lp = a->loop;
   if (a->n_blocks < 1 || a->first_block < 0 || (int64_t)a->first_block + a->n_blocks > 65536)
