@@ -617,6 +617,18 @@ ds_status ds_sampler_step_host(ds_sampler* s, const ds_step_args* h, void* strea
   a.E = h->E;
   a.H = dev;
   a.s = reinterpret_cast<float*>(dev + nH);
+  // s in page-locked host memory that the device can address (cudaHostAlloc'd or registered as
+  // mapped): the finalize kernel writes it there directly, instead of a copy after the step
+  bool s_direct = false;
+  {
+    cudaPointerAttributes pa{};
+    if (cudaPointerGetAttributes(&pa, h->s) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+        pa.devicePointer != nullptr && (reinterpret_cast<uintptr_t>(pa.devicePointer) & 15) == 0) {
+      a.s = static_cast<float*>(pa.devicePointer);
+      s_direct = true;
+    }
+    cudaGetLastError();  // a pointer the runtime does not know is not an error here
+  }
   a.temperature = reinterpret_cast<const float*>(blk_d + oT);
   a.tau = reinterpret_cast<const float*>(blk_d + otau);
   a.step = reinterpret_cast<int32_t*>(blk_d + ostep);
@@ -640,7 +652,7 @@ ds_status ds_sampler_step_host(ds_sampler* s, const ds_step_args* h, void* strea
   // left as the caller had them: s comes back for each run of consecutive live sequences (one
   // copy when all are live), the small outputs row by row from the staging mirror.
   const uint8_t* done_in = blk_h + odone;  // the flags as they were before the step
-  for (size_t b0 = 0; b0 < B && e == cudaSuccess;) {
+  for (size_t b0 = 0; b0 < B && e == cudaSuccess && !s_direct;) {
     if (done_in[b0]) {
       ++b0;
       continue;

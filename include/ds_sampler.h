@@ -231,7 +231,9 @@ ds_status ds_sampler_step(ds_sampler* sampler, const ds_step_args* args, void* s
  * ds_sampler_step, the outputs (s, sampled, conf, entropy, argmax) of sequences with done == 1
  * on entry are left as the caller had them. Uses a device staging area and a page-locked host
  * staging block of the sampler (allocated on the first call), so calls on one sampler must not
- * overlap. */
+ * overlap. When s is page-locked host memory the device can address (cudaHostAlloc, or
+ * cudaHostRegister with the mapped flag), the step writes s into it directly instead of copying
+ * it back after the step. */
 ds_status ds_sampler_step_host(ds_sampler* sampler, const ds_step_args* host_args, void* stream);
 
 /* Enqueue a denoising loop on `stream` (see ds_loop_args). */

@@ -22,9 +22,12 @@ def _pinned(a, dtype=None):
     return t.pin_memory()
 
 
+@pytest.mark.parametrize("s_pinned", [True, False], ids=["s_pinned", "s_pageable"])
 @pytest.mark.parametrize("rule", ["threshold", "entropy_budget"])
 @pytest.mark.parametrize("batch,done", [(3, (0, 1, 0)), (4, (0, 0, 0, 0)), (1, (0,))])
-def test_host_entry_matches_device(rule, batch, done):
+def test_host_entry_matches_device(rule, batch, done, s_pinned):
+    # s in page-locked memory is written by the step directly; in pageable memory it comes back
+    # by a copy after the step: both must give the device step's results
     w = replace(W.scaled(BASE, V=8192, d=256, B=batch), max_steps=12)
     inp = W.make_inputs(w)
     inp["done"] = np.array(done, np.uint8)
@@ -56,6 +59,9 @@ def test_host_entry_matches_device(rule, batch, done):
     host_state = CanvasState(_pinned(inp["canvas"]), _pinned(lock), _pinned(step),
                              _pinned(inp["done"]), _pinned(prev))
     host_out = StepOutputs.empty(batch, w.L, w.d, pin=True)
+    if not s_pinned:
+        host_out.s = torch.zeros(batch, w.L, w.d, dtype=torch.float32)
+        assert not host_out.s.is_pinned()
     for t in (host_out.s, host_out.conf, host_out.entropy):
         t.fill_(-7.0)
     host_out.sampled.fill_(-7)
