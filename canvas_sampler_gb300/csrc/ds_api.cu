@@ -745,9 +745,13 @@ ds_status ds_sampler_step_shard(ds_sampler* s, const ds_step_args* a, int32_t to
 ds_status ds_merge_shards(ds_sampler* s, const ds_step_args* a, int32_t n_shards,
                           const ds_shard_partial* parts, int64_t vocab_total, void* stream) {
   NvtxRange nvtx_range("ds_merge_shards");
-  if (!s || !parts) return DS_ERR_INVALID_ARG;
-  ds_status r = check_step_args(s, a);
-  if (r != DS_OK) return r;
+  if (!s || !parts || !a) return DS_ERR_INVALID_ARG;
+  // the merge reads no H, E or temperature: only the state, tau and the outputs are checked
+  if (a->batch < 1 || a->batch > s->cfg.max_batch) return DS_ERR_INVALID_ARG;
+  if (!a->tau || !a->step || !a->canvas || !a->lock || !a->done || !a->s || !a->sampled ||
+      !a->conf || !a->entropy || !a->argmax || !aligned(a->s, 16))
+    return DS_ERR_INVALID_ARG;
+  if (s->cfg.lock_rule == DS_LOCK_ENTROPY_BUDGET && !a->prev_argmax) return DS_ERR_INVALID_ARG;
   const int k = s->cfg.top_k;
   if (n_shards < 1 || n_shards > kMaxShards || !parts->rows || !parts->best || !parts->O ||
       (k > 0 && !parts->cand) || !aligned(parts->O, 16))

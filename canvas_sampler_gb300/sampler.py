@@ -275,9 +275,7 @@ class Sampler:
         B = state.canvas.shape[0]
         out = StepOutputs.empty(B, self.L, self.d) if out is None else out
         n = parts.rows.shape[0]
-        # H and E are not read by the merge; any valid device pointers satisfy the argument checks
-        ref = parts.O
-        a = self._step_args(ref, ref, temperature, tau, state, out, seed)
+        a = self._step_args(None, None, temperature, tau, state, out, seed)  # merge reads no H, E
         part = parts.c_struct()
         C.check(self.lib.ds_merge_shards(self.handle, byref(a), int(n), byref(part),
                                          int(vocab_total), _stream_handle(stream)),

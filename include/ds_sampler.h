@@ -308,7 +308,8 @@ ds_status ds_sampler_step_shard(ds_sampler* sampler, const ds_step_args* args,
 /* Enqueue the merge of n_shards partial records (1 <= n_shards <= 64, else
  * DS_ERR_INVALID_ARG; n_shards * top_k <= 8192, else DS_ERR_UNSUPPORTED) into the
  * step's outputs (s, sampled, conf, entropy, argmax) and the lock / re-noise / stop update of
- * args (all [device], as for ds_sampler_step), re-noising over vocab_total tokens. The sampler
+ * args (all [device], as for ds_sampler_step; H, E and temperature are not read and may be
+ * NULL), re-noising over vocab_total tokens. The sampler
  * must have the shards' canvas_len, d_model, top_k, max_steps and lock rule (its vocab is not
  * used). With top_k > 0 the sample is drawn from the top_k of the shards' pooled candidates. */
 ds_status ds_merge_shards(ds_sampler* sampler, const ds_step_args* args, int32_t n_shards,
