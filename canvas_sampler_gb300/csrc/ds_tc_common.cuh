@@ -71,6 +71,14 @@ DS_DEV void ctl_init(Ctl& c, int stages, uint32_t tempty_count = 32 * kEpiWarps)
   fence_mbar_init();
 }
 
+// True when every sequence with a row in [r0, r0 + n) is finished.
+DS_DEV bool rows_done(const uint8_t* done, int r0, int n, int L) {
+  if (!done) return false;
+  for (int b = r0 / L; b <= (r0 + n - 1) / L; ++b)
+    if (!done[b]) return false;
+  return true;
+}
+
 // After an abort: wait for the copies issued but not consumed by the MMA thread.
 DS_DEV void producer_drain(Ctl& c, int issued, int stages) {
   const int consumed = *(volatile int*)&c.consumed;

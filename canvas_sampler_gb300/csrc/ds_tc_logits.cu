@@ -72,14 +72,6 @@ constexpr size_t LG2_SMEM = (size_t)LG2_STAGES * LG2_STAGE_BYTES +
 // epilogue H = bf16(tanh(acc)) instead of y and the statistics (V plays N = d, d plays K = 2d).
 enum { kOutY = 0, kOutP = 1, kStandin = 2 };
 
-// True when every sequence with a row in [r0, r0 + n) is finished.
-DS_DEV bool rows_done(const uint8_t* done, int r0, int n, int L) {
-  if (!done) return false;
-  for (int b = r0 / L; b <= (r0 + n - 1) / L; ++b)
-    if (!done[b]) return false;
-  return true;
-}
-
 // PAIR: launched in clusters of two CTAs; a work item is a 256-row x 256-token tile computed by
 // M = 256 MMAs that the even CTA issues for both, each CTA holding the accumulator of its own
 // 128 rows (its epilogue is the one-CTA epilogue of that 128 x 256 tile). Needs R % 256 == 0.
