@@ -139,24 +139,26 @@ DS_DEV void gumbel_race16(const uint4& hia, const uint4& loa, float sa, const ui
                           const uint4& lob, float sb, int64_t j, uint32_t i, uint32_t b,
                           uint32_t step, uint64_t seed, float cut, float& kbest, int32_t& bj,
                           float& bp) {
-  float pu[16];
-  {
-    const float sau = sa * kHiBound, sbu = sb * kHiBound;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      pu[e] = bf16_at(hia, e) * sau;
-      pu[8 + e] = bf16_at(hib, e) * sbu;
-    }
-  }
-  bool need[4];
+  // the upper bound of p of each group of four from its largest hi half: hi is a non-negative
+  // bf16 (the sign bit clear), so the integer order of the 16-bit patterns is the value order,
+  // and fp32 multiplication by the positive scale is monotone, so this is exactly the largest
+  // of the four tokens' bounds hi sc (1 + 2^-7)
+  const float sau = sa * kHiBound, sbu = sb * kHiBound;
+  auto group_bound = [](uint32_t w0, uint32_t w1, float scale) {
+    const uint32_t m2 = __vmaxu2(w0, w1);
+    return __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16) * scale;
+  };
   float pmq[4];
+  pmq[0] = group_bound(hia.x, hia.y, sau);
+  pmq[1] = group_bound(hia.z, hia.w, sau);
+  pmq[2] = group_bound(hib.x, hib.y, sbu);
+  pmq[3] = group_bound(hib.z, hib.w, sbu);
+  bool need[4];
   bool any = false;
   const float kc0 = fminf(kbest, cut);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const float pm = fmaxf(fmaxf(pu[4 * q], pu[4 * q + 1]), fmaxf(pu[4 * q + 2], pu[4 * q + 3]));
-    pmq[q] = pm;
-    need[q] = !(SKIP4 && q == 0) && !(5.9604645e-8f >= kc0 * pm);
+    need[q] = !(SKIP4 && q == 0) && !(5.9604645e-8f >= kc0 * pmq[q]);
     any |= need[q];
   }
   if (!any) return;
@@ -183,7 +185,8 @@ DS_DEV void gumbel_race16(const uint4& hia, const uint4& loa, float sa, const ui
       const int t = 4 * q + e;
       const uint32_t r = word_of(w[q], e);
       const float f = __uint_as_float(0x3F800000u | (r >> 9));
-      if ((2.0f - f) - 5.9604644775390625e-8f > kcs * pu[t]) continue;
+      const float pu = t < 8 ? bf16_at(hia, t) * sau : bf16_at(hib, t - 8) * sbu;
+      if ((2.0f - f) - 5.9604644775390625e-8f > kcs * pu) continue;
       const float pe = t < 8 ? (bf16_at(hia, t) + bf16_at(loa, t)) * sa
                              : (bf16_at(hib, t - 8) + bf16_at(lob, t - 8)) * sb;
       if (!(pe > 0.f)) continue;
