@@ -654,16 +654,22 @@ def run_loop(args):
             one_loop(use_graph)
         torch.cuda.synchronize()
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        clocks = clock_sampler(0 if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                               int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[0]))
+        clocks.start()
+        t0 = time.time()
         ev0.record()
         for _ in range(args.steps):
             one_loop(use_graph)
         ev1.record()
         torch.cuda.synchronize()
+        t1 = time.time()
+        clk = clocks.stop(window=(t0, t1))
         ms = ev0.elapsed_time(ev1) / args.steps
         iters = int(state.step.max().item())  # the loop runs until its last sequence is done
         res["graph" if use_graph else "plain"] = {
             "ms_per_loop": ms, "iterations": iters, "ms_per_iteration": ms / max(1, iters),
-            "steps_per_s": iters / (ms / 1e3)}
+            "steps_per_s": iters / (ms / 1e3), "timed_region_s": t1 - t0, "clocks": clk}
     assert sampler.device_status() == 0
     line = {"mode": "loop", "workload": w.name, "B": B, "L": L, "V": w.V, "d": w.d,
             "top_k": w.top_k, "h_mode": w.h_mode, "max_steps": w.max_steps,
