@@ -6,6 +6,7 @@ import os
 import subprocess
 import sys
 
+import numpy as np
 import pytest
 
 pytestmark = pytest.mark.gpu
@@ -26,3 +27,31 @@ def test_step_parity_with_one_cta_kernels(env):
     tail = (r.stdout + r.stderr)[-3000:]
     assert r.returncode == 0, tail
     assert " passed" in r.stdout and " failed" not in r.stdout, tail
+
+
+_CHILD = r"""
+import sys
+import numpy as np
+import torch
+sys.path.insert(0, "tests")
+from _helpers import GpuCase, out_np
+from canvas_sampler_gb300 import workloads as W
+w = W.scaled(W.WORKLOADS["step_bf16_b8_v262144_d2816"], V=16384, d=512, B=2)
+case = GpuCase(w)
+outs = out_np(case.run_step(case.state()))
+np.savez(sys.argv[1], **outs)
+"""
+
+
+def test_pair_and_one_cta_self_conditioning_agree_bit_for_bit(tmp_path):
+    # the pair kernel issues the same MMAs in the same k order for every output element and
+    # promotes the same TMEM chunks: s, the samples and the confidences must be identical
+    res = {}
+    for tag, env in (("pair", {}), ("one", {"DS_SELFCOND_PAIR": "0"})):
+        path = tmp_path / f"{tag}.npz"
+        r = subprocess.run([sys.executable, "-c", _CHILD, str(path)], cwd=ROOT,
+                           env={**os.environ, **env}, capture_output=True, text=True, timeout=600)
+        assert r.returncode == 0, (r.stdout + r.stderr)[-3000:]
+        res[tag] = dict(np.load(path))
+    for k in res["pair"]:
+        assert np.array_equal(res["pair"][k], res["one"][k]), k
