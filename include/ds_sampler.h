@@ -36,6 +36,9 @@
  *     enqueued then. Errors found by a kernel (a bounded wait that ran out) set a device error
  *     word that ds_sampler_device_status reports. No call throws across the ABI.
  *   - One sampler must not be used from two streams at once (its workspace is shared).
+ *   - Launch shapes (the SM count and how many CTA pairs can be resident) are read once per
+ *     process, from the device that is current at the first call; samplers on GPUs of another
+ *     kind in the same process are not supported.
  */
 #ifndef DS_SAMPLER_H
 #define DS_SAMPLER_H
