@@ -55,7 +55,7 @@ extern "C" {
 typedef enum ds_status {
   DS_OK = 0,
   DS_ERR_INVALID_ARG = 1,  /* null pointer, bad size or bad enum value */
-  DS_ERR_UNSUPPORTED = 2,  /* valid request this build cannot serve (e.g. shape constraints) */
+  DS_ERR_UNSUPPORTED = 2,  /* valid request the library cannot serve (e.g. shape constraints) */
   DS_ERR_CUDA = 3,         /* a CUDA runtime call failed; the sampler may be unusable */
   DS_ERR_TIMEOUT = 4,      /* a kernel's bounded wait ran out (reported by device_status) */
   DS_ERR_OOM = 5,          /* workspace allocation failed */
