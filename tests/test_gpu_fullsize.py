@@ -37,10 +37,15 @@ def _sample_positions(g, b, n):
 
 
 @pytest.mark.parametrize("impl", ["auto", "fused"])
-@pytest.mark.parametrize("name,per_seq", [("step_bf16_b1_v262144_d2816", 12),
-                                          ("step_bf16_b8_v262144_d2816", 3)])
-def test_full_size_step(name, per_seq, impl):
+@pytest.mark.parametrize("name,per_seq,B", [("step_bf16_b1_v262144_d2816", 12, 1),
+                                            # two canvases: the race inside the paired
+                                            # self-conditioning launch over two row pairs
+                                            ("step_bf16_b8_v262144_d2816", 8, 2),
+                                            ("step_bf16_b8_v262144_d2816", 3, 8)])
+def test_full_size_step(name, per_seq, B, impl):
     w = W.WORKLOADS[name]
+    if B != w.B:
+        w = W.scaled(w, B=B)
     case = GpuCase(w, impl=impl)
     state = case.state()
     pre = state_np(state)
