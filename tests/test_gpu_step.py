@@ -374,21 +374,24 @@ def test_phase_timing_levels():
     sampler = case.sampler
     for _ in range(5):  # first launches of a fresh sampler are not representative
         case.run_step(case.state())
-    totals = {}
-    for level, coarse in ((1, False), (2, True)):
-        sampler.set_phase_timing(True, coarse=coarse)
-        for _ in range(20):
-            case.run_step(case.state())
-        ph, n = sampler.phase_times()
-        sampler.set_phase_timing(False)
-        assert n == 20
-        assert ph["logits"] > 0 and ph["selfcond"] > 0 and ph["convert"] > 0 and ph["lock"] > 0
-        if coarse:
-            assert ph["stats"] == 0 and ph["topk"] == 0 and ph["finalize"] == 0
-        else:
-            assert ph["stats"] > 0 and ph["finalize"] > 0
-        totals[level] = sum(ph.values()) / n
-    assert abs(totals[1] - totals[2]) <= 0.25 * totals[1]
+    # the steps here are ~0.1 ms, comparable to the host's time to enqueue one, so a host stall
+    # shows up in the event times: each level keeps the least of three 20-step passes
+    totals = {1: float("inf"), 2: float("inf")}
+    for _ in range(3):
+        for level, coarse in ((1, False), (2, True)):
+            sampler.set_phase_timing(True, coarse=coarse)
+            for _ in range(20):
+                case.run_step(case.state())
+            ph, n = sampler.phase_times()
+            sampler.set_phase_timing(False)
+            assert n == 20
+            assert ph["logits"] > 0 and ph["selfcond"] > 0 and ph["convert"] > 0 and ph["lock"] > 0
+            if coarse:
+                assert ph["stats"] == 0 and ph["topk"] == 0 and ph["finalize"] == 0
+            else:
+                assert ph["stats"] > 0 and ph["finalize"] > 0
+            totals[level] = min(totals[level], sum(ph.values()) / n)
+    assert abs(totals[1] - totals[2]) <= 0.25 * min(totals[1], totals[2])
     lib = C.load_library()
     assert lib.ds_sampler_set_phase_timing(sampler.handle, 3) == C.DS_ERR_INVALID_ARG
 
