@@ -654,6 +654,15 @@ __global__ void __launch_bounds__(kThreads) k_topk_row(const uint16_t* __restric
 // Per row: the sampled token, its confidence, the entropy and the argmax.
 // With Opart set, it also writes s for the row: the sum of the vocabulary-split partials in
 // split order, divided by the softmax normaliser.
+// POOL: the top-k selection over a pool of several chunks' candidates (the CUDA-core and
+// no-allocation top-k paths), whose per-thread arrays set the kernel's register count; without
+// it the kernel needs far fewer registers and more CTAs fit on an SM. NB: split partials a
+// thread requests at once — 16 where the rows fit in one wave anyway (the 13 splits of a canvas
+// in one round trip: latency decides), 8 where they take several (fewer registers, more CTAs:
+// occupancy decides). Same sums in the same order either way. Same box, finalize per step:
+// B = 1 0.0148–0.0156 against 0.0141–0.0145 ms with one kernel for every path (two CTAs an SM),
+// B = 2 0.020 against 0.041, B = 4 0.021 against 0.047, B = 8 0.039 against 0.096–0.099.
+template <bool POOL, int NB>
 __global__ void __launch_bounds__(kThreads) k_finalize(
     const RowStat* __restrict__ rs, const Best* __restrict__ best, const Cand* __restrict__ cand,
     int n_chunks, int k, int L, const uint8_t* __restrict__ done, const int32_t* __restrict__ step,
@@ -683,22 +692,41 @@ __global__ void __launch_bounds__(kThreads) k_finalize(
     float4* dst = reinterpret_cast<float4*>(s_out + (size_t)r * d);
     for (int q = threadIdx.x; q < d / 4; q += kThreads) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      // unrolled so that a thread's loads of the split partials are in flight together
-#pragma unroll 13
-      for (int sp = 0; sp < S; ++sp) {
-        const float4 t = src[sp * plane / 4 + q];
-        const float c = sh_sc[sp];
-        acc.x = fmaf(t.x, c, acc.x);
-        acc.y = fmaf(t.y, c, acc.y);
-        acc.z = fmaf(t.z, c, acc.z);
-        acc.w = fmaf(t.w, c, acc.w);
+      // the split partials are loaded NB at a time before they are summed (in split order), so
+      // that a thread's loads are in flight together
+      int sp = 0;
+      for (; sp + NB <= S; sp += NB) {
+        float4 t[NB];
+#pragma unroll
+        for (int u = 0; u < NB; ++u) t[u] = src[(sp + u) * plane / 4 + q];
+#pragma unroll
+        for (int u = 0; u < NB; ++u) {
+          const float c = sh_sc[sp + u];
+          acc.x = fmaf(t[u].x, c, acc.x);
+          acc.y = fmaf(t[u].y, c, acc.y);
+          acc.z = fmaf(t[u].z, c, acc.z);
+          acc.w = fmaf(t[u].w, c, acc.w);
+        }
       }
+      float4 t[NB];
+#pragma unroll
+      for (int u = 0; u < NB; ++u)
+        if (sp + u < S) t[u] = src[(sp + u) * plane / 4 + q];
+#pragma unroll
+      for (int u = 0; u < NB; ++u)
+        if (sp + u < S) {
+          const float c = sh_sc[sp + u];
+          acc.x = fmaf(t[u].x, c, acc.x);
+          acc.y = fmaf(t[u].y, c, acc.y);
+          acc.z = fmaf(t[u].z, c, acc.z);
+          acc.w = fmaf(t[u].w, c, acc.w);
+        }
       dst[q] = make_float4(acc.x / st.l, acc.y / st.l, acc.z / st.l, acc.w / st.l);
     }
   }
   float bv = -INFINITY, by = 0.f;
   int32_t bj = INT_MAX;
-  float cval;
+  float cval = 0.f;
   if (k == 0) {
     // Best::y is y at the winner, or y - m where Best::rel is 1
     for (int q = threadIdx.x; q < n_chunks; q += kThreads) {
@@ -731,7 +759,7 @@ __global__ void __launch_bounds__(kThreads) k_finalize(
     e_sum = block_sum(e_sum, shf);
     block_best(bv, bj, by, shv, shj, &shy);
     cval = expf(by - st.m) / e_sum;
-  } else {
+  } else if constexpr (POOL) {
     // The pool holds each chunk's candidates in token order, chunks in order, so pool order
     // is token order; element q of thread t is pool entry t + 256 q.
     constexpr int NP = kMaxTopKPool / kThreads;
@@ -1171,8 +1199,8 @@ void launch_finalize(const RowStat* rs, const Best* best, const Cand* cand, int 
                      int R, int L, const uint8_t* done, const int32_t* step, uint64_t seed,
                      const int32_t* blk, int32_t* sampled, float* conf, float* entropy,
                      int32_t* argmax, cudaStream_t st) {
-  launch_k(k_finalize, dim3(R), dim3(kThreads), 0, st, rs, best, cand, n_chunks, k, L, done, step,
-           seed, blk, sampled, conf, entropy, argmax, nullptr, 0, R, 0, nullptr, nullptr);
+  launch_finalize_with_s(rs, best, cand, n_chunks, k, R, L, done, step, seed, blk, sampled, conf,
+                         entropy, argmax, nullptr, 0, 0, nullptr, nullptr, st);
 }
 
 void launch_finalize_with_s(const RowStat* rs, const Best* best, const Cand* cand, int n_chunks,
@@ -1180,8 +1208,18 @@ void launch_finalize_with_s(const RowStat* rs, const Best* best, const Cand* can
                             uint64_t seed, const int32_t* blk, int32_t* sampled, float* conf,
                             float* entropy, int32_t* argmax, const float* Opart, int S, int d,
                             float* s, const float* mref, cudaStream_t st) {
-  launch_k(k_finalize, dim3(R), dim3(kThreads), 0, st, rs, best, cand, n_chunks, k, L, done, step,
-           seed, blk, sampled, conf, entropy, argmax, Opart, S, R, d, s, mref);
+  // rows in one wave at two CTAs an SM: the per-row latency decides, so all of a canvas's split
+  // partials are requested at once; more rows: occupancy decides (same sums in the same order)
+  const bool one_wave = R <= 2 * std::max(1, tc_num_sms());
+  if (k > 0 && n_chunks > 1)
+    launch_k(k_finalize<true, 8>, dim3(R), dim3(kThreads), 0, st, rs, best, cand, n_chunks, k, L,
+             done, step, seed, blk, sampled, conf, entropy, argmax, Opart, S, R, d, s, mref);
+  else if (one_wave)
+    launch_k(k_finalize<false, 16>, dim3(R), dim3(kThreads), 0, st, rs, best, cand, n_chunks, k,
+             L, done, step, seed, blk, sampled, conf, entropy, argmax, Opart, S, R, d, s, mref);
+  else
+    launch_k(k_finalize<false, 8>, dim3(R), dim3(kThreads), 0, st, rs, best, cand, n_chunks, k, L,
+             done, step, seed, blk, sampled, conf, entropy, argmax, Opart, S, R, d, s, mref);
 }
 
 void launch_gumbel_items(const uint16_t* Phi, const uint16_t* Plo, const ChunkStat* seg,
